@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs for the HeadTail ring-attention workloads.
+
+This module only draws random tensors and rounds them to their storage dtype.
+It holds none of the attention arithmetic, so both the CUDA path (tests,
+bench) and the CPU oracle can take their inputs from it without sharing any
+part of the method.
+
+Recipe (one per workload): q, k, v are i.i.d. Gaussian times ``qkv_std``; dO
+is i.i.d. standard Gaussian; draws come from one ``torch.Generator`` seeded
+with ``seed`` in the order q, k, v, dO, in fp32 on the CPU, then rounded
+round-to-nearest-even to the storage dtype. Rows at natural positions
+``>= T_valid`` (padding) keep their random q, k, v but get dO = 0, which is
+how a padded batch reaches the attention layer.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    T: int          # padded length, a multiple of 2*cp
+    T_valid: int    # real tokens; keys at positions >= T_valid are masked
+    H: int
+    d: int
+    cp: int         # virtual ring ranks; 2*cp HeadTail chunks of T/(2*cp)
+    causal: bool
+    rope: bool
+    dtype: str      # "f32" or "bf16": storage and input dtype of q, k, v, dO
+    qkv_std: float
+
+    @property
+    def chunk(self) -> int:
+        return self.T // (2 * self.cp)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return {"f32": torch.float32, "bf16": torch.bfloat16}[self.dtype]
+
+    def fwd_flops(self) -> float:
+        """Algorithmic forward flops: QK^T and PV over the live score pairs.
+
+        Causal counts half of the dense T_valid x T_valid square
+        (2 GEMMs x 2 flops x d per pair); non-causal counts all of it.
+        """
+        pairs = self.T_valid * self.T_valid * (0.5 if self.causal else 1.0)
+        return 4.0 * self.B * self.H * pairs * self.d
+
+    def fwdbwd_flops(self) -> float:
+        """Forward plus backward: the backward is counted as 5 GEMMs (2.5x forward)."""
+        return 3.5 * self.fwd_flops()
+
+
+# The five workloads of the benchmark description.
+WORKLOADS = {
+    "tiny_fp32": Workload("tiny_fp32", B=1, T=512, T_valid=512, H=4, d=64, cp=2,
+                          causal=True, rope=False, dtype="f32", qkv_std=1.0),
+    "gpt2_small": Workload("gpt2_small", B=4, T=4096, T_valid=4096, H=12, d=64, cp=4,
+                           causal=True, rope=True, dtype="bf16", qkv_std=0.5),
+    "long_16k": Workload("long_16k", B=1, T=16384, T_valid=16384, H=16, d=128, cp=2,
+                         causal=True, rope=True, dtype="bf16", qkv_std=0.5),
+    "window_32k": Workload("window_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
+                           causal=True, rope=True, dtype="bf16", qkv_std=0.5),
+    "padded_12289": Workload("padded_12289", B=2, T=12296, T_valid=12289, H=8, d=128, cp=4,
+                             causal=True, rope=True, dtype="bf16", qkv_std=0.5),
+}
+
+# Seeds: 1234 + the workload's position in the list above (1-based).
+SEEDS = {name: 1234 + i + 1 for i, name in enumerate(WORKLOADS)}
+
+
+def make_workload(name: str = "custom", *, B: int, T: int, H: int, d: int, cp: int,
+                  T_valid: int | None = None, causal: bool = True, rope: bool = False,
+                  dtype: str = "bf16", qkv_std: float = 0.5) -> Workload:
+    return Workload(name, B=B, T=T, T_valid=T if T_valid is None else T_valid, H=H, d=d,
+                    cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std)
+
+
+def make_inputs(w: Workload, seed: int) -> dict[str, torch.Tensor]:
+    """q, k, v, dO in natural token order, shape [B, H, T, d], CPU, storage dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    shape = (w.B, w.H, w.T, w.d)
+    out = {}
+    for name in ("q", "k", "v"):
+        out[name] = (torch.randn(shape, generator=g, dtype=torch.float32) * w.qkv_std).to(w.torch_dtype)
+    do = torch.randn(shape, generator=g, dtype=torch.float32)
+    if w.T_valid < w.T:
+        do[:, :, w.T_valid:, :] = 0.0
+    out["do"] = do.to(w.torch_dtype)
+    return out

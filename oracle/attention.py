@@ -1,0 +1,320 @@
+"""Float64 single-pass causal attention, its gradients, the LSE merge and the ring.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+What the pages fix, and where:
+
+* "BluScriptCP -- docs/Claude Logs.md", entry 2026-03-20 (ring attention with
+  an SDPA per step and an SDPAMerger), 2026-04-20 (global causal mask through
+  T_q / T_k / q_offset / k_offset), 2026-06-17 (the three step shapes of a
+  HeadTail ring: the 2c x 2c causal diagonal and two dense rectangles),
+  2026-03-24 (the backward's D correction), 2026-06-22 (dK/dV accumulate
+  across ring steps and return to their owner), 2026-05-07 and 2026-06-05
+  (a RoPE applied at local instead of global positions was a bug), 2026-06-29
+  (standard RoPE under HeadTail needs each token's global position).
+* "fix(cp): preserve gradients when sharding VLM inputs - #2931": sequences
+  are padded at the tail to a multiple of 2*cp before sharding; pad tokens
+  must not change the loss.
+
+Readings taken where the pages are silent (each is listed in the design
+notes): softmax scale 1/sqrt(d); LSE is the natural log of the sum of
+exponentials of the *scaled* scores; RoPE is the rotate-half pairing
+(i, i + d/2) with theta_i = 10000^(-2i/d) at the token's natural position;
+keys at positions >= T_valid are masked; the backward differentiates the
+loss sum(dO * O) of the single-pass result (final O and LSE).
+
+Everything here is a direct transcription of those definitions. A row's
+forward result depends on that row alone, so rows may be evaluated in groups
+(``_ROW_BLOCK``) to bound memory; no other blocking or reordering is done.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+from . import headtail
+
+_ROW_BLOCK = 1024
+ROPE_BASE = 10000.0
+
+
+def as_f64(x) -> np.ndarray:
+    """Accept numpy arrays or torch tensors (any float dtype) and return float64."""
+    if hasattr(x, "detach"):
+        x = x.detach().to("cpu").double().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+# ---------------------------------------------------------------- RoPE ----
+
+def rope_angles(positions: np.ndarray, d: int) -> np.ndarray:
+    """angle[p, i] = pos_p * theta_i, theta_i = base^(-2i/d), i in [0, d/2)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    theta = ROPE_BASE ** (-2.0 * i / d)
+    return np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+
+
+def rope(x: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    """Rotate-half RoPE of x[..., T, d] at the given per-row positions.
+
+    x'_i = x_i cos - x_{i+d/2} sin ;  x'_{i+d/2} = x_{i+d/2} cos + x_i sin.
+    """
+    d = x.shape[-1]
+    ang = rope_angles(positions, d)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., : d // 2], x[..., d // 2:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+def rope_transpose(g: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    """R(p)^T g: the adjoint of ``rope``, which carries a gradient back through it."""
+    d = g.shape[-1]
+    ang = rope_angles(positions, d)
+    c, s = np.cos(ang), np.sin(ang)
+    g1, g2 = g[..., : d // 2], g[..., d // 2:]
+    return np.concatenate([g1 * c + g2 * s, g2 * c - g1 * s], axis=-1)
+
+
+# ------------------------------------------------------- masked softmax ----
+
+def allowed(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool, T_valid: int) -> np.ndarray:
+    """allowed[a, b] = (not causal or k_pos[b] <= q_pos[a]) and k_pos[b] < T_valid."""
+    ok = np.broadcast_to(k_pos[None, :] < T_valid, (len(q_pos), len(k_pos))).copy()
+    if causal:
+        ok &= k_pos[None, :] <= q_pos[:, None]
+    return ok
+
+
+def partial_attention(qr: np.ndarray, kr: np.ndarray, vr: np.ndarray, q_pos: np.ndarray,
+                      k_pos: np.ndarray, causal: bool, T_valid: int):
+    """Softmax attention of query rows over a key set, with the global mask.
+
+    qr, kr are already rotated (if RoPE is on). Returns (O, LSE); a row with no
+    allowed key gets the merge identity (O = 0, LSE = -inf).
+    """
+    d = qr.shape[-1]
+    S = (qr @ kr.T) / math.sqrt(d)
+    ok = allowed(q_pos, k_pos, causal, T_valid)
+    S = np.where(ok, S, -np.inf)
+    m = S.max(axis=1, initial=-np.inf)
+    has = np.isfinite(m)
+    m_safe = np.where(has, m, 0.0)
+    E = np.exp(S - m_safe[:, None])                    # exp(-inf) = 0 on masked pairs
+    ssum = E.sum(axis=1)
+    lse = np.where(has, m_safe + np.log(np.where(has, ssum, 1.0)), -np.inf)
+    P = np.where(has[:, None], E / np.where(has, ssum, 1.0)[:, None], 0.0)
+    return P @ vr, lse
+
+
+def _heads(x):
+    x = as_f64(x)
+    B, H = x.shape[0], x.shape[1]
+    return x, B, H
+
+
+def _rotated(xh: np.ndarray, rope_on: bool) -> np.ndarray:
+    if not rope_on:
+        return xh
+    return rope(xh, np.arange(xh.shape[0]))
+
+
+def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool = False):
+    """Single-pass attention over natural-order [B, H, T, d] inputs.
+
+    Returns O [B, H, T, d] and LSE [B, H, T] (float64). RoPE, when on, is applied
+    to q and k at their natural (global) positions.
+    """
+    q, B, H = _heads(q)
+    k, v = as_f64(k), as_f64(v)
+    T = q.shape[2]
+    T_valid = T if T_valid is None else T_valid
+    pos = np.arange(T)
+    O = np.zeros_like(q)
+    L = np.zeros(q.shape[:3])
+    for b in range(B):
+        for h in range(H):
+            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, h], rope_on)
+            for r0 in range(0, T, _ROW_BLOCK):
+                rows = pos[r0:r0 + _ROW_BLOCK]
+                O[b, h, rows], L[b, h, rows] = partial_attention(
+                    qh[rows], kh, v[b, h], rows, pos, causal, T_valid)
+    return O, L
+
+
+def forward_rows(q, k, v, b: int, h: int, rows, causal: bool = True,
+                 T_valid: int | None = None, rope_on: bool = False):
+    """O and LSE of selected natural rows of one head (each row is independent)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    qh, kh, vh = as_f64(q[b, h]), as_f64(k[b, h]), as_f64(v[b, h])
+    T = kh.shape[0]
+    T_valid = T if T_valid is None else T_valid
+    qr = rope(qh[rows], rows) if rope_on else qh[rows]
+    kr = _rotated(kh, rope_on)
+    return partial_attention(qr, kr, vh, rows, np.arange(T), causal, T_valid)
+
+
+# ------------------------------------------------------------ backward ----
+
+def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
+    """Gradient of sum(dO * O) for one head, all rows (T x T matrices)."""
+    T, d = qh.shape
+    pos = np.arange(T)
+    qr, kr = _rotated(qh, rope_on), _rotated(kh, rope_on)
+    S = (qr @ kr.T) / math.sqrt(d)
+    ok = allowed(pos, pos, causal, T_valid)
+    P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lseh[:, None]), 0.0)
+    dV = P.T @ doh
+    dP = doh @ vh.T
+    D = np.sum(doh * oh, axis=1)
+    dS = P * (dP - D[:, None])
+    dQr = dS @ kr / math.sqrt(d)
+    dKr = dS.T @ qr / math.sqrt(d)
+    if rope_on:
+        return rope_transpose(dQr, pos), rope_transpose(dKr, pos), dV
+    return dQr, dKr, dV
+
+
+def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = None,
+             rope_on: bool = False):
+    """dq, dk, dv of the loss sum(dO * O), through RoPE if it is on.
+
+    o and lse are the single-pass forward results (float64). With P = exp(S - LSE):
+    dV = P^T dO;  dP = dO V^T;  D = rowsum(dO * O);  dS = P * (dP - D);
+    dQ' = dS K' / sqrt(d);  dK' = dS^T Q' / sqrt(d);  dq = R^T dQ', dk = R^T dK'.
+    """
+    q, B, H = _heads(q)
+    k, v, o, lse, do = (as_f64(x) for x in (k, v, o, lse, do))
+    T = q.shape[2]
+    T_valid = T if T_valid is None else T_valid
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h] = _backward_head(
+                q[b, h], k[b, h], v[b, h], o[b, h], lse[b, h], do[b, h], causal, T_valid, rope_on)
+    return dq, dk, dv
+
+
+def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
+                     T_valid: int | None = None, rope_on: bool = False):
+    """dq of selected natural rows of one head; each needs only its own row of P."""
+    rows = np.asarray(rows, dtype=np.int64)
+    kh, vh, doh = as_f64(k[b, h]), as_f64(v[b, h]), as_f64(do[b, h])
+    T, d = kh.shape
+    T_valid = T if T_valid is None else T_valid
+    o_r, lse_r = forward_rows(q, k, v, b, h, rows, causal, T_valid, rope_on)
+    qr = rope(as_f64(q[b, h])[rows], rows) if rope_on else as_f64(q[b, h])[rows]
+    kr = _rotated(kh, rope_on)
+    ok = allowed(rows, np.arange(T), causal, T_valid)
+    S = (qr @ kr.T) / math.sqrt(d)
+    P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lse_r[:, None]), 0.0)
+    dP = doh[rows] @ vh.T
+    D = np.sum(doh[rows] * o_r, axis=1)
+    dQr = (P * (dP - D[:, None])) @ kr / math.sqrt(d)
+    return rope_transpose(dQr, rows) if rope_on else dQr
+
+
+def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
+                       T_valid: int | None = None, rope_on: bool = False):
+    """dk, dv of selected natural key rows of one head.
+
+    Needs O and LSE of every query row of the head (computed here, row by row as
+    in ``forward``), then one column of P, dP and dS per selected key.
+    """
+    cols = np.asarray(cols, dtype=np.int64)
+    qh, kh, vh, doh = (as_f64(x[b, h]) for x in (q, k, v, do))
+    T, d = qh.shape
+    T_valid = T if T_valid is None else T_valid
+    pos = np.arange(T)
+    O = np.zeros_like(qh)
+    L = np.zeros(T)
+    qr, kr = _rotated(qh, rope_on), _rotated(kh, rope_on)
+    for r0 in range(0, T, _ROW_BLOCK):
+        rows = pos[r0:r0 + _ROW_BLOCK]
+        O[rows], L[rows] = partial_attention(qr[rows], kr, vh, rows, pos, causal, T_valid)
+    D = np.sum(doh * O, axis=1)
+    ok = allowed(pos, cols, causal, T_valid)            # [T, n_cols]
+    S = (qr @ kr[cols].T) / math.sqrt(d)
+    P = np.where(ok, np.exp(np.where(ok, S, 0.0) - L[:, None]), 0.0)
+    dV = P.T @ doh
+    dP = doh @ vh[cols].T
+    dS = P * (dP - D[:, None])
+    dKr = dS.T @ qr / math.sqrt(d)
+    return (rope_transpose(dKr, cols) if rope_on else dKr), dV
+
+
+# ---------------------------------------------------------- LSE merge ----
+
+def merge(o_a: np.ndarray, l_a: np.ndarray, o_b: np.ndarray, l_b: np.ndarray):
+    """SDPAMerger for two partials of the same rows.
+
+    L = m + log(e^{L_a - m} + e^{L_b - m}) with m = max(L_a, L_b);
+    O = e^{L_a - L} O_a + e^{L_b - L} O_b. (-inf, 0) is the identity, and two
+    empty partials give (-inf, 0).
+    """
+    l_a, l_b = np.asarray(l_a, np.float64), np.asarray(l_b, np.float64)
+    m = np.maximum(l_a, l_b)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    wa = np.where(np.isfinite(l_a), np.exp(l_a - m_safe), 0.0)
+    wb = np.where(np.isfinite(l_b), np.exp(l_b - m_safe), 0.0)
+    tot = wa + wb
+    L = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, tot)))
+    scale_a = np.where(empty, 0.0, wa / np.where(empty, 1.0, tot))
+    scale_b = np.where(empty, 0.0, wb / np.where(empty, 1.0, tot))
+    O = scale_a[..., None] * o_a + scale_b[..., None] * o_b
+    return O, L
+
+
+def merge_many(o_parts, l_parts):
+    """Left fold of ``merge`` over a list of partials, starting from the identity."""
+    O = np.zeros_like(np.asarray(o_parts[0], np.float64))
+    L = np.full(np.asarray(l_parts[0]).shape, -np.inf)
+    for o_s, l_s in zip(o_parts, l_parts):
+        O, L = merge(O, L, o_s, l_s)
+    return O, L
+
+
+# ---------------------------------------------------------------- ring ----
+
+def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = None,
+                 rope_on: bool = False):
+    """The ring schedule, stated step by step; returns natural-order O and LSE.
+
+    Virtual rank r holds HeadTail chunks r and 2cp-1-r. At ring step s it
+    holds the K/V of rank j = (r - s) mod cp (received from its predecessor),
+    attends its queries to those keys under the global causal mask, and merges
+    that partial into its running (O, LSE) with the SDPAMerger.
+    """
+    q, B, H = _heads(q)
+    k, v = as_f64(k), as_f64(v)
+    T = q.shape[2]
+    T_valid = T if T_valid is None else T_valid
+    O = np.zeros_like(q)
+    L = np.zeros(q.shape[:3])
+    for b in range(B):
+        for h in range(H):
+            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, h], rope_on)
+            for r in range(cp):
+                rows = headtail.rank_tokens(T, cp, r)
+                o_run = np.zeros((len(rows), q.shape[3]))
+                l_run = np.full(len(rows), -np.inf)
+                for s in range(cp):
+                    j = (r - s) % cp
+                    keys = headtail.rank_tokens(T, cp, j)
+                    o_s, l_s = partial_attention(qh[rows], kh[keys], v[b, h][keys], rows, keys,
+                                                 causal, T_valid)
+                    o_run, l_run = merge(o_run, l_run, o_s, l_s)
+                O[b, h, rows], L[b, h, rows] = o_run, l_run
+    return O, L
+
+
+def rank_causal_work(T: int, cp: int, causal: bool = True, T_valid: int | None = None) -> list[int]:
+    """Number of allowed (query, key) pairs whose query sits on each virtual rank."""
+    T_valid = T if T_valid is None else T_valid
+    pos = np.arange(T)
+    work = []
+    for r in range(cp):
+        rows = headtail.rank_tokens(T, cp, r)
+        work.append(int(allowed(rows, pos, causal, T_valid).sum()))
+    return work

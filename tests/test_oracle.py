@@ -1,0 +1,361 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+The pins are the pages' worked HeadTail example (tests/golden), brute-force
+softmax written with plain Python loops and complex-number RoPE, closed forms,
+scipy's softmax / logsumexp, the ring == single-pass invariant, the algebra of
+the LSE merge, and central finite differences of the analytic gradients. The
+"planted" tests feed deliberately wrong variants of oracle pieces to the same
+checks and require them to fail, so a plausible slip (a dropped term, a wrong
+sign, an off-by-one mask, a transposed operand) cannot pass unnoticed.
+"""
+from __future__ import annotations
+
+import cmath
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special
+
+from oracle import attention as A
+from oracle import headtail as HT
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(20261202)
+
+
+def rnd(*shape, std=1.0):
+    return rng.standard_normal(shape) * std
+
+
+# ------------------------------------------------------------ HeadTail ----
+
+def test_headtail_worked_example():
+    want = {}
+    with open(os.path.join(GOLDEN, "headtail_T8_cp2.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            r, toks = line.split(":")
+            want[int(r)] = [int(t) for t in toks.split()]
+    assert set(want) == {0, 1}
+    for r, toks in want.items():
+        assert list(HT.rank_tokens(8, 2, r)) == toks
+    pos = HT.positions_of_sharded_rows(8, 2)
+    assert list(pos) == want[0] + want[1]
+
+
+def _pairing_by_enumeration(T, cp):
+    """Independent construction: list the 2cp chunks, give rank r chunks r and 2cp-1-r."""
+    c = T // (2 * cp)
+    chunks = [list(range(i * c, (i + 1) * c)) for i in range(2 * cp)]
+    order = []
+    for r in range(cp):
+        order += chunks[r] + chunks[2 * cp - 1 - r]
+    return order
+
+
+@pytest.mark.parametrize("T,cp", [(8, 1), (8, 2), (24, 3), (64, 4), (48, 8), (30, 5)])
+def test_headtail_closed_form_and_bijection(T, cp):
+    sigma = HT.shard_index(T, cp)
+    assert sorted(sigma.tolist()) == list(range(T))               # bijection
+    assert HT.positions_of_sharded_rows(T, cp).tolist() == _pairing_by_enumeration(T, cp)
+    x = rnd(2, 3, T, 5)
+    assert np.array_equal(HT.unshard(HT.shard(x, cp), cp), x)     # round trip, bit-exact
+    if cp == 1:
+        assert np.array_equal(sigma, np.arange(T))                # cp=1 is the identity
+
+
+@pytest.mark.parametrize("T,cp", [(16, 2), (64, 4), (96, 3), (128, 8)])
+def test_headtail_balances_causal_work(T, cp):
+    work = A.rank_causal_work(T, cp)
+    assert len(set(work)) == 1, work
+    # and contiguous sharding would not: rank 0 of a contiguous split does least
+    c2 = T // cp
+    contiguous = [sum(t + 1 for t in range(r * c2, (r + 1) * c2)) for r in range(cp)]
+    assert cp == 1 or len(set(contiguous)) > 1
+
+
+def test_headtail_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        HT.shard_index(10, 2)
+
+
+# ---------------------------------------------------------------- RoPE ----
+
+def _rope_complex(x, positions):
+    """Textbook form: pair (x_i, x_{i+d/2}) as a complex number times e^{i p theta_i}."""
+    T, d = x.shape
+    out = np.empty_like(x)
+    for t in range(T):
+        for i in range(d // 2):
+            theta = 10000.0 ** (-2.0 * i / d)
+            z = complex(x[t, i], x[t, i + d // 2]) * cmath.exp(1j * positions[t] * theta)
+            out[t, i], out[t, i + d // 2] = z.real, z.imag
+    return out
+
+
+def check_rope(rope_fn, rope_t_fn):
+    x = rnd(9, 8)
+    pos = np.array([0, 1, 2, 5, 17, 100, 1000, 4097, 32767])
+    err = np.abs(rope_fn(x, pos) - _rope_complex(x, pos)).max()
+    y = rnd(9, 8)
+    # adjoint: <R x, y> == <x, R^T y>
+    err = max(err, abs(np.sum(rope_fn(x, pos) * y) - np.sum(x * rope_t_fn(y, pos))))
+    return err
+
+
+def test_rope_against_complex_rotation():
+    assert check_rope(A.rope, A.rope_transpose) < 1e-12
+
+
+def test_rope_properties():
+    x = rnd(6, 16)
+    pos = np.arange(6) * 7
+    assert np.allclose(np.linalg.norm(A.rope(x, pos), axis=1), np.linalg.norm(x, axis=1), atol=1e-12)
+    assert np.array_equal(A.rope(x, np.zeros(6)), x)                  # p = 0 is the identity
+    q, k = rnd(16), rnd(16)
+    for m, n, delta in [(5, 2, 11), (100, 99, 1000), (3, 30, 7)]:
+        a = A.rope(q[None], np.array([m])) @ A.rope(k[None], np.array([n])).T
+        b = A.rope(q[None], np.array([m + delta])) @ A.rope(k[None], np.array([n + delta])).T
+        assert abs(a - b).max() < 1e-10                              # relative position only
+    assert np.allclose(A.rope_transpose(A.rope(x, pos), pos), x, atol=1e-12)
+
+
+def test_planted_rope_sign_is_caught():
+    def bad_rope(x, positions):
+        d = x.shape[-1]
+        ang = A.rope_angles(positions, d)
+        c, s = np.cos(ang), np.sin(ang)
+        x1, x2 = x[..., : d // 2], x[..., d // 2:]
+        return np.concatenate([x1 * c + x2 * s, x2 * c - x1 * s], axis=-1)
+    assert check_rope(bad_rope, A.rope_transpose) > 1e-3
+
+
+# ------------------------------------------------------------- forward ----
+
+def brute_force_forward(q, k, v, causal, T_valid, rope_on):
+    """Plain Python loops, direct exp and sum with no max shift, complex RoPE."""
+    T, d = q.shape
+    if rope_on:
+        q, k = _rope_complex(q, np.arange(T)), _rope_complex(k, np.arange(T))
+    O = np.zeros((T, d))
+    L = np.zeros(T)
+    for t in range(T):
+        w = []
+        for j in range(T):
+            if (causal and j > t) or j >= T_valid:
+                w.append(0.0)
+            else:
+                w.append(math.exp(sum(q[t, i] * k[j, i] for i in range(d)) / math.sqrt(d)))
+        tot = sum(w)
+        L[t] = math.log(tot)
+        for i in range(d):
+            O[t, i] = sum(w[j] * v[j, i] for j in range(T)) / tot
+    return O, L
+
+
+def check_forward(fwd):
+    err = 0.0
+    for causal, T_valid, rope_on in [(True, 7, False), (False, 7, False), (True, 5, True),
+                                     (False, 6, True), (True, 7, True)]:
+        q, k, v = rnd(1, 1, 7, 6), rnd(1, 1, 7, 6), rnd(1, 1, 7, 6)
+        O, L = fwd(q, k, v, causal=causal, T_valid=T_valid, rope_on=rope_on)
+        Ob, Lb = brute_force_forward(q[0, 0], k[0, 0], v[0, 0], causal, T_valid, rope_on)
+        err = max(err, np.abs(O[0, 0] - Ob).max(), np.abs(L[0, 0] - Lb).max())
+    return err
+
+
+def test_forward_against_brute_force():
+    assert check_forward(A.forward) < 1e-12
+
+
+def test_planted_forward_mistakes_are_caught(monkeypatch):
+    real_allowed = A.allowed
+
+    def strict_causal(q_pos, k_pos, causal, T_valid):   # j < t instead of j <= t
+        ok = real_allowed(q_pos, k_pos, causal, T_valid)
+        if causal:
+            ok &= k_pos[None, :] != q_pos[:, None]
+        return ok
+    monkeypatch.setattr(A, "allowed", strict_causal)
+    with np.errstate(all="ignore"):
+        assert not check_forward(A.forward) < 1e-6
+    monkeypatch.setattr(A, "allowed", real_allowed)
+
+    def no_pad_mask(q_pos, k_pos, causal, T_valid):
+        return real_allowed(q_pos, k_pos, causal, 10 ** 9)
+    monkeypatch.setattr(A, "allowed", no_pad_mask)
+    assert not check_forward(A.forward) < 1e-6
+    monkeypatch.setattr(A, "allowed", real_allowed)
+
+    real_pa = A.partial_attention
+
+    def transposed_v(qr, kr, vr, q_pos, k_pos, causal, T_valid):
+        return real_pa(qr, kr, vr[::-1], q_pos, k_pos, causal, T_valid)
+    monkeypatch.setattr(A, "partial_attention", transposed_v)
+    assert not check_forward(A.forward) < 1e-6
+
+
+def test_forward_closed_forms():
+    T, d = 12, 8
+    q, k, v = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, causal=True)
+    # row 0 sees only key 0
+    assert np.allclose(O[:, :, 0], v[:, :, 0], atol=1e-14)
+    assert np.allclose(L[:, :, 0], np.sum(q[:, :, 0] * k[:, :, 0], -1) / math.sqrt(d), atol=1e-14)
+    # k == 0: uniform weights over the causal prefix
+    O0, L0 = A.forward(q, np.zeros_like(k), v, causal=True)
+    prefix_mean = np.cumsum(v, axis=2) / np.arange(1, T + 1)[None, None, :, None]
+    assert np.allclose(O0, prefix_mean, atol=1e-13)
+    assert np.allclose(L0, np.log(np.arange(1, T + 1))[None, None], atol=1e-13)
+    # v constant: every row returns it
+    u = rnd(d)
+    Ou, _ = A.forward(q, k, np.broadcast_to(u, v.shape), causal=True)
+    assert np.allclose(Ou, np.broadcast_to(u, v.shape), atol=1e-13)
+
+
+def test_noncausal_matches_scipy_softmax():
+    T, d = 33, 16
+    q, k, v = rnd(2, 1, T, d), rnd(2, 1, T, d), rnd(2, 1, T, d)
+    O, L = A.forward(q, k, v, causal=False)
+    for b in range(2):
+        S = q[b, 0] @ k[b, 0].T / math.sqrt(d)
+        assert np.allclose(O[b, 0], special.softmax(S, axis=1) @ v[b, 0], atol=1e-13)
+        assert np.allclose(L[b, 0], special.logsumexp(S, axis=1), atol=1e-13)
+
+
+def test_forward_rows_matches_full():
+    q, k, v = rnd(1, 2, 40, 8), rnd(1, 2, 40, 8), rnd(1, 2, 40, 8)
+    O, L = A.forward(q, k, v, causal=True, T_valid=37, rope_on=True)
+    rows = [0, 3, 17, 36, 39]
+    o_r, l_r = A.forward_rows(q, k, v, 0, 1, rows, True, 37, True)
+    assert np.allclose(o_r, O[0, 1, rows], atol=1e-13) and np.allclose(l_r, L[0, 1, rows], atol=1e-13)
+
+
+# ---------------------------------------------------------- ring + merge ----
+
+@pytest.mark.parametrize("cp", [1, 2, 4, 8])
+@pytest.mark.parametrize("causal,T_valid,rope_on", [(True, 64, False), (True, 59, True),
+                                                    (False, 64, True)])
+def test_ring_equals_single_pass(cp, causal, T_valid, rope_on):
+    T, d = 64, 8
+    q, k, v = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, causal, T_valid, rope_on)
+    Or, Lr = A.ring_forward(q, k, v, cp, causal, T_valid, rope_on)
+    assert np.abs(O - Or).max() <= 1e-12 and np.abs(L - Lr).max() <= 1e-12
+
+
+def test_merge_algebra():
+    n, d = 10, 5
+    parts = [(rnd(n, d), rnd(n)) for _ in range(3)]
+    parts[1][1][2] = -np.inf                                  # one empty partial row
+    (oa, la), (ob, lb), (oc, lc) = parts
+    left = A.merge(*A.merge(oa, la, ob, lb), oc, lc)
+    right = A.merge(oa, la, *A.merge(ob, lb, oc, lc))
+    assert np.abs(left[0] - right[0]).max() <= 1e-13 and np.abs(left[1] - right[1]).max() <= 1e-13
+    ab, ba = A.merge(oa, la, ob, lb), A.merge(ob, lb, oa, la)
+    assert np.abs(ab[0] - ba[0]).max() <= 1e-13 and np.abs(ab[1] - ba[1]).max() <= 1e-13
+    ident = A.merge(oa, la, np.zeros((n, d)), np.full(n, -np.inf))
+    assert np.abs(ident[0] - oa).max() <= 1e-15 and np.abs(ident[1] - la).max() <= 1e-15
+    empty = A.merge(np.zeros((n, d)), np.full(n, -np.inf), np.zeros((n, d)), np.full(n, -np.inf))
+    assert np.all(empty[1] == -np.inf) and np.all(empty[0] == 0)
+    # merge of two disjoint key sets == softmax over their union (scipy)
+    d2 = 6
+    q, k, v = rnd(4, d2), rnd(9, d2), rnd(9, d2)
+    S = q @ k.T / math.sqrt(d2)
+    pa = A.partial_attention(q, k[:4], v[:4], np.full(4, 100), np.arange(4), False, 100)
+    pb = A.partial_attention(q, k[4:], v[4:], np.full(4, 100), np.arange(4, 9), False, 100)
+    Om, Lm = A.merge(*pa, *pb)
+    assert np.allclose(Om, special.softmax(S, axis=1) @ v, atol=1e-13)
+    assert np.allclose(Lm, special.logsumexp(S, axis=1), atol=1e-13)
+
+
+# ------------------------------------------------------------ backward ----
+
+def check_gradients_fd(bwd, causal, T_valid, rope_on, h=1e-6):
+    """Max relative error of analytic grads against central finite differences."""
+    T, d = 6, 4
+    q, k, v, do = rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d)
+
+    def loss(q_, k_, v_):
+        O, _ = A.forward(q_, k_, v_, causal, T_valid, rope_on)
+        return np.sum(do * O)
+
+    O, L = A.forward(q, k, v, causal, T_valid, rope_on)
+    grads = bwd(q, k, v, O, L, do, causal, T_valid, rope_on)
+    worst = 0.0
+    for which, g in enumerate(grads):
+        fd = np.zeros_like(g)
+        for idx in np.ndindex(g.shape):
+            args_p = [q.copy(), k.copy(), v.copy()]
+            args_m = [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        worst = max(worst, np.abs(g - fd).max() / max(np.abs(fd).max(), 1e-3))
+    return worst
+
+
+@pytest.mark.parametrize("causal,T_valid,rope_on", [(True, 6, False), (True, 6, True),
+                                                    (False, 6, True), (True, 4, True)])
+def test_backward_against_finite_differences(causal, T_valid, rope_on):
+    assert check_gradients_fd(A.backward, causal, T_valid, rope_on) <= 1e-6
+
+
+def test_planted_backward_mistakes_are_caught(monkeypatch):
+    real = A._backward_head
+
+    def no_D(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):   # drops the D term
+        return real(qh, kh, vh, np.zeros_like(oh), lseh, doh, causal, T_valid, rope_on)
+    monkeypatch.setattr(A, "_backward_head", no_D)
+    assert check_gradients_fd(A.backward, True, 6, False) > 1e-3
+
+    def no_rope_adjoint(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
+        dq, dk, dv = real(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on)
+        pos = np.arange(qh.shape[0])
+        return A.rope(A.rope(dq, pos), pos), dk, dv                     # R instead of R^T
+    monkeypatch.setattr(A, "_backward_head", no_rope_adjoint)
+    assert check_gradients_fd(A.backward, True, 6, True) > 1e-3
+
+
+def test_backward_invariants():
+    T, d = 20, 8
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, True)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True)
+    # softmax rows sum to one: sum_j dV_j = sum_t dO_t
+    assert np.allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+    # sum_j dS_tj = 0 per row, so without RoPE sum_j dK_j = 0
+    assert np.abs(dk.sum(axis=2)).max() < 1e-12
+
+
+def test_sampled_backward_matches_full():
+    T, d = 48, 8
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    do[:, :, 45:] = 0
+    O, L = A.forward(q, k, v, True, 45, True)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, 45, True)
+    rows = [0, 1, 30, 44, 47]
+    assert np.allclose(A.backward_dq_rows(q, k, v, do, 0, 1, rows, True, 45, True), dq[0, 1, rows],
+                       atol=1e-12)
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 0, 1, rows, True, 45, True)
+    assert np.allclose(dk_c, dk[0, 1, rows], atol=1e-12)
+    assert np.allclose(dv_c, dv[0, 1, rows], atol=1e-12)
+
+
+# ------------------------------------------------------------- padding ----
+
+def test_padding_is_invisible_to_real_rows():
+    Tr, Tp, d = 13, 16, 8
+    q, k, v, do = rnd(1, 2, Tp, d), rnd(1, 2, Tp, d), rnd(1, 2, Tp, d), rnd(1, 2, Tp, d)
+    do[:, :, Tr:] = 0
+    Op, Lp = A.forward(q, k, v, True, Tr, True)
+    Ou, Lu = A.forward(q[:, :, :Tr], k[:, :, :Tr], v[:, :, :Tr], True, Tr, True)
+    assert np.abs(Op[:, :, :Tr] - Ou).max() < 1e-13 and np.abs(Lp[:, :, :Tr] - Lu).max() < 1e-13
+    gp = A.backward(q, k, v, Op, Lp, do, True, Tr, True)
+    gu = A.backward(q[:, :, :Tr], k[:, :, :Tr], v[:, :, :Tr], Ou, Lu, do[:, :, :Tr], True, Tr, True)
+    for a, b in zip(gp, gu):
+        assert np.abs(a[:, :, :Tr] - b).max() < 1e-13
+        assert np.all(a[:, :, Tr:] == 0.0)                 # pad-row grads are exactly zero
