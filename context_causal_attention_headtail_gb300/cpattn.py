@@ -1,0 +1,176 @@
+"""Thin ctypes binding of libcpattn's C ABI (include/cpattn.h).
+
+The ``cpattn_*`` functions here have the C names and arguments (device
+pointers as Python ints, sizes, a stream handle) and do nothing but
+marshalling. ``shard``, ``fwd``, ``bwd`` ... below them only read pointers and
+sizes off torch tensors and call those functions; every step of the
+computation runs in the library's CUDA kernels. There is no fallback: if the
+shared library is missing or a call fails, a ``CpattnError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcpattn.so")
+
+OK, ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPORTED = range(8)
+F32, BF16 = 0, 1
+
+# Every symbol the header declares.
+EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_index", "cpattn_fwd",
+           "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
+           "cpattn_sync_status", "cpattn_version")
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"cpattn status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+_c = ctypes
+_vp, _i, _sz = _c.c_void_p, _c.c_int, _c.c_size_t
+
+
+def _declare(lib):
+    sig = {
+        "cpattn_shard": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_unshard": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_shard_index": [_i, _i, _c.POINTER(_c.c_int32)],
+        "cpattn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
+        "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
+        "cpattn_sync_status": [_vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _i
+    lib.cpattn_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i]
+    lib.cpattn_bwd_workspace_bytes.restype = _sz
+    lib.cpattn_last_error.argtypes = []
+    lib.cpattn_last_error.restype = _c.c_char_p
+    lib.cpattn_version.argtypes = []
+    lib.cpattn_version.restype = _c.c_char_p
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise CpattnError(ERR_UNSUPPORTED, f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        _declare(handle)
+        _lib = handle
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise CpattnError(status, lib().cpattn_last_error().decode(errors="replace"))
+
+
+# ------------------------------------------------------- C-named entry points
+
+def cpattn_shard(src, dst, B, H, T, d, cp, dt, stream=None):
+    _check(lib().cpattn_shard(src, dst, B, H, T, d, cp, dt, stream))
+
+
+def cpattn_unshard(src, dst, B, H, T, d, cp, dt, stream=None):
+    _check(lib().cpattn_unshard(src, dst, B, H, T, d, cp, dt, stream))
+
+
+def cpattn_shard_index(T, cp):
+    buf = (ctypes.c_int32 * T)()
+    _check(lib().cpattn_shard_index(T, cp, buf))
+    return list(buf)
+
+
+def cpattn_fwd(q, k, v, o, lse, B, T, T_valid, H, d, cp, causal, rope, dt, stream=None):
+    _check(lib().cpattn_fwd(q, k, v, o, lse, B, T, T_valid, H, d, cp, causal, rope, dt, stream))
+
+
+def cpattn_bwd_workspace_bytes(B, T, H, d):
+    return int(lib().cpattn_bwd_workspace_bytes(B, T, H, d))
+
+
+def cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, cp, causal, rope,
+               dt, stream=None):
+    _check(lib().cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, cp,
+                            causal, rope, dt, stream))
+
+
+def cpattn_merge(o_parts, lse_parts, o, lse, B, H, T, d, dt, stream=None):
+    n = len(o_parts)
+    po = (ctypes.c_void_p * n)(*o_parts)
+    pl = (ctypes.c_void_p * n)(*lse_parts)
+    _check(lib().cpattn_merge(po, pl, n, o, lse, B, H, T, d, dt, stream))
+
+
+def cpattn_sync_status(stream=None):
+    _check(lib().cpattn_sync_status(stream))
+
+
+def cpattn_last_error():
+    return lib().cpattn_last_error().decode(errors="replace")
+
+
+def cpattn_version():
+    return lib().cpattn_version().decode()
+
+
+# ------------------------------------------------------ tensor conveniences
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise CpattnError(ERR_DTYPE, f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ptr(t):
+    if not t.is_cuda or not t.is_contiguous():
+        raise CpattnError(ERR_ARG, "tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def shard(src, dst, cp, stream=None):
+    B, H, T, d = src.shape
+    cpattn_shard(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+
+
+def unshard(src, dst, cp, stream=None):
+    B, H, T, d = src.shape
+    cpattn_unshard(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+
+
+def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None):
+    B, H, T, d = q.shape
+    cpattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, T if T_valid is None else T_valid,
+               H, d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
+
+
+def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=True, rope=False,
+        stream=None):
+    B, H, T, d = q.shape
+    cpattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+               _ptr(dv), _ptr(workspace), B, T, T if T_valid is None else T_valid, H, d, cp,
+               int(causal), int(rope), _dtype_code(q), _stream(stream))
+
+
+def merge(o_parts, lse_parts, o, lse, stream=None):
+    B, H, T, d = o.shape
+    cpattn_merge([_ptr(x) for x in o_parts], [_ptr(x) for x in lse_parts], _ptr(o), _ptr(lse),
+                 B, H, T, d, _dtype_code(o), _stream(stream))

@@ -1,0 +1,261 @@
+// C-ABI entry points of libcpattn: argument validation and dispatch. Every
+// step of the computation runs in the kernels of the other translation units.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace cpattn {
+
+static thread_local char g_msg[512] = "";
+
+cpattn_status fail(cpattn_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+cpattn_status check_launch(const char *what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(CPATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return CPATTN_OK;
+}
+
+// One flag per device, written by kernels whose bounded waits expire.
+__device__ int g_err_flag;
+
+int *device_err_flag() {
+  static std::mutex mu;
+  static int *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_flag) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int *>(p);
+  }
+  return addr[dev];
+}
+
+void make_rope_theta(int d, RopeTheta *t) {
+  for (int i = 0; i < 64; ++i) {
+    double th = (2 * i < d) ? pow(10000.0, -2.0 * i / d) : 0.0;
+    float hi = (float)th;
+    t->hi[i] = hi;
+    t->lo[i] = (float)(th - (double)hi);
+  }
+}
+
+EncodeTiledFn encode_tiled_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace cpattn
+
+using namespace cpattn;
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static cpattn_status check_common(int B, int H, int T, int d, int cp) {
+  if (B < 1 || H < 1 || T < 1 || d < 1 || cp < 1)
+    return fail(CPATTN_ERR_SHAPE, "sizes must be >= 1 (B=%d H=%d T=%d d=%d cp=%d)", B, H, T, d, cp);
+  if (T % (2 * cp) != 0)
+    return fail(CPATTN_ERR_SHAPE, "T=%d is not a multiple of 2*cp=%d (pad the tail first)", T, 2 * cp);
+  if ((long long)B * H * T > (1LL << 31) - 1)
+    return fail(CPATTN_ERR_SHAPE, "B*H*T too large");
+  return CPATTN_OK;
+}
+
+static cpattn_status check_attn(int B, int T, int T_valid, int H, int d, int cp, int causal,
+                                int rope, cpattn_dtype dt) {
+  cpattn_status st = check_common(B, H, T, d, cp);
+  if (st != CPATTN_OK) return st;
+  if (d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: only 64 and 128 are supported", d);
+  if (T_valid < 1 || T_valid > T)
+    return fail(CPATTN_ERR_SHAPE, "T_valid=%d must be in [1, T=%d]", T_valid, T);
+  if ((causal != 0 && causal != 1) || (rope != 0 && rope != 1))
+    return fail(CPATTN_ERR_ARG, "causal and rope must be 0 or 1");
+  if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (T > (1 << 24)) return fail(CPATTN_ERR_SHAPE, "T=%d exceeds 2^24", T);
+  return CPATTN_OK;
+}
+
+static Geometry geometry(int B, int H, int T, int T_valid, int d, int cp, int causal, int rope) {
+  Geometry g;
+  g.B = B; g.H = H; g.T = T; g.T_valid = T_valid; g.d = d; g.cp = cp;
+  g.c = T / (2 * cp); g.causal = causal; g.rope = rope;
+  return g;
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+extern "C" {
+
+const char *cpattn_last_error(void) { return g_msg; }
+
+const char *cpattn_version(void) { return "cpattn 0.1 sm_103a"; }
+
+cpattn_status cpattn_sync_status(cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(CPATTN_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  int *flag = device_err_flag();
+  if (!flag) return fail(CPATTN_ERR_CUDA, "cannot resolve the device error flag");
+  int v = 0;
+  if (cudaMemcpy(&v, flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(CPATTN_ERR_CUDA, "reading the device error flag failed");
+  if (v != 0) {
+    int zero = 0;
+    cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (v & ERR_FLAG_TIMEOUT)
+      return fail(CPATTN_ERR_TIMEOUT, "a kernel's bounded wait expired (flag=%d)", v);
+    return fail(CPATTN_ERR_CUDA, "device error flag=%d", v);
+  }
+  return CPATTN_OK;
+}
+
+cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host) {
+  g_msg[0] = 0;
+  if (!idx_host) return fail(CPATTN_ERR_ARG, "idx_host is NULL");
+  cpattn_status st = check_common(1, 1, T, 1, cp);
+  if (st != CPATTN_OK) return st;
+  const int c = T / (2 * cp);
+  for (int t = 0; t < T; ++t) {
+    int kappa = t / c, o = t % c;
+    idx_host[t] = kappa < cp ? 2 * c * kappa + o : 2 * c * (2 * cp - 1 - kappa) + c + o;
+  }
+  return CPATTN_OK;
+}
+
+static cpattn_status shard_common(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                  cpattn_dtype dt, cpattn_stream_t stream, bool inverse) {
+  g_msg[0] = 0;
+  if (!src || !dst) return fail(CPATTN_ERR_ARG, "null pointer");
+  cpattn_status st = check_common(B, H, T, d, cp);
+  if (st != CPATTN_OK) return st;
+  if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  const int elt = dt == CPATTN_F32 ? 4 : 2;
+  if ((d * elt) % 16 != 0) return fail(CPATTN_ERR_ALIGN, "row of d*elt=%d bytes is not a multiple of 16", d * elt);
+  if (!aligned16(src) || !aligned16(dst)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t bytes = (size_t)B * H * T * d * elt;
+  if (overlaps(src, bytes, dst, bytes)) return fail(CPATTN_ERR_ARG, "src and dst overlap");
+  Geometry g = geometry(B, H, T, T, d, cp, 1, 0);
+  return launch_shard(src, dst, g, elt, inverse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cpattn_status cpattn_shard(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                           cpattn_dtype dt, cpattn_stream_t stream) {
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, false);
+}
+
+cpattn_status cpattn_unshard(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                             cpattn_dtype dt, cpattn_stream_t stream) {
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, true);
+}
+
+cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int T, int T_valid, int H, int d, int cp, int causal, int rope,
+                         cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
+  cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
+  if (st != CPATTN_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t elt = dt == CPATTN_F32 ? 4 : 2;
+  const size_t tb = (size_t)B * H * T * d * elt;
+  if (overlaps(o, tb, q, tb) || overlaps(o, tb, k, tb) || overlaps(o, tb, v, tb) ||
+      overlaps(lse, (size_t)B * H * T * 4, o, tb))
+    return fail(CPATTN_ERR_ARG, "outputs overlap inputs");
+  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == CPATTN_F32)
+    return launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                          static_cast<const float *>(v), static_cast<float *>(o), lse, g, s);
+  return launch_fwd_bf16(q, k, v, o, lse, g, s);
+}
+
+size_t cpattn_bwd_workspace_bytes(int B, int T, int H, int d) {
+  (void)d;
+  if (B < 1 || T < 1 || H < 1) return 0;
+  size_t rows = (size_t)B * H * T;
+  return ((rows * sizeof(float) + 255) / 256) * 256;   // D = rowsum(dO * O), fp32
+}
+
+cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                         void *workspace, int B, int T, int T_valid, int H, int d, int cp,
+                         int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
+    return fail(CPATTN_ERR_ARG, "null pointer");
+  cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
+  if (st != CPATTN_OK) return st;
+  const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, workspace};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t elt = dt == CPATTN_F32 ? 4 : 2;
+  const size_t tb = (size_t)B * H * T * d * elt;
+  const size_t wb = cpattn_bwd_workspace_bytes(B, T, H, d);
+  const void *outs[] = {dq, dk, dv};
+  const void *ins[] = {q, k, v, o, dO};
+  for (const void *a : outs) {
+    for (const void *b : ins)
+      if (overlaps(a, tb, b, tb)) return fail(CPATTN_ERR_ARG, "gradient outputs overlap inputs");
+    for (const void *b : outs)
+      if (a != b && overlaps(a, tb, b, tb)) return fail(CPATTN_ERR_ARG, "gradient outputs overlap");
+    if (overlaps(a, tb, workspace, wb)) return fail(CPATTN_ERR_ARG, "workspace overlaps outputs");
+  }
+  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float *D = static_cast<float *>(workspace);
+  st = launch_bwd_preprocess(o, dO, D, (long long)B * H * T, d, dt, s);
+  if (st != CPATTN_OK) return st;
+  if (dt == CPATTN_F32)
+    return launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                          static_cast<const float *>(v), static_cast<const float *>(o), lse,
+                          static_cast<const float *>(dO), static_cast<float *>(dq),
+                          static_cast<float *>(dk), static_cast<float *>(dv), D, g, s);
+  return launch_bwd_bf16(q, k, v, o, lse, dO, dq, dk, dv, D, g, s);
+}
+
+cpattn_status cpattn_merge(const float *const *o_parts, const float *const *lse_parts, int n,
+                           void *o, float *lse, int B, int H, int T, int d, cpattn_dtype dt,
+                           cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!o_parts || !lse_parts || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
+  if (n < 1 || n > 16) return fail(CPATTN_ERR_ARG, "n=%d must be in [1, 16]", n);
+  if (B < 1 || H < 1 || T < 1) return fail(CPATTN_ERR_SHAPE, "sizes must be >= 1");
+  if (d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: only 64 and 128 are supported", d);
+  if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  for (int i = 0; i < n; ++i) {
+    if (!o_parts[i] || !lse_parts[i]) return fail(CPATTN_ERR_ARG, "null partial pointer %d", i);
+    if (!aligned16(o_parts[i]) || !aligned16(lse_parts[i]))
+      return fail(CPATTN_ERR_ALIGN, "partial %d not 16-byte aligned", i);
+  }
+  if (!aligned16(o) || !aligned16(lse)) return fail(CPATTN_ERR_ALIGN, "outputs must be 16-byte aligned");
+  return launch_merge(o_parts, lse_parts, n, o, lse, (long long)B * H * T, d, dt,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,380 @@
+// Ring attention forward on tcgen05 tensor cores (bf16 in, fp32 accumulate).
+//
+// One CTA owns one 128-row query tile of one (b,h): a tile of virtual rank r's
+// head or tail chunk. It walks the K/V tiles the ring would bring to rank r,
+// step by step (j = (r - s) mod cp, head then tail chunk), skipping tiles that
+// lie wholly above the shifted causal diagonal (Claude Logs, 2026-04-20 and
+// 2026-06-17). The online-softmax update at each tile boundary is the
+// SDPAMerger rule applied to the running (O, m, l) and the new tile's
+// partial, so at every ring-step boundary the running state equals the merge
+// of the steps seen so far (Claude Logs, 2026-03-20).
+//
+// Warp roles (NT threads):
+//   warps 0-3  softmax: thread i owns query row i = TMEM lane i. Reads S from
+//              TMEM, masks, keeps (m, l), writes P (bf16) back into TMEM over
+//              S, rescales O in TMEM when the row max grows by > 2^8, and
+//              writes O and LSE at the end.
+//   warp 4     TMA producer (lane 0) and TMEM allocator (whole warp).
+//   warp 5     MMA issuer (lane 0): S = Q K^T (A, B from smem), O += P V
+//              (A = P from TMEM, B = V from smem, MN-major).
+//   warps 6-9  (RoPE only) rotate the Q tile once and every K tile in smem.
+// TMEM columns: S/P buffer 0 at 0, buffer 1 at 128, O at 256 (512 allocated).
+#include <math.h>
+
+#include "attn_common.cuh"
+
+namespace cpattn {
+namespace {
+
+struct FwdParams {
+  __nv_bfloat16 *o;
+  float *lse;
+  int *err;
+  int BH, T, T_valid, c, cp, causal, tpc;
+  float scale_log2;  // log2(e) / sqrt(d)
+  RopeTheta theta;
+};
+
+template <int D>
+struct FwdCfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;    // K/V pipeline stages
+  static constexpr int TILE = kTile * D * 2;       // bytes of one 128 x D bf16 tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // barriers: q_full, q_ready, fin, o_done, s_full[2], p_full[2], kv_full[NS], k_ready[NS], kv_empty[NS]
+  static constexpr int NBAR = 8 + 3 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;  // + alignment slack
+};
+
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kTmemCols = 512;
+
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q;
+  auto sK = [&](int st) { return sbase + C::OFF_K + st * C::TILE; };
+  auto sV = [&](int st) { return sbase + C::OFF_V + st * C::TILE; };
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_q_full = bar0, bar_q_ready = bar0 + 8, bar_fin = bar0 + 16, bar_o_done = bar0 + 24;
+  auto bar_s_full = [&](int b) { return bar0 + 32 + 8 * b; };
+  auto bar_p_full = [&](int b) { return bar0 + 48 + 8 * b; };
+  auto bar_kv_full = [&](int st) { return bar0 + 64 + 8 * st; };
+  auto bar_k_ready = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  auto bar_kv_empty = [&](int st) { return bar0 + 64 + 16 * NS + 8 * st; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- which query tile: heaviest (latest natural position) first, heads interleaved
+  const int cp = p.cp, c = p.c, tpc = p.tpc;
+  const int bh = blockIdx.x % p.BH;
+  const int g = blockIdx.x / p.BH;
+  const int kq = 2 * cp - 1 - g / tpc;
+  const int qt = tpc - 1 - g % tpc;
+  int rq, hq;
+  owner_of(kq, cp, rq, hq);
+  const int q_z = bh * 2 * cp + 2 * rq + hq;
+  const int q_pos0 = kq * c + qt * kTile;
+  const int q_rows = min(kTile, c - qt * kTile);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const uint32_t b = bar0 + 8 * i;
+      bool by_threads = b == bar_q_ready || b == bar_p_full(0) || b == bar_p_full(1);
+      for (int st = 0; st < NS; ++st) by_threads |= b == bar_k_ready(st);
+      tc::mbar_init(b, by_threads ? 128 : 1);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;   // never set: lets teardown waits honour only the time limit
+    tc::mbar_fence_init();
+  }
+  if (warp == 4) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const tc::WaitCtx wc{abort_flag, p.err};
+
+  KvSchedule sched;
+  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
+  TileInfo t;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_q);
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+      tc::mbar_arrive_expect_tx(bar_q_full, C::TILE);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tc::tma_load_3d(sQ + blk * kTile * 128, &tm_q, bar_q_full, blk * 64, qt * kTile, q_z);
+      int n = 0;
+      while (sched.next(t)) {
+        const int st = n % NS;
+        if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
+        tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
+        const int z = bh * 2 * cp + t.slot;
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_kv_full(st), blk * 64, t.y0, z);
+          tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_kv_full(st), blk * 64, t.y0, z);
+        }
+        ++n;
+      }
+      // Let every issued copy land before the CTA can exit.
+      const tc::WaitCtx drain{abort_flag + 1, p.err};
+      tc::mbar_wait(bar_q_full, 0, drain);
+      for (int m = (n > NS ? n - NS : 0); m < n; ++m) tc::mbar_wait(bar_kv_full(m % NS), (m / NS) & 1, drain);
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = tc::idesc_bf16(128, D, false, true);
+      bool ok = tc::mbar_wait(ROPE ? bar_q_ready : bar_q_full, 0, wc);
+      auto issue_s = [&](int n) -> bool {
+        const int st = n % NS;
+        if (!tc::mbar_wait(bar_kv_full(st), (n / NS) & 1, wc)) return false;
+        if (ROPE && !tc::mbar_wait(bar_k_ready(st), (n / NS) & 1, wc)) return false;
+        if (n >= 2 && !tc::mbar_wait(bar_o_done, (n - 2) & 1, wc)) return false;
+        tc::tc_fence_after();
+        const uint32_t dS = tmem + ((n & 1) ? kColS1 : kColS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ss(dS, tc::desc_kmajor(sQ, kTile, kk), tc::desc_kmajor(sK(st), kTile, kk), idS, kk > 0);
+        tc::mma_commit(bar_s_full(n & 1));
+        return true;
+      };
+      if (ok && sched.next(t)) {
+        ok = issue_s(0);
+        for (int n = 0; ok; ++n) {
+          const bool more = sched.next(t);
+          if (more && !issue_s(n + 1)) break;
+          if (!tc::mbar_wait(bar_p_full(n & 1), (n >> 1) & 1, wc)) break;
+          tc::tc_fence_after();
+          const uint32_t aP = tmem + ((n & 1) ? kColS1 : kColS0);
+          const int st = n % NS;
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk)
+            tc::mma_ts(tmem + kColO, aP + kk * 8, tc::desc_mnmajor(sV(st), kTile, kk), idPV,
+                       (n > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(bar_o_done);
+          tc::mma_commit(bar_kv_empty(st));
+          if (!more) break;
+        }
+      }
+      // All issued MMAs complete before teardown.
+      tc::mma_commit(bar_fin);
+      const tc::WaitCtx drain{abort_flag + 1, p.err};
+      tc::mbar_wait(bar_fin, 0, drain);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------- softmax
+    const int row = threadIdx.x;
+    const int q_pos = q_pos0 + row;
+    const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l = 0.f;
+    int n = 0;
+    bool ok = true;
+    while (sched.next(t)) {
+      const int b = n & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(b), (n >> 1) & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+      // Pass 1: masked row max over the tile (S read from TMEM in 32-column chunks).
+      const uint32_t t_s = t_row + (b ? kColS1 : kColS0);
+      float mt = -INFINITY;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float v = __uint_as_float(r[e]);
+          if (t.need_mask) {
+            const int j = cb * 32 + e, kp = t.pos0 + j;
+            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v = -INFINITY;
+          }
+          mt = fmaxf(mt, v);
+        }
+      }
+      const float m_new = fmaxf(m_run, mt * sl2);
+      bool need = m_new > m_run + 8.f;
+      if (n == 0) {
+        m_run = m_new;
+        need = false;
+      } else if (__any_sync(0xffffffffu, need)) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done, (n - 1) & 1, wc));
+        if (!ok) break;
+        tc::tc_fence_after();
+        const float alpha = need ? exp2f(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_row + kColO + cb * 32, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tc::tmem_st32(t_row + kColO + cb * 32, r);
+        }
+        tc::tmem_st_wait();
+        if (need) {
+          l *= alpha;
+          m_run = m_new;
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // Pass 2: P = 2^(S*scale*log2e - m), rounded to bf16 and written over S.
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float v0 = __uint_as_float(r[2 * e]), v1 = __uint_as_float(r[2 * e + 1]);
+          if (t.need_mask) {
+            const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
+            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
+            if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
+          }
+          pk[e] = pack_bf16x2(exp2f(fmaf(v0, sl2, -m_use)), exp2f(fmaf(v1, sl2, -m_use)));
+          l += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
+        }
+        tc::tmem_st16(t_s + cb * 16, pk);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_p_full(b));
+      ++n;
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done, (n - 1) & 1, wc));
+      if (ok) {
+        tc::tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const bool valid = row < q_rows;
+        const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + qt * kTile + row);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_row + kColO + cb * 32, r);
+          tc::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[cb * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid) p.lse[grow] = l > 0.f ? (m_run + log2f(l)) * 0.693147180559945309f : -INFINITY;
+      }
+    }
+  } else if (ROPE) {
+    // ------------------------------------------------ RoPE transform warps
+    const int wid = warp - 6;
+    bool ok = tc::mbar_wait(bar_q_full, 0, wc);
+    if (ok) {
+      tc::rope_tile<D>(smem + C::OFF_Q, q_pos0, wid, lane, p.theta);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_q_ready);
+      int n = 0;
+      while (sched.next(t)) {
+        const int st = n % NS;
+        if (!tc::mbar_wait(bar_kv_full(st), (n / NS) & 1, wc)) break;
+        tc::rope_tile<D>(smem + C::OFF_K + st * C::TILE, t.pos0, wid, lane, p.theta);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(bar_k_ready(st));
+        ++n;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)c, (cuuint64_t)n_slots};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)c * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+template <int D, bool ROPE>
+cpattn_status launch_fwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const FwdParams &fp, unsigned grid, cudaStream_t s) {
+  constexpr int smem = FwdCfg<D>::SMEM;
+  auto kern = fwd_tc_kernel<D, ROPE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the forward kernel", smem);
+  kern<<<grid, ROPE ? 320 : 192, smem, s>>>(mq, mk, mv, fp);
+  return check_launch("tensor-core forward kernel");
+}
+
+}  // namespace
+
+cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const Geometry &g, cudaStream_t s) {
+  const long long BH = (long long)g.B * g.H;
+  const long long n_slots = BH * 2 * g.cp;
+  CUtensorMap mq, mk, mv;
+  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_slots) ||
+      !make_tile_map(&mv, v, g.d, g.c, n_slots))
+    return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
+  FwdParams fp;
+  fp.o = static_cast<__nv_bfloat16 *>(o);
+  fp.lse = lse;
+  fp.err = device_err_flag();
+  fp.BH = (int)BH;
+  fp.T = g.T;
+  fp.T_valid = g.T_valid;
+  fp.c = g.c;
+  fp.cp = g.cp;
+  fp.causal = g.causal;
+  fp.tpc = (g.c + kTile - 1) / kTile;
+  fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
+  make_rope_theta(g.d, &fp.theta);
+  const long long grid = BH * 2 * g.cp * fp.tpc;
+  if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
+  if (g.d == 128)
+    return g.rope ? launch_fwd_t<128, true>(mq, mk, mv, fp, (unsigned)grid, s)
+                  : launch_fwd_t<128, false>(mq, mk, mv, fp, (unsigned)grid, s);
+  return g.rope ? launch_fwd_t<64, true>(mq, mk, mv, fp, (unsigned)grid, s)
+                : launch_fwd_t<64, false>(mq, mk, mv, fp, (unsigned)grid, s);
+}
+
+}  // namespace cpattn

@@ -1,0 +1,68 @@
+// Internal declarations shared by the translation units of libcpattn.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn.h"
+
+namespace cpattn {
+
+// Records a thread-local message and returns `s`.
+cpattn_status fail(cpattn_status s, const char *fmt, ...);
+// Turns a pending launch error into CPATTN_ERR_CUDA with a message.
+cpattn_status check_launch(const char *what);
+// Device address of this device's error flag (set by kernels, read and
+// cleared by cpattn_sync_status). nullptr if it could not be resolved.
+int *device_err_flag();
+
+// Device error codes written to the flag.
+enum : int { ERR_FLAG_TIMEOUT = 1 };
+
+// RoPE frequencies theta_i = 10000^(-2i/d), i < d/2, split into two floats
+// (hi + lo carries ~48 bits) so that pos * theta can be formed without
+// double arithmetic on the device.
+struct RopeTheta {
+  float hi[64];
+  float lo[64];
+};
+void make_rope_theta(int d, RopeTheta *t);
+
+// HeadTail geometry of one [B,H,T,d] problem.
+struct Geometry {
+  int B, H, T, T_valid, d, cp, c;  // c = T / (2 cp)
+  int causal, rope;
+};
+
+// ---- launchers (one per kernel family), all asynchronous on `s` ----------
+cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
+                           bool inverse, cudaStream_t s);
+cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,
+                             float *lse, const Geometry &g, cudaStream_t s);
+cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                             const float *lse, const float *dO, float *dq, float *dk, float *dv,
+                             float *D, const Geometry &g, cudaStream_t s);
+cpattn_status launch_bwd_preprocess(const void *o, const void *dO, float *D, long long rows,
+                                    int d, cpattn_dtype dt, cudaStream_t s);
+cpattn_status launch_merge(const float *const *o_parts, const float *const *lse_parts, int n,
+                           void *o, float *lse, long long rows, int d, cpattn_dtype dt,
+                           cudaStream_t s);
+cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void *o, float *lse,
+                              const Geometry &g, cudaStream_t s);
+cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                              float *D, const Geometry &g, cudaStream_t s);
+
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+// 3-D tensor map over a sharded [B*H*2cp chunk slots][c rows][D] bf16 tensor,
+// box {64 columns, 128 rows, 1 slot}, 128-byte swizzle, zero fill past row c.
+bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots);
+
+}  // namespace cpattn

@@ -1,0 +1,436 @@
+// CUDA-core kernels of libcpattn:
+//  * HeadTail shard / unshard (HBM-bound chunk copies),
+//  * the backward preprocess D = rowsum(dO * O),
+//  * the standalone SDPAMerger over n partial (O, LSE),
+//  * the exact-fp32 ring attention forward and backward (the correctness
+//    path for fp32 inputs; it follows the ring step by step and merges each
+//    step's partial with the SDPAMerger rule, as the pages' ring does).
+#include <math.h>
+
+#include "device_common.cuh"
+
+namespace cpattn {
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// ------------------------------------------------------------------ shard ---
+// One natural chunk kappa of one (b,h) is c contiguous rows; it lands as c
+// contiguous rows at slot 2r+half of the sharded tensor. Each grid row (y)
+// takes whole chunks, each x-block a strided slice of 16-byte words.
+template <bool INVERSE>
+__global__ void __launch_bounds__(256) shard_kernel(const uint4 *__restrict__ src,
+                                                    uint4 *__restrict__ dst, int cp,
+                                                    long long n_chunks, long long chunk_u4) {
+  const int two_cp = 2 * cp;
+  for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
+    const long long bh = ch / two_cp;
+    const int kappa = (int)(ch % two_cp);
+    int r, half;
+    owner_of(kappa, cp, r, half);
+    const long long nat = (bh * two_cp + kappa) * chunk_u4;
+    const long long shd = (bh * two_cp + 2 * r + half) * chunk_u4;
+    const uint4 *s = src + (INVERSE ? shd : nat);
+    uint4 *d = dst + (INVERSE ? nat : shd);
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < chunk_u4; i += 4 * stride) {
+      uint4 a = s[i], b = s[i + stride], c = s[i + 2 * stride], e = s[i + 3 * stride];
+      d[i] = a; d[i + stride] = b; d[i + 2 * stride] = c; d[i + 3 * stride] = e;
+    }
+    for (; i < chunk_u4; i += stride) d[i] = s[i];
+  }
+}
+
+cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
+                           bool inverse, cudaStream_t s) {
+  const long long n_chunks = (long long)g.B * g.H * 2 * g.cp;
+  const long long chunk_u4 = (long long)g.c * g.d * elt_bytes / 16;
+  const long long want_blocks = (long long)sm_count() * 8;
+  long long bx = (chunk_u4 + 1023) / 1024;
+  long long per_chunk = (want_blocks + n_chunks - 1) / n_chunks;
+  if (bx > per_chunk) bx = per_chunk;
+  if (bx < 1) bx = 1;
+  long long gy = n_chunks < 65535 ? n_chunks : 65535;
+  dim3 grid((unsigned)bx, (unsigned)gy);
+  if (inverse)
+    shard_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                            g.cp, n_chunks, chunk_u4);
+  else
+    shard_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                             g.cp, n_chunks, chunk_u4);
+  return check_launch(inverse ? "unshard kernel" : "shard kernel");
+}
+
+// ------------------------------------------------------------- D = dO.O ---
+template <typename T>
+__device__ __forceinline__ float ld_f(const T *p);
+template <>
+__device__ __forceinline__ float ld_f<float>(const float *p) { return *p; }
+template <>
+__device__ __forceinline__ float ld_f<__nv_bfloat16>(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// One warp per row; lane l reads elements l, l+32, ... (coalesced rows).
+template <typename T>
+__global__ void __launch_bounds__(256) preprocess_kernel(const T *__restrict__ o,
+                                                         const T *__restrict__ dO,
+                                                         float *__restrict__ D, long long rows,
+                                                         int d) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    const T *a = o + row * d, *b = dO + row * d;
+    float acc = 0.f;
+    for (int e = lane; e < d; e += 32) acc = fmaf(ld_f(a + e), ld_f(b + e), acc);
+    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) D[row] = acc;
+  }
+}
+
+cpattn_status launch_bwd_preprocess(const void *o, const void *dO, float *D, long long rows,
+                                    int d, cpattn_dtype dt, cudaStream_t s) {
+  long long blocks = (rows + 7) / 8;
+  long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (dt == CPATTN_F32)
+    preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const float *>(o), static_cast<const float *>(dO), D, rows, d);
+  else
+    preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), D, rows, d);
+  return check_launch("backward preprocess kernel");
+}
+
+// ------------------------------------------------------------------ merge ---
+struct MergeParts {
+  const float *o[16];
+  const float *l[16];
+};
+
+// One warp per row. Lane i < n reads L_i; the max, the weights and their sum
+// are formed with shuffles and each weight is broadcast from its lane while
+// every lane accumulates its d/32-wide slice of O.
+template <int D, typename TO>
+__global__ void __launch_bounds__(256) merge_kernel(MergeParts parts, int n, TO *__restrict__ o,
+                                                    float *__restrict__ lse, long long rows) {
+  constexpr int V = D / 32;  // floats per lane (2 or 4)
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows;
+       row += warps) {
+    float li = lane < n ? parts.l[lane][row] : -INFINITY;
+    float m = li;
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const bool empty = !(m > -INFINITY);
+    float w = (lane < n && li > -INFINITY) ? expf(li - m) : 0.f;
+    float tot = w;
+    for (int off = 16; off; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    float acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    for (int i = 0; i < n; ++i) {
+      const float wi = __shfl_sync(0xffffffffu, w, i);
+      if (empty || wi == 0.f) continue;
+      const float *src = parts.o[i] + row * D + lane * V;
+      if constexpr (V == 4) {
+        float4 x = *reinterpret_cast<const float4 *>(src);
+        acc[0] = fmaf(wi, x.x, acc[0]); acc[1] = fmaf(wi, x.y, acc[1]);
+        acc[2] = fmaf(wi, x.z, acc[2]); acc[3] = fmaf(wi, x.w, acc[3]);
+      } else {
+        float2 x = *reinterpret_cast<const float2 *>(src);
+        acc[0] = fmaf(wi, x.x, acc[0]); acc[1] = fmaf(wi, x.y, acc[1]);
+      }
+    }
+    const float inv = empty ? 0.f : 1.f / tot;
+    TO *dst = o + row * D + lane * V;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      if constexpr (sizeof(TO) == 4) dst[e] = acc[e] * inv;
+      else dst[e] = __float2bfloat16_rn(acc[e] * inv);
+    }
+    if (lane == 0) lse[row] = empty ? -INFINITY : m + logf(tot);
+  }
+}
+
+cpattn_status launch_merge(const float *const *o_parts, const float *const *lse_parts, int n,
+                           void *o, float *lse, long long rows, int d, cpattn_dtype dt,
+                           cudaStream_t s) {
+  MergeParts p;
+  for (int i = 0; i < 16; ++i) {
+    p.o[i] = i < n ? o_parts[i] : nullptr;
+    p.l[i] = i < n ? lse_parts[i] : nullptr;
+  }
+  long long blocks = (rows + 7) / 8;
+  long long cap = (long long)sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  const unsigned gb = (unsigned)blocks;
+  if (d == 128) {
+    if (dt == CPATTN_F32) merge_kernel<128, float><<<gb, 256, 0, s>>>(p, n, static_cast<float *>(o), lse, rows);
+    else merge_kernel<128, __nv_bfloat16><<<gb, 256, 0, s>>>(p, n, static_cast<__nv_bfloat16 *>(o), lse, rows);
+  } else {
+    if (dt == CPATTN_F32) merge_kernel<64, float><<<gb, 256, 0, s>>>(p, n, static_cast<float *>(o), lse, rows);
+    else merge_kernel<64, __nv_bfloat16><<<gb, 256, 0, s>>>(p, n, static_cast<__nv_bfloat16 *>(o), lse, rows);
+  }
+  return check_launch("merge kernel");
+}
+
+// ------------------------------------------------- exact fp32 ring attention ---
+// Geometry of sharded row i: rank r = i / 2c, half = (i % 2c) / c; its
+// natural position is chunk_of(r, half) * c + i % c.
+__device__ __forceinline__ int natural_pos(int i, int c, int cp) {
+  const int r = i / (2 * c), l = i % (2 * c);
+  return chunk_of(r, l / c, cp) * c + (l % c);
+}
+
+// A lane holds elements lane + 32*e of a row (e < D/32); for rotate-half
+// RoPE the partner of e is e +- D/64, held by the same lane. Angles are taken
+// in double: this path is about exactness, not speed.
+template <int D>
+__device__ __forceinline__ void rope_row_f32(float (&x)[D / 32], int pos, int lane, bool transpose) {
+  constexpr int V = D / 32, HV = V / 2;
+#pragma unroll
+  for (int e = 0; e < HV; ++e) {
+    const int i = lane + 32 * e;  // frequency index < D/2
+    const double th = pow(10000.0, -2.0 * i / D);
+    double sn, cs;
+    sincos((double)pos * th, &sn, &cs);
+    const float c = (float)cs, s = transpose ? -(float)sn : (float)sn;
+    const float a = x[e], b = x[e + HV];
+    x[e] = a * c - b * s;
+    x[e + HV] = b * c + a * s;
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void load_row(const float *p, int lane, float (&x)[D / 32]) {
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) x[e] = p[lane + 32 * e];
+}
+
+template <int D>
+__device__ __forceinline__ float warp_dot(const float (&a)[D / 32], const float (&b)[D / 32]) {
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < D / 32; ++e) s = fmaf(a[e], b[e], s);
+  for (int off = 16; off; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
+__device__ __forceinline__ bool pair_allowed(int qp, int kp, const Geometry &g) {
+  return (!g.causal || kp <= qp) && kp < g.T_valid;
+}
+
+// Forward: one warp per sharded query row. For ring step s the row's rank r
+// holds the K/V of rank j = (r - s) mod cp; the step's partial (O_s, LSE_s)
+// is formed over that rank's head and tail chunks and merged into the
+// running result with the SDPAMerger rule.
+template <int D>
+__global__ void __launch_bounds__(128) fwd_f32_kernel(const float *__restrict__ q,
+                                                      const float *__restrict__ k,
+                                                      const float *__restrict__ v,
+                                                      float *__restrict__ o, float *__restrict__ lse,
+                                                      Geometry g) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (long long)g.B * g.H * g.T) return;
+  const long long bh = row / g.T;
+  const int i = (int)(row % g.T);
+  const int r = i / (2 * g.c);
+  const int qp = natural_pos(i, g.c, g.cp);
+  const float scale = 1.f / sqrtf((float)D);
+  const float *kb = k + bh * g.T * D, *vb = v + bh * g.T * D;
+  float qr[V];
+  load_row<D>(q + row * D, lane, qr);
+  if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+  float O[V], L = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < V; ++e) O[e] = 0.f;
+  for (int s = 0; s < g.cp; ++s) {
+    const int j = (r - s + g.cp) % g.cp;
+    float m_s = -INFINITY, l_s = 0.f, acc[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+    for (int half = 0; half < 2; ++half) {
+      const int kappa = chunk_of(j, half, g.cp);
+      const int row0 = 2 * g.c * j + half * g.c;
+      for (int u = 0; u < g.c; ++u) {
+        const int kp = kappa * g.c + u;
+        if (!pair_allowed(qp, kp, g)) continue;
+        float kr[V], vr[V];
+        load_row<D>(kb + (long long)(row0 + u) * D, lane, kr);
+        if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+        load_row<D>(vb + (long long)(row0 + u) * D, lane, vr);
+        const float sc = warp_dot<D>(qr, kr) * scale;
+        const float m_new = fmaxf(m_s, sc);
+        const float alpha = expf(m_s - m_new);  // 0 when m_s = -inf
+        const float p = expf(sc - m_new);
+        l_s = l_s * alpha + p;
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(p, vr[e], acc[e] * alpha);
+        m_s = m_new;
+      }
+    }
+    if (m_s > -INFINITY) {  // merge step partial (acc/l_s, m_s + log l_s) into (O, L)
+      const float L_s = m_s + logf(l_s);
+      const float m = fmaxf(L, L_s);
+      const float wa = (L > -INFINITY) ? expf(L - m) : 0.f, wb = expf(L_s - m);
+      const float tot = wa + wb;
+#pragma unroll
+      for (int e = 0; e < V; ++e) O[e] = (wa * O[e] + wb * (acc[e] / l_s)) / tot;
+      L = m + logf(tot);
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) o[row * D + lane + 32 * e] = O[e];
+  if (lane == 0) lse[row] = L;
+}
+
+// dQ: one warp per sharded query row, over every allowed key.
+template <int D>
+__global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict__ q,
+                                                         const float *__restrict__ k,
+                                                         const float *__restrict__ v,
+                                                         const float *__restrict__ lse,
+                                                         const float *__restrict__ dO,
+                                                         const float *__restrict__ Dv,
+                                                         float *__restrict__ dq, Geometry g) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (long long)g.B * g.H * g.T) return;
+  const long long bh = row / g.T;
+  const int i = (int)(row % g.T);
+  const int r = i / (2 * g.c);
+  const int qp = natural_pos(i, g.c, g.cp);
+  const float scale = 1.f / sqrtf((float)D);
+  const float *kb = k + bh * g.T * D, *vb = v + bh * g.T * D;
+  float qr[V], dor[V], acc[V];
+  load_row<D>(q + row * D, lane, qr);
+  if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+  load_row<D>(dO + row * D, lane, dor);
+  const float L = lse[row], Dt = Dv[row];
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] = 0.f;
+  for (int s = 0; s < g.cp; ++s) {
+    const int j = (r - s + g.cp) % g.cp;
+    for (int half = 0; half < 2; ++half) {
+      const int kappa = chunk_of(j, half, g.cp);
+      const int row0 = 2 * g.c * j + half * g.c;
+      for (int u = 0; u < g.c; ++u) {
+        const int kp = kappa * g.c + u;
+        if (!pair_allowed(qp, kp, g)) continue;
+        float kr[V], vr[V];
+        load_row<D>(kb + (long long)(row0 + u) * D, lane, kr);
+        if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+        load_row<D>(vb + (long long)(row0 + u) * D, lane, vr);
+        const float p = expf(warp_dot<D>(qr, kr) * scale - L);
+        const float ds = p * (warp_dot<D>(dor, vr) - Dt);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(ds, kr[e], acc[e]);
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) acc[e] *= scale;
+  if (g.rope) rope_row_f32<D>(acc, qp, lane, true);
+#pragma unroll
+  for (int e = 0; e < V; ++e) dq[row * D + lane + 32 * e] = acc[e];
+}
+
+// dK, dV: one warp per sharded key row. Its K/V travel the ring: at step s
+// they sit on rank (j + s) mod cp, whose queries add their contributions.
+template <int D>
+__global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restrict__ q,
+                                                           const float *__restrict__ k,
+                                                           const float *__restrict__ v,
+                                                           const float *__restrict__ lse,
+                                                           const float *__restrict__ dO,
+                                                           const float *__restrict__ Dv,
+                                                           float *__restrict__ dk,
+                                                           float *__restrict__ dv, Geometry g) {
+  constexpr int V = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (long long)g.B * g.H * g.T) return;
+  const long long bh = row / g.T;
+  const int i = (int)(row % g.T);
+  const int j = i / (2 * g.c);
+  const int kp = natural_pos(i, g.c, g.cp);
+  const float scale = 1.f / sqrtf((float)D);
+  const float *qb = q + bh * g.T * D, *dob = dO + bh * g.T * D;
+  const float *lb = lse + bh * g.T, *Db = Dv + bh * g.T;
+  float kr[V], vr[V], adk[V], adv[V];
+  load_row<D>(k + row * D, lane, kr);
+  if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+  load_row<D>(v + row * D, lane, vr);
+#pragma unroll
+  for (int e = 0; e < V; ++e) { adk[e] = 0.f; adv[e] = 0.f; }
+  for (int s = 0; s < g.cp; ++s) {
+    const int r = (j + s) % g.cp;
+    for (int half = 0; half < 2; ++half) {
+      const int kappa = chunk_of(r, half, g.cp);
+      const int row0 = 2 * g.c * r + half * g.c;
+      for (int u = 0; u < g.c; ++u) {
+        const int qp = kappa * g.c + u;
+        if (!pair_allowed(qp, kp, g)) continue;
+        const int t = row0 + u;
+        float qr[V], dor[V];
+        load_row<D>(qb + (long long)t * D, lane, qr);
+        if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+        load_row<D>(dob + (long long)t * D, lane, dor);
+        const float p = expf(warp_dot<D>(qr, kr) * scale - lb[t]);
+        const float ds = p * (warp_dot<D>(dor, vr) - Db[t]);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          adv[e] = fmaf(p, dor[e], adv[e]);
+          adk[e] = fmaf(ds, qr[e], adk[e]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < V; ++e) adk[e] *= scale;
+  if (g.rope) rope_row_f32<D>(adk, kp, lane, true);
+#pragma unroll
+  for (int e = 0; e < V; ++e) {
+    dk[row * D + lane + 32 * e] = adk[e];
+    dv[row * D + lane + 32 * e] = adv[e];
+  }
+}
+
+cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,
+                             const Geometry &g, cudaStream_t s) {
+  const long long rows = (long long)g.B * g.H * g.T;
+  const unsigned blocks = (unsigned)((rows + 3) / 4);
+  if (g.d == 128) fwd_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g);
+  else fwd_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g);
+  return check_launch("fp32 forward kernel");
+}
+
+cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                             const float *lse, const float *dO, float *dq, float *dk, float *dv,
+                             float *D, const Geometry &g, cudaStream_t s) {
+  (void)o;
+  const long long rows = (long long)g.B * g.H * g.T;
+  const unsigned blocks = (unsigned)((rows + 3) / 4);
+  if (g.d == 128) {
+    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
+    bwd_dkdv_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+  } else {
+    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
+    bwd_dkdv_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+  }
+  return check_launch("fp32 backward kernels");
+}
+
+}  // namespace cpattn

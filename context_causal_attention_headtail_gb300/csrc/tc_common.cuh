@@ -1,0 +1,272 @@
+// Blackwell (sm_103a) building blocks written as inline PTX: mbarriers with
+// bounded waits, TMA tile loads, tensor-memory allocation and access, and
+// tcgen05.mma with shared-memory descriptors for 128-byte-swizzled tiles.
+//
+// Tile convention used by every tensor-core kernel here. A tile of R rows by
+// D bf16 columns (D = 64 or 128) lives in shared memory as D/64 column blocks;
+// block b holds columns [64b, 64b+64) of all R rows, 128 bytes per row, in the
+// 128-byte swizzle that TMA writes (16-byte chunk index XOR row % 8), and
+// each block starts on a 1024-byte boundary. Such a tile is
+//  * a K-major operand when its columns are the contraction dimension
+//    (Q, K as used in Q K^T): 8-row groups are 1024 bytes apart (SBO); a
+//    16-column k-step moves 32 bytes inside the swizzle row or to the next
+//    column block;
+//  * an MN-major operand when its rows are the contraction dimension (V in
+//    P V, dO in P^T dO, Q in dS^T Q, K in dS K): 8-row groups are 1024 bytes
+//    apart (SBO), column blocks R*128 bytes apart (LBO), and a 16-row k-step
+//    moves 2048 bytes.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+
+namespace cpattn {
+namespace tc {
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier ---
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Shared state for bounded waits: a CTA-wide abort flag in shared memory and
+// the device error flag. A wait that has not completed after kWaitLimitNs,
+// or that sees another role abort, records the failure and returns false; its
+// caller then leaves its loop and the kernel runs its teardown.
+struct WaitCtx {
+  volatile int *abort;  // shared memory
+  int *err;             // global memory
+};
+
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx w) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *w.abort = 1;
+      if (w.err) atomicOr(w.err, ERR_FLAG_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, WaitCtx w) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, w);
+}
+
+// ---------------------------------------------------------------------- TMA ---
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 3-D tiled load of box {64, rows, 1} at (x, y, z) into 128B-swizzled smem.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (MMA, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- TMEM ---
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: lane i of the warp gets row
+// (warp%4)*32 + i, columns [col, col+32) of the address's lane quarter.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------- MMA ---
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4)                           // D format: f32
+         | (1u << 7)                         // A format: bf16
+         | (1u << 10)                        // B format: bf16
+         | ((a_mn_major ? 1u : 0u) << 15)    // A major-ness (0 = K-major)
+         | ((b_mn_major ? 1u : 0u) << 16)    // B major-ness
+         | ((uint32_t)(N >> 3) << 17)        // N / 8
+         | ((uint32_t)(M >> 4) << 24);       // M / 16
+}
+
+// Shared-memory matrix descriptor with 128-byte swizzling.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;   // fixed field of the tcgen05 descriptor format
+  d |= (uint64_t)2 << 61;   // swizzle mode: 128 bytes
+  return d;
+}
+
+// K-major operand: tile of R rows at `base`, k-step kk (16 columns).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t base, int R, int kk) {
+  const uint32_t addr = base + (uint32_t)(kk >> 2) * (uint32_t)R * 128u + (uint32_t)(kk & 3) * 32u;
+  return sdesc_sw128(addr, 16u, 1024u);
+}
+// MN-major operand: tile of R rows (the contraction dim) at `base`, k-step kk
+// (16 rows); N runs over the column blocks, R*128 bytes apart.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int R, int kk) {
+  const uint32_t addr = base + (uint32_t)kk * 2048u;
+  return sdesc_sw128(addr, (uint32_t)R * 128u, 1024u);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem]; A is M lanes x K bf16, two per 32-bit column.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on `bar` when all previously issued tcgen05 ops of this thread finish.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// ------------------------------------------------------ swizzled smem access ---
+// Byte offset of element (row, col) in a 128B-swizzled tile of R rows.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int R) {
+  const int blk = col >> 6, cc = col & 63;
+  return (uint32_t)blk * (uint32_t)R * 128u + (uint32_t)row * 128u +
+         ((uint32_t)((cc >> 3) ^ (row & 7)) << 4) + ((uint32_t)(cc & 7) << 1);
+}
+
+// Rotate (rotate-half RoPE) the 128 rows of a swizzled bf16 tile in place;
+// row i sits at natural position pos0 + i. Called by
+// the four warps of a warpgroup (wid 0..3). A lane owns frequency pair
+// (f, f+1) of one row at a time and walks rows with a fixed stride; its
+// cos/sin are seeded once with rope_sincos and advanced by an exact
+// angle-addition step (error grows by ~1 ulp per step, <= 32 steps).
+template <int D>
+__device__ __forceinline__ void rope_tile(uint8_t *tile, int pos0, int wid, int lane,
+                                          const RopeTheta &th) {
+  constexpr int LPR = D / 4;        // lanes per row (each lane: 2 frequencies)
+  constexpr int RPI = 32 / LPR;     // rows per warp step
+  constexpr int STEP = 4 * RPI;     // row stride of one lane
+  const int sub = lane / LPR, f = 2 * (lane % LPR);
+  const int row0 = wid * RPI + sub;
+  float c0, s0, c1, s1, cd0, sd0, cd1, sd1;
+  rope_sincos(pos0 + row0, th.hi[f], th.lo[f], s0, c0);
+  rope_sincos(pos0 + row0, th.hi[f + 1], th.lo[f + 1], s1, c1);
+  rope_sincos(STEP, th.hi[f], th.lo[f], sd0, cd0);
+  rope_sincos(STEP, th.hi[f + 1], th.lo[f + 1], sd1, cd1);
+#pragma unroll 4
+  for (int row = row0; row < 128; row += STEP) {
+    uint32_t *pa = reinterpret_cast<uint32_t *>(tile + sw128_offset(row, f, 128));
+    uint32_t *pb = reinterpret_cast<uint32_t *>(tile + sw128_offset(row, f + D / 2, 128));
+    const uint32_t a = *pa, b = *pb;
+    const float x0 = bf16lo_to_f32(a), x1 = bf16hi_to_f32(a);
+    const float y0 = bf16lo_to_f32(b), y1 = bf16hi_to_f32(b);
+    *pa = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+    *pb = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+    const float nc0 = fmaf(c0, cd0, -s0 * sd0), ns0 = fmaf(s0, cd0, c0 * sd0);
+    const float nc1 = fmaf(c1, cd1, -s1 * sd1), ns1 = fmaf(s1, cd1, c1 * sd1);
+    c0 = nc0; s0 = ns0; c1 = nc1; s1 = ns1;
+  }
+}
+
+}  // namespace tc
+}  // namespace cpattn

@@ -1,0 +1,147 @@
+/*
+ * cpattn -- HeadTail-balanced ring (context-parallel) causal attention on one
+ * GB300 (sm_103a). C ABI: plain pointers, sizes and a CUDA stream; no C++ or
+ * framework types cross this boundary.
+ *
+ * What it computes. A sequence of T tokens is cut into 2*cp chunks of
+ * c = T/(2*cp); virtual rank r owns chunk r (head) and chunk 2*cp-1-r (tail)
+ * ("BluScriptCP -- docs/Claude Logs.md", entries 2026-05-16 and 2026-06-29;
+ * "fix(cp): preserve gradients when sharding VLM inputs - #2931", head-tail
+ * chunk pairing). Each rank's queries attend, ring step by ring step, to the
+ * K/V chunks of rank j = (r - s) mod cp under the global causal mask
+ * (Claude Logs, 2026-04-20: T_q/T_k/q_offset/k_offset masking; 2026-06-17:
+ * the three step shapes), and the per-step partials are merged by the
+ * log-sum-exp rule (Claude Logs, 2026-03-20: SDPAMerger). The backward
+ * recomputes P from the saved LSE and accumulates dQ/dK/dV over all ring
+ * steps (Claude Logs, 2026-03-24: D correction; 2026-06-22: dK/dV travel
+ * with K/V and return to their owner). Here the ring's K/V rotation is a loop
+ * over resident chunks, so the result equals single-pass causal attention.
+ *
+ * Conventions shared by every call:
+ *  - Tensors are dense, contiguous, row-major. [B,H,T,d] tensors passed to
+ *    cpattn_fwd / cpattn_bwd are in HeadTail-sharded token order (the output
+ *    order of cpattn_shard); LSE and D are [B,H,T] in the same order.
+ *  - Device pointers must be 16-byte aligned and must not alias unless
+ *    stated. The caller owns every buffer; the library allocates nothing on
+ *    the device and keeps no per-call state.
+ *  - All work is enqueued on `stream` and is asynchronous. The return value
+ *    reports host-detectable errors (arguments, shapes, launch failures). A
+ *    device-side error (a bounded wait that timed out) is recorded in a
+ *    per-device flag and reported by the next cpattn_sync_status().
+ *  - No call aborts, exits or traps; on error nothing is enqueued (or the
+ *    launch failed) and cpattn_last_error() describes it.
+ *  - softmax scale = 1/sqrt(d). LSE is the natural log of the sum of
+ *    exponentials of the scaled scores. RoPE (rope = 1) is the rotate-half
+ *    pairing (i, i + d/2) with theta_i = 10000^(-2i/d), applied to q and k at
+ *    each token's global (natural) position.
+ *  - T_valid <= T real tokens: keys at natural positions >= T_valid (tail
+ *    padding, "fix(cp) ... #2931": pad to a multiple of 2*cp at the end) are
+ *    masked out.
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *cpattn_stream_t;
+
+typedef enum {
+  CPATTN_OK = 0,
+  CPATTN_ERR_ARG = 1,         /* null pointer, bad enum, aliasing buffers      */
+  CPATTN_ERR_SHAPE = 2,       /* T % (2*cp) != 0, T_valid out of range, d ...  */
+  CPATTN_ERR_DTYPE = 3,       /* dtype not supported by this call              */
+  CPATTN_ERR_ALIGN = 4,       /* pointer not 16-byte aligned                   */
+  CPATTN_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed   */
+  CPATTN_ERR_TIMEOUT = 6,     /* a kernel's bounded wait expired (device flag) */
+  CPATTN_ERR_UNSUPPORTED = 7  /* valid request this build does not implement   */
+} cpattn_status;
+
+typedef enum { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
+
+/* ---------------------------------------------------------------- shard ---
+ * HeadTail permutation along T of a [B,H,T,d] tensor (Claude Logs,
+ * 2026-05-16, chunk-level HeadTail; 2026-06-29, worked example {0,1,6,7} for
+ * N=2). cpattn_shard writes dst[b,h,sigma(t),:] = src[b,h,t,:] with
+ *   kappa = t / c, o = t % c,
+ *   sigma(t) = 2c*kappa + o            if kappa < cp,
+ *            = 2c*(2cp-1-kappa) + c + o otherwise.
+ * cpattn_unshard is its inverse. Out of place: src and dst must not overlap.
+ * dt selects the element size (4 or 2 bytes); d*elt must be a multiple of 16.
+ * Errors: CPATTN_ERR_SHAPE if T % (2*cp) != 0 or any size < 1. */
+cpattn_status cpattn_shard(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                           cpattn_dtype dt, cpattn_stream_t stream);
+cpattn_status cpattn_unshard(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                             cpattn_dtype dt, cpattn_stream_t stream);
+
+/* Host-only: idx_host[t] = sigma(t) for t in [0, T) (int32, caller-owned,
+ * T entries). Launches nothing. */
+cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host);
+
+/* ------------------------------------------------------------- forward ---
+ * Ring attention forward (Claude Logs, 2026-03-20 ring + SDPAMerger;
+ * 2026-04-20 global causal masking; 2026-06-17 step shapes).
+ *   q, k, v : [B,H,T,d] sharded, dtype dt (read only)
+ *   o       : [B,H,T,d] sharded, dtype dt (written)
+ *   lse     : [B,H,T]   sharded, fp32     (written)
+ * d in {64, 128}. causal in {0,1}, rope in {0,1}, 1 <= T_valid <= T.
+ * dt = CPATTN_BF16 runs the tensor-core (tcgen05) kernel; dt = CPATTN_F32 runs
+ * the exact-fp32 CUDA-core kernel (a correctness path, not a fast one). */
+cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int T, int T_valid, int H, int d, int cp, int causal, int rope,
+                         cpattn_dtype dt, cpattn_stream_t stream);
+
+/* ------------------------------------------------------------ backward ---
+ * Gradient of sum(dO * O) with respect to the q, k, v given to cpattn_fwd
+ * (before RoPE), from that call's o and lse (Claude Logs, 2026-03-24 D
+ * correction; 2026-06-22 dK/dV accumulate over every ring step; 2026-04-20).
+ * With P = exp(S - LSE): dV = P^T dO; D = rowsum(dO * O); dS = P*(dO V^T - D);
+ * dQ = scale * dS K; dK = scale * dS^T Q (then R^T when rope = 1).
+ *   q, k, v, o, dO : [B,H,T,d] sharded, dtype dt (read only)
+ *   lse            : [B,H,T] fp32 (read only, from cpattn_fwd)
+ *   dq, dk, dv     : [B,H,T,d] sharded, dtype dt (written; fp32 accumulation)
+ *   workspace      : device scratch of at least cpattn_bwd_workspace_bytes()
+ *                    bytes, 16-byte aligned, caller-owned; holds D (fp32).
+ * dQ is accumulated without atomics: one kernel owns each dQ tile (query
+ * stationary) and another each dK/dV tile (key stationary). */
+size_t cpattn_bwd_workspace_bytes(int B, int T, int H, int d);
+cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                         void *workspace, int B, int T, int T_valid, int H, int d, int cp,
+                         int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
+
+/* --------------------------------------------------------------- merge ---
+ * Standalone SDPAMerger (Claude Logs, 2026-03-20; 2026-03-26 on keeping P
+ * and LSE consistent; 2026-05-20 partial-merge fix): merges n partial
+ * results of the same rows,
+ *   L = m + log(sum_i exp(L_i - m)), m = max_i L_i;  O = sum_i exp(L_i - L) O_i,
+ * with (O_i = 0, L_i = -inf) the identity and an all-empty row giving (0, -inf).
+ *   o_parts, lse_parts : host arrays of n device pointers; O_i fp32 [B,H,T,d],
+ *                        L_i fp32 [B,H,T]
+ *   o   : [B,H,T,d] dtype dt (written);  lse : [B,H,T] fp32 (written)
+ * 1 <= n <= 16. Any row order (the merge is row-wise). */
+cpattn_status cpattn_merge(const float *const *o_parts, const float *const *lse_parts, int n,
+                           void *o, float *lse, int B, int H, int T, int d, cpattn_dtype dt,
+                           cpattn_stream_t stream);
+
+/* ----------------------------------------------------------- diagnostics -- */
+/* Thread-local description of the last non-OK status ("" if none). */
+const char *cpattn_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * flag: CPATTN_ERR_TIMEOUT if a kernel's bounded wait expired since the last
+ * check, CPATTN_ERR_CUDA if the stream reports an error, else CPATTN_OK. */
+cpattn_status cpattn_sync_status(cpattn_stream_t stream);
+
+/* Library version, e.g. "cpattn 0.1 sm_103a". */
+const char *cpattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CPATTN_H */

@@ -1,0 +1,96 @@
+"""Runs the CUDA path end to end through the C-ABI binding, and compares.
+
+``run_gpu`` takes natural-order CPU inputs from ``synth.make_inputs``, shards
+them on the device with cpattn_shard, runs cpattn_fwd and cpattn_bwd, and
+unshards O, LSE and the gradients back to natural order, returning CPU
+tensors. Nothing here computes attention: the CUDA kernels do, and the oracle
+(float64, CPU) is what the results are compared with.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from context_causal_attention_headtail_gb300 import cpattn
+from context_causal_attention_headtail_gb300.synth import Workload
+
+# Tolerances of the parity bar: fp32 path max-abs 1e-4 on O and LSE; bf16
+# path max-abs 2e-2 on O, 5e-2 on dQ/dK/dV, cosine >= 0.9999.
+TOL = {
+    "f32": {"o": 1e-4, "lse": 1e-4, "grad": 1e-4, "cos": 0.999999},
+    "bf16": {"o": 2e-2, "lse": 2e-2, "grad": 5e-2, "cos": 0.9999},
+}
+
+
+def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1) -> dict:
+    dt = w.torch_dtype
+    dev = torch.device(device)
+    stream = torch.cuda.current_stream(dev)
+    nat = {k: v.to(dev).contiguous() for k, v in inp.items()}
+    sh = {k: torch.empty_like(v) for k, v in nat.items()}
+    for k in nat:
+        cpattn.shard(nat[k], sh[k], w.cp, stream)
+    o = torch.empty_like(sh["q"])
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    out = {}
+    for _ in range(repeat):
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, w.rope, stream)
+    if with_bwd:
+        dq, dk, dv = (torch.empty_like(sh["q"]) for _ in range(3))
+        ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
+                         device=dev)
+        for _ in range(repeat):
+            cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
+                       w.causal, w.rope, stream)
+        for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+            nt = torch.empty_like(t)
+            cpattn.unshard(t, nt, w.cp, stream)
+            out[name] = nt
+    on = torch.empty_like(o)
+    cpattn.unshard(o, on, w.cp, stream)
+    out["o"] = on
+    # LSE [B,H,T] is unsharded as a [B,H,T,4]-float view padded to 16 bytes per row.
+    lse4 = torch.zeros((w.B, w.H, w.T, 4), dtype=torch.float32, device=dev)
+    lse4[..., 0] = lse
+    lse4n = torch.empty_like(lse4)
+    cpattn.unshard(lse4, lse4n, w.cp, stream)
+    out["lse"] = lse4n[..., 0].contiguous()
+    cpattn.cpattn_sync_status(stream.cuda_stream)
+    return {k: v.float().cpu() for k, v in out.items()}
+
+
+def compare(name: str, got, want, tol_abs: float, tol_cos: float | None = None) -> dict:
+    g = np.asarray(got, dtype=np.float64)
+    e = np.asarray(want, dtype=np.float64)
+    assert g.shape == e.shape, (name, g.shape, e.shape)
+    finite = np.isfinite(e)
+    assert np.array_equal(np.isfinite(g), finite), f"{name}: finiteness differs"
+    diff = np.abs(g[finite] - e[finite])
+    maxabs = float(diff.max()) if diff.size else 0.0
+    rep = {"name": name, "maxabs": maxabs}
+    if tol_cos is not None and diff.size:
+        num = float(np.dot(g[finite].ravel(), e[finite].ravel()))
+        den = float(np.linalg.norm(g[finite]) * np.linalg.norm(e[finite]))
+        rep["cos"] = num / den if den > 0 else 1.0
+    assert maxabs <= tol_abs, f"{name}: max-abs {maxabs:.3e} > {tol_abs:.1e}"
+    if tol_cos is not None and "cos" in rep:
+        assert rep["cos"] >= tol_cos, f"{name}: cosine {rep['cos']:.7f} < {tol_cos}"
+    return rep
+
+
+def sample_rows(w: Workload, n_random: int, seed: int) -> np.ndarray:
+    """Rows at chunk seams, both ends, the last real token, plus random ones."""
+    c = w.chunk
+    rows = {0, 1, w.T - 1, w.T_valid - 1, min(w.T_valid, w.T - 1)}
+    for kappa in range(2 * w.cp):
+        rows |= {kappa * c, kappa * c + c - 1, min(kappa * c + 127, w.T - 1), min(kappa * c + 128, w.T - 1)}
+    rng = np.random.default_rng(seed)
+    rows |= set(rng.integers(0, w.T, size=n_random).tolist())
+    return np.array(sorted(r for r in rows if 0 <= r < w.T))
+
+
+def cosine(a, b) -> float:
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / max(np.linalg.norm(a) * np.linalg.norm(b), 1e-300))
+

@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small cases are compared element by element over the whole output; they span
+several 128-row tiles per chunk, ragged last tiles (c not a multiple of 128,
+c < 128), cp in {1, 2, 3, 4}, d in {64, 128}, non-causal attention and tail
+padding. The five benchmark workloads run at full size and are compared on
+sampled rows (O, LSE, dQ over several heads; dK, dV over one head, which needs
+that head's full forward in the oracle), plus properties that hold at any size
+(pad-row gradients exactly zero, bitwise determinism).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from context_causal_attention_headtail_gb300 import cpattn
+from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make_inputs, make_workload
+from oracle import attention as A
+from oracle import headtail as HT
+
+from harness import TOL, compare, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_full(w, inp):
+    q, k, v, do = (inp[n].double().numpy() for n in ("q", "k", "v", "do"))
+    O, L = A.forward(q, k, v, w.causal, w.T_valid, w.rope)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, w.causal, w.T_valid, w.rope)
+    return {"o": O, "lse": L, "dq": dq, "dk": dk, "dv": dv}
+
+
+def _check_full(w, got, want):
+    tol = TOL[w.dtype]
+    reps = [compare("o", got["o"], want["o"], tol["o"], tol["cos"]),
+            compare("lse", got["lse"], want["lse"], tol["lse"])]
+    for g in ("dq", "dk", "dv"):
+        reps.append(compare(g, got[g], want[g], tol["grad"], tol["cos"]))
+    return reps
+
+
+# ------------------------------------------------------------- shard ----
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,T,d,cp", [(1, 2, 8, 64, 2), (2, 3, 24, 128, 3), (1, 1, 512, 64, 1),
+                                        (2, 2, 12296, 128, 4)])
+def test_shard_unshard_bit_exact(dtype, B, H, T, d, cp):
+    x = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(T + cp)).to(dtype)
+    xs = x.cuda()
+    ys, zs = torch.empty_like(xs), torch.empty_like(xs)
+    cpattn.shard(xs, ys, cp)
+    cpattn.unshard(ys, zs, cp)
+    torch.cuda.synchronize()
+    want = torch.from_numpy(HT.shard(x.float().numpy(), cp)).to(dtype)
+    assert torch.equal(ys.cpu(), want)
+    assert torch.equal(zs.cpu(), x)
+
+
+def test_shard_index_matches_oracle():
+    for T, cp in [(8, 2), (24, 3), (32768, 2), (12296, 4)]:
+        assert cpattn.cpattn_shard_index(T, cp) == HT.shard_index(T, cp).tolist()
+
+
+# -------------------------------------------------- small, full compare ----
+
+SMALL_F32 = [
+    WORKLOADS["tiny_fp32"],
+    make_workload("f32_rope_pad", B=1, T=384, T_valid=381, H=2, d=128, cp=3, rope=True, dtype="f32",
+                  qkv_std=1.0),
+    make_workload("f32_noncausal", B=2, T=256, H=1, d=64, cp=2, causal=False, rope=True, dtype="f32",
+                  qkv_std=1.0),
+]
+
+SMALL_BF16 = [
+    make_workload("two_tiles_rope", B=1, T=1024, H=2, d=128, cp=2, rope=True),
+    make_workload("ragged_d64_pad", B=2, T=800, T_valid=797, H=1, d=64, cp=2, rope=False),
+    make_workload("cp1", B=1, T=512, H=1, d=128, cp=1, rope=True),
+    make_workload("noncausal_cp3", B=1, T=768, H=2, d=64, cp=3, causal=False, rope=True),
+    make_workload("small_chunks_cp4", B=1, T=512, T_valid=509, H=1, d=128, cp=4, rope=True),
+    make_workload("ragged_c300", B=1, T=1200, T_valid=1195, H=2, d=128, cp=2, rope=True),
+    make_workload("noncausal_pad_d128", B=1, T=640, T_valid=600, H=1, d=128, cp=2, causal=False,
+                  rope=False),
+]
+
+
+@pytest.mark.parametrize("w", SMALL_F32, ids=lambda w: w.name)
+def test_fp32_path_full(w):
+    inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
+    _check_full(w, run_gpu(w, inp), _oracle_full(w, inp))
+
+
+@pytest.mark.parametrize("w", SMALL_BF16, ids=lambda w: w.name)
+def test_bf16_path_full(w):
+    inp = make_inputs(w, seed=7 + w.T + w.cp)
+    got = run_gpu(w, inp)
+    want = _oracle_full(w, inp)
+    _check_full(w, got, want)
+    if w.T_valid < w.T:   # pad rows: dO = 0 there, so every gradient row is exactly zero
+        for g in ("dq", "dk", "dv"):
+            assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0
+
+
+def test_bf16_deterministic():
+    w = make_workload("det", B=1, T=1024, T_valid=1020, H=2, d=128, cp=2, rope=True)
+    inp = make_inputs(w, seed=5)
+    a, b = run_gpu(w, inp), run_gpu(w, inp)
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+# ------------------------------------------------------------- merge ----
+
+@pytest.mark.parametrize("n,d,dtype", [(1, 64, torch.float32), (2, 128, torch.float32),
+                                       (5, 128, torch.bfloat16), (16, 64, torch.float32)])
+def test_merge_against_oracle(n, d, dtype):
+    B, H, T = 2, 3, 257
+    g = torch.Generator().manual_seed(n * 1000 + d)
+    o_parts = [torch.randn(B, H, T, d, generator=g) for _ in range(n)]
+    l_parts = [torch.randn(B, H, T, generator=g) * 3 for _ in range(n)]
+    for i, l in enumerate(l_parts):          # empty partials, incl. rows empty in every part
+        l[:, :, i::7] = -float("inf")
+        o_parts[i][:, :, i::7] = 0.0
+    l_parts[0][:, :, 5] = -float("inf")
+    for i in range(n):
+        l_parts[i][:, :, 5] = -float("inf")
+        o_parts[i][:, :, 5] = 0.0
+    o = torch.empty(B, H, T, d, dtype=dtype, device="cuda")
+    lse = torch.empty(B, H, T, device="cuda")
+    cpattn.merge([x.cuda() for x in o_parts], [x.cuda() for x in l_parts], o, lse)
+    torch.cuda.synchronize()
+    Ow, Lw = A.merge_many([x.double().numpy() for x in o_parts], [x.double().numpy() for x in l_parts])
+    tol = 1e-5 if dtype == torch.float32 else 2e-2
+    compare("merge_o", o.float().cpu(), Ow, tol)
+    compare("merge_lse", lse.cpu(), Lw, 1e-5)
+
+
+# ------------------------------------------------- full-size workloads ----
+
+def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
+    tol = TOL[w.dtype]
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
+    rows = sample_rows(w, n_random, seed=w.T)
+    real = rows[rows < w.T_valid]
+    for (b, h) in heads:
+        o_r, l_r = A.forward_rows(q, k, v, b, h, rows, w.causal, w.T_valid, w.rope)
+        compare(f"o[{b},{h}]", got["o"][b, h, rows], o_r, tol["o"], tol["cos"])
+        compare(f"lse[{b},{h}]", got["lse"][b, h, rows], l_r, tol["lse"])
+        dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, w.rope)
+        compare(f"dq[{b},{h}]", got["dq"][b, h, real], dq_r, tol["grad"], tol["cos"])
+    b, h = kv_head
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, w.rope)
+    compare(f"dk[{b},{h}]", got["dk"][b, h, rows], dk_c, tol["grad"], tol["cos"])
+    compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
+
+
+@pytest.mark.parametrize("name", ["gpt2_small", "long_16k", "window_32k", "padded_12289"])
+def test_workload_full_size_sampled(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, SEEDS[name])
+    got = run_gpu(w, inp)
+    for g in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.isfinite(got[g][:, :, : w.T_valid]).all(), g
+    heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
+    _sampled_check(w, inp, got, heads, kv_head=(w.B - 1, w.H // 3))
+    if w.T_valid < w.T:
+        for g in ("dq", "dk", "dv"):
+            assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
+        # gradient invariance: the padded run's real rows equal the unpadded oracle
+        wu = make_workload("unpadded", B=w.B, T=w.T_valid, H=w.H, d=w.d, cp=1, rope=w.rope,
+                           causal=w.causal, dtype=w.dtype, qkv_std=w.qkv_std)
+        inp_u = {k_: t[:, :, : w.T_valid] for k_, t in inp.items()}
+        rows = sample_rows(wu, 8, seed=3)
+        b, h = 1, 5
+        o_u, l_u = A.forward_rows(inp_u["q"], inp_u["k"], inp_u["v"], b, h, rows, True, w.T_valid, w.rope)
+        compare("o_vs_unpadded", got["o"][b, h, rows], o_u, TOL["bf16"]["o"], TOL["bf16"]["cos"])
+        dq_u = A.backward_dq_rows(inp_u["q"], inp_u["k"], inp_u["v"], inp_u["do"], b, h, rows, True,
+                                  w.T_valid, w.rope)
+        compare("dq_vs_unpadded", got["dq"][b, h, rows], dq_u, TOL["bf16"]["grad"], TOL["bf16"]["cos"])
+
+
+def test_error_codes_on_device_buffers():
+    x = torch.zeros(1, 1, 10, 64, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.shard(x, y, 2)            # T=10 is not a multiple of 4
+    assert e.value.status == cpattn.ERR_SHAPE
+    lse = torch.empty(1, 1, 10, device="cuda")
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.fwd(x, x, x, y, lse, cp=1, T_valid=11)
+    assert e.value.status == cpattn.ERR_SHAPE
+    cpattn.cpattn_sync_status(None)

@@ -1,0 +1,92 @@
+"""Host-side checks of the C-ABI library: it loads, exports every symbol its
+header declares, and validates arguments without touching a GPU."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from context_causal_attention_headtail_gb300 import cpattn
+from oracle import headtail as HT
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(cpattn.LIB_PATH):
+        from context_causal_attention_headtail_gb300 import build
+        build.build_library()
+    return cpattn.lib()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "cpattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(cpattn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(cpattn.EXPORTS) == names
+    assert "sm_103a" in cpattn.cpattn_version()
+
+
+def test_shard_index_host_only(lib):
+    for T, cp in [(8, 2), (48, 3), (4096, 4), (12296, 4)]:
+        assert cpattn.cpattn_shard_index(T, cp) == HT.shard_index(T, cp).tolist()
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.cpattn_shard_index(10, 2)
+    assert e.value.status == cpattn.ERR_SHAPE
+
+
+# Fake, aligned, non-null addresses: validation must reject before any device access.
+P = [0x100000 * (i + 1) for i in range(10)]
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(T=1000, cp=3), cpattn.ERR_SHAPE),          # T % (2 cp) != 0
+    (dict(d=96), cpattn.ERR_SHAPE),                  # unsupported head dim
+    (dict(T_valid=0), cpattn.ERR_SHAPE),
+    (dict(T_valid=1025), cpattn.ERR_SHAPE),
+    (dict(causal=2), cpattn.ERR_ARG),
+    (dict(dt=5), cpattn.ERR_DTYPE),
+    (dict(misalign=True), cpattn.ERR_ALIGN),
+    (dict(null=True), cpattn.ERR_ARG),
+    (dict(B=0), cpattn.ERR_SHAPE),
+])
+def test_fwd_validation(lib, args, status):
+    a = dict(B=1, T=1024, T_valid=1024, H=2, d=128, cp=2, causal=1, rope=1, dt=cpattn.BF16)
+    a.update({k: v for k, v in args.items() if k in a})
+    ptrs = list(P[:5])
+    if args.get("misalign"):
+        ptrs[1] += 8
+    if args.get("null"):
+        ptrs[2] = None
+    st = lib.cpattn_fwd(*ptrs, a["B"], a["T"], a["T_valid"], a["H"], a["d"], a["cp"], a["causal"],
+                        a["rope"], a["dt"], None)
+    assert st == status
+    assert cpattn.cpattn_last_error() != ""
+
+
+def test_bwd_and_merge_validation(lib):
+    ws = cpattn.cpattn_bwd_workspace_bytes(2, 4096, 12, 64)
+    assert ws >= 2 * 4096 * 12 * 4 and ws % 256 == 0
+    st = lib.cpattn_bwd(*P, 1, 1000, 1000, 2, 128, 3, 1, 1, cpattn.BF16, None)
+    assert st == cpattn.ERR_SHAPE
+    # gradient output aliasing an input is rejected
+    st = lib.cpattn_bwd(*(P[:6] + [P[0]] + P[7:]), 1, 1024, 1024, 2, 128, 2, 1, 1, cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG
+    arr = (ctypes.c_void_p * 17)(*([P[0]] * 17))
+    st = lib.cpattn_merge(arr, arr, 17, P[1], P[2], 1, 1, 8, 64, cpattn.F32, None)
+    assert st == cpattn.ERR_ARG
+    st = lib.cpattn_shard(P[0], P[0] + 8, 1, 1, 8, 64, 2, cpattn.BF16, None)
+    assert st == cpattn.ERR_ALIGN
+    st = lib.cpattn_shard(P[0], P[0] + 16, 1, 1, 8, 64, 2, cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG                    # overlapping src and dst
