@@ -1,0 +1,430 @@
+#!/usr/bin/env python3
+"""Benchmark of HeadTail ring (context-parallel) causal attention, fwd + bwd.
+
+One step = the whole hot path over one batch of synthetic inputs resident in
+HBM: HeadTail shard of q, k, v, dO -> ring attention forward (O, LSE) ->
+backward (D preprocess, dK/dV kernel, dQ kernel) -> unshard of O, dQ, dK, dV.
+Every step of it runs in libcpattn's CUDA kernels, called through the C ABI.
+
+value  = algorithmic causal fwd+bwd TFLOP/s (7 * B * H * T^2 * d / 2 ... see
+         flops below) summed over ranks / max-over-ranks step time.
+e2e    = the same metric with pinned-host -> device copies of q, k, v, dO and
+         device -> host copies of O, LSE, dQ, dK, dV inside the timed region.
+roofline: the kernel with the most device time per step, timed live with CUDA
+         events that the library records at kernel boundaries.
+cpu_baseline: the float64 CPU oracle, timed on a bounded sample (rank 0, N=1).
+
+N > 1 (torchrun): every rank runs its own replica on its own batch (the
+(b, h) problems are independent), so there is no collective on the data path;
+only the timing uses a barrier and a max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal attn fwd+bwd TFLOP/s & tokens/s at T=32k, % of GB300 BF16 TC peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "window_32k"
+
+# DRAM bytes (read + write) per launch from ncu captures of the named kernel on
+# the 32k workload, by the command written in profiles/; None when no capture
+# of the current kernel exists.
+NCU_TRAFFIC_BYTES = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rope-in-kernel", action="store_true",
+                    help="rotate q, k inside the attention kernels (rope=1) instead of in shard/unshard")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "T": w.T, "T_valid": w.T_valid, "H": w.H, "d": w.d,
+            "cp": w.cp, "causal": w.causal, "rope": w.rope,
+            "l2": "inputs larger than L2: q,k,v,dO = %d MiB per step vs 129 MB L2"
+                  % (4 * w.B * w.H * w.T * w.d * 2 // 2 ** 20)}
+
+
+# --------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        sm, smax, reasons, power = [], [], set(), []
+        for line in self.out.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.out.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------- CPU oracle ----
+
+_INPUT_CACHE = {}
+
+
+def _workload_inputs(w):
+    from context_causal_attention_headtail_gb300.synth import SEEDS, make_inputs
+    if w.name not in _INPUT_CACHE:
+        _INPUT_CACHE[w.name] = make_inputs(w, SEEDS.get(w.name, 1234))
+    return _INPUT_CACHE[w.name]
+
+
+def oracle_sample(w, seconds_target=12.0, max_heads=8):
+    """Times the float64 oracle on a bounded sample of the workload.
+
+    Sample: full forward + backward of whole heads (b=0, h=0,1,...) over the
+    first T_s tokens of the workload's own inputs. For causal attention the
+    first T_s output rows of a head are exactly that prefix's attention, so
+    this is a slice of the same problem; its algorithmic work is
+    7 * T_s^2 * d flops per head (3.5 x the causal forward 2 * T_s^2 * d).
+    """
+    from oracle import attention as A
+
+    T_s = min(w.T_valid, 4096)
+    inp = _workload_inputs(w)
+    q, k, v, do = (inp[n][0:1, :, :T_s].double().numpy() for n in ("q", "k", "v", "do"))
+    heads, t0 = 0, time.perf_counter()
+    while heads < min(max_heads, w.H):
+        sl = slice(heads, heads + 1)
+        O, L = A.forward(q[:, sl], k[:, sl], v[:, sl], w.causal, T_s, w.rope)
+        A.backward(q[:, sl], k[:, sl], v[:, sl], O, L, do[:, sl], w.causal, T_s, w.rope)
+        heads += 1
+        if time.perf_counter() - t0 >= seconds_target:
+            break
+    dt = time.perf_counter() - t0
+    flops = heads * 7.0 * T_s * T_s * w.d * (0.5 if w.causal else 1.0) * 2.0
+    return {"seconds": dt, "flops": flops, "tokens": heads * T_s, "T_s": T_s, "heads": heads,
+            "cores": os.cpu_count(),
+            "blas_threads": os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+            or str(os.cpu_count())}
+
+
+def cpu_baseline_entry(w, s):
+    tflops = s["flops"] / s["seconds"] / 1e12
+    return {"value": tflops, "unit": UNIT, "cores": int(s["blas_threads"]), "kind": "oracle",
+            "tokens_per_s": s["tokens"] / s["seconds"],
+            "sample": (f"float64 oracle forward+backward of {s['heads']} head(s), first {s['T_s']} "
+                       f"tokens of the {w.name} inputs (b=0), {s['seconds']:.1f} s on the host")}
+
+
+def run_reference(args):
+    """--impl reference: the oracle, timed as it stands on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from context_causal_attention_headtail_gb300.synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        oracle_sample(w, seconds_target=0.0, max_heads=1)
+    times, samples = [], []
+    for _ in range(args.steps):
+        s = oracle_sample(w, seconds_target=0.0, max_heads=1)
+        times.append(s["seconds"])
+        samples.append(s)
+    tot_flops = sum(s["flops"] for s in samples)
+    tot_t = sum(times)
+    value = tot_flops / tot_t / 1e12
+    base = cpu_baseline_entry(w, {**samples[0], "seconds": tot_t, "flops": tot_flops,
+                                  "tokens": sum(s["tokens"] for s in samples),
+                                  "heads": sum(s["heads"] for s in samples)})
+    base["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w), "cpu_baseline": base,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU ----
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from context_causal_attention_headtail_gb300 import cpattn
+    from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make_inputs
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("bench runs the bf16 tensor-core path; pick a bf16 workload")
+
+    inp = make_inputs(w, SEEDS[w.name] + rank)
+    if rank == 0:
+        _INPUT_CACHE[w.name] = inp
+    host_in = {k: v.pin_memory() for k, v in inp.items()}
+    nat = {k: v.to(dev) for k, v in inp.items()}
+    sh = {k: torch.empty_like(v) for k, v in nat.items()}
+    o, dq, dk, dv = (torch.empty_like(sh["q"]) for _ in range(4))
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8, device=dev)
+    outs = {"o": o, "dq": dq, "dk": dk, "dv": dv}
+    outs_nat = {k: torch.empty_like(v) for k, v in outs.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    stream = torch.cuda.current_stream(dev)
+
+    kernels = ["shard", "fwd", "bwd_D", "bwd_dkdv", "bwd_dq", "unshard"]
+    launches_per_step = 4 + 1 + 3 + 4
+
+    def new_events():
+        evs = {"shard": [], "unshard": []}
+        for _ in range(4):
+            evs["shard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            evs["unshard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+        evs["fwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        evs["bwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for e in [x for p in evs["shard"] + evs["unshard"] for x in p] + evs["fwd"] + evs["bwd"]:
+            e.record(stream)   # creates the underlying CUDA event so its handle can be passed down
+        return evs
+
+    # RoPE at global positions: fused into the shard / unshard passes of q, k
+    # and dq, dk (default), or applied inside the attention kernels.
+    fused = w.rope and not args.rope_in_kernel
+    rope_flag = w.rope and not fused
+
+    def step(evs=None):
+        for i, name in enumerate(("q", "k", "v", "do")):
+            if evs:
+                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
+            if fused and name in ("q", "k"):
+                cpattn.shard_rope(nat[name], sh[name], w.cp, stream)
+            else:
+                cpattn.shard(nat[name], sh[name], w.cp, stream)
+        if evs:
+            cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["fwd"]])
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream)
+        if evs:
+            cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["bwd"]])
+        cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
+                   w.causal, rope_flag, stream)
+        for i, name in enumerate(("o", "dq", "dk", "dv")):
+            if evs:
+                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
+            if fused and name in ("dq", "dk"):
+                cpattn.unshard_rope(outs[name], outs_nat[name], w.cp, stream)
+            else:
+                cpattn.unshard(outs[name], outs_nat[name], w.cp, stream)
+        if evs:
+            cpattn.cpattn_set_trace_events([])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    cpattn.cpattn_sync_status(stream.cuda_stream)
+
+    step_events = [new_events() for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    sampler = ClockSampler(gpu_id)
+    torch.cuda.synchronize(dev)
+    barrier()
+    sampler.start()
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        step(step_events[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop()
+    cpattn.cpattn_sync_status(stream.cuda_stream)
+    ms_local = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms_local)
+
+    # per-kernel device time per step (averaged over the timed steps)
+    ker_ms = {k: 0.0 for k in kernels}
+    for evs in step_events:
+        ker_ms["shard"] += sum(a.elapsed_time(b) for a, b in evs["shard"])
+        ker_ms["unshard"] += sum(a.elapsed_time(b) for a, b in evs["unshard"])
+        ker_ms["fwd"] += evs["fwd"][0].elapsed_time(evs["fwd"][1])
+        b = evs["bwd"]
+        ker_ms["bwd_D"] += b[0].elapsed_time(b[1])
+        ker_ms["bwd_dkdv"] += b[1].elapsed_time(b[2])
+        ker_ms["bwd_dq"] += b[2].elapsed_time(b[3])
+    ker_ms = {k: v / args.steps for k, v in ker_ms.items()}
+
+    # e2e through the same public API, host buffers in and out
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s2.record(stream)
+        for _ in range(args.steps):
+            for k_ in nat:
+                nat[k_].copy_(host_in[k_], non_blocking=True)
+            step()
+            for k_ in outs_nat:
+                host_out[k_].copy_(outs_nat[k_], non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+        e2.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
+        e2e = {"value": world * w.fwdbwd_flops() / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "tokens_per_s": world * w.B * w.T_valid / (e2e_ms * 1e-3)}
+
+    peaks = measured_peaks()
+    unit_flops = w.fwd_flops() / 2.0          # one GEMM over the live causal pairs
+    elt = 2
+    tensor_bytes = w.B * w.H * w.T * w.d * elt
+    ker_work = {
+        "fwd": ("tensor", 2 * unit_flops),
+        "bwd_dkdv": ("tensor", 4 * unit_flops),
+        "bwd_dq": ("tensor", 1 * unit_flops),     # S and dP recomputation is not credited
+        "bwd_D": ("hbm", 2 * tensor_bytes + w.B * w.H * w.T * 4),
+        "shard": ("hbm", 4 * 2 * tensor_bytes),
+        "unshard": ("hbm", 4 * 2 * tensor_bytes),
+    }
+    ker_rep = {}
+    for name, (bound, work) in ker_work.items():
+        t = ker_ms[name] * 1e-3
+        if bound == "tensor":
+            ach = work / t / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            ker_rep[name] = {"ms": ker_ms[name], "bound": "tensor", "achieved": ach, "unit": "TFLOP/s",
+                             "frac": ach / peak}
+        else:
+            ach = work / t / 1e9
+            ker_rep[name] = {"ms": ker_ms[name], "bound": "hbm", "achieved": ach, "unit": "GB/s",
+                             "frac": ach / peaks["hbm_gbs"]}
+    dom = max(("fwd", "bwd_dkdv", "bwd_dq", "bwd_D"), key=lambda k: ker_ms[k])
+    d = ker_rep[dom]
+    roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"],
+                "peak": peaks["bf16_tflops_sustained"] if d["bound"] == "tensor" else peaks["hbm_gbs"],
+                "unit": d["unit"], "frac": d["frac"], "traffic": NCU_TRAFFIC_BYTES.get(dom),
+                "peak_source": f"{peaks['source']} "
+                               + ("bf16_tflops_sustained (kernel timed inside a long step)"
+                                  if d["bound"] == "tensor" else "hbm_gbs"),
+                "work_per_launch": ker_work[dom][1]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_entry(w, oracle_sample(w))
+
+    value = world * w.fwdbwd_flops() / (ms * 1e-3) / 1e12
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {**workload_config(w), "parallelism": f"replica per GPU x{world}",
+                           "rope_path": ("fused into shard/unshard" if fused else
+                                         "inside the attention kernels" if rope_flag else "none")},
+                "tokens_per_s": world * w.B * w.T_valid / (ms * 1e-3),
+                "frac_of_bf16_peak": value / world / peaks["bf16_tflops_sustained"],
+                "fwd_tflops": w.fwd_flops() / (ker_ms["fwd"] * 1e-3) / 1e12,
+                "e2e": e2e, "roofline": roofline, "kernels": ker_rep, "cpu_baseline": cpu,
+                "clocks": clocks, "gpu_launches": launches_per_step * args.steps}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

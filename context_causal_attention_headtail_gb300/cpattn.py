@@ -19,9 +19,10 @@ OK, ERR_ARG, ERR_SHAPE, ERR_DTYPE, ERR_ALIGN, ERR_CUDA, ERR_TIMEOUT, ERR_UNSUPPO
 F32, BF16 = 0, 1
 
 # Every symbol the header declares.
-EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_index", "cpattn_fwd",
+EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshard_rope",
+           "cpattn_shard_index", "cpattn_fwd",
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
-           "cpattn_sync_status", "cpattn_version")
+           "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events")
 
 
 class CpattnError(RuntimeError):
@@ -39,11 +40,14 @@ def _declare(lib):
     sig = {
         "cpattn_shard": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
         "cpattn_unshard": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_shard_rope": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_unshard_rope": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
         "cpattn_shard_index": [_i, _i, _c.POINTER(_c.c_int32)],
         "cpattn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp],
         "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
+        "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -84,6 +88,14 @@ def cpattn_unshard(src, dst, B, H, T, d, cp, dt, stream=None):
     _check(lib().cpattn_unshard(src, dst, B, H, T, d, cp, dt, stream))
 
 
+def cpattn_shard_rope(src, dst, B, H, T, d, cp, dt, stream=None):
+    _check(lib().cpattn_shard_rope(src, dst, B, H, T, d, cp, dt, stream))
+
+
+def cpattn_unshard_rope(src, dst, B, H, T, d, cp, dt, stream=None):
+    _check(lib().cpattn_unshard_rope(src, dst, B, H, T, d, cp, dt, stream))
+
+
 def cpattn_shard_index(T, cp):
     buf = (ctypes.c_int32 * T)()
     _check(lib().cpattn_shard_index(T, cp, buf))
@@ -113,6 +125,13 @@ def cpattn_merge(o_parts, lse_parts, o, lse, B, H, T, d, dt, stream=None):
 
 def cpattn_sync_status(stream=None):
     _check(lib().cpattn_sync_status(stream))
+
+
+def cpattn_set_trace_events(events):
+    """events: list of raw cudaEvent_t handles (ints), or [] to turn tracing off."""
+    n = len(events)
+    arr = (ctypes.c_void_p * max(n, 1))(*events) if n else None
+    _check(lib().cpattn_set_trace_events(arr, n))
 
 
 def cpattn_last_error():
@@ -154,6 +173,16 @@ def shard(src, dst, cp, stream=None):
 def unshard(src, dst, cp, stream=None):
     B, H, T, d = src.shape
     cpattn_unshard(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+
+
+def shard_rope(src, dst, cp, stream=None):
+    B, H, T, d = src.shape
+    cpattn_shard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+
+
+def unshard_rope(src, dst, cp, stream=None):
+    B, H, T, d = src.shape
+    cpattn_unshard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
 
 
 def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None):

@@ -12,6 +12,12 @@
 namespace cpattn {
 
 static thread_local char g_msg[512] = "";
+static thread_local cudaEvent_t g_trace[8];
+static thread_local int g_ntrace = 0;
+
+void trace_record(int i, cudaStream_t s) {
+  if (i < g_ntrace && g_trace[i]) cudaEventRecord(g_trace[i], s);
+}
 
 cpattn_status fail(cpattn_status s, const char *fmt, ...) {
   va_list ap;
@@ -115,6 +121,15 @@ const char *cpattn_last_error(void) { return g_msg; }
 
 const char *cpattn_version(void) { return "cpattn 0.1 sm_103a"; }
 
+cpattn_status cpattn_set_trace_events(void *const *events, int n) {
+  g_msg[0] = 0;
+  if (n < 0 || n > 8) return fail(CPATTN_ERR_ARG, "n=%d must be in [0, 8]", n);
+  if (!events) n = 0;
+  for (int i = 0; i < 8; ++i) g_trace[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  g_ntrace = n;
+  return CPATTN_OK;
+}
+
 cpattn_status cpattn_sync_status(cpattn_stream_t stream) {
   g_msg[0] = 0;
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
@@ -148,7 +163,8 @@ cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host) {
 }
 
 static cpattn_status shard_common(const void *src, void *dst, int B, int H, int T, int d, int cp,
-                                  cpattn_dtype dt, cpattn_stream_t stream, bool inverse) {
+                                  cpattn_dtype dt, cpattn_stream_t stream, bool inverse,
+                                  bool rope = false) {
   g_msg[0] = 0;
   if (!src || !dst) return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_common(B, H, T, d, cp);
@@ -159,8 +175,14 @@ static cpattn_status shard_common(const void *src, void *dst, int B, int H, int 
   if (!aligned16(src) || !aligned16(dst)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
   const size_t bytes = (size_t)B * H * T * d * elt;
   if (overlaps(src, bytes, dst, bytes)) return fail(CPATTN_ERR_ARG, "src and dst overlap");
-  Geometry g = geometry(B, H, T, T, d, cp, 1, 0);
-  return launch_shard(src, dst, g, elt, inverse, reinterpret_cast<cudaStream_t>(stream));
+  if (rope && d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: RoPE needs d in {64, 128}", d);
+  if (rope && T > (1 << 24)) return fail(CPATTN_ERR_SHAPE, "T=%d exceeds 2^24", T);
+  Geometry g = geometry(B, H, T, T, d, cp, 1, rope ? 1 : 0);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  trace_record(0, s);
+  st = rope ? launch_shard_rope(src, dst, g, dt, inverse, s) : launch_shard(src, dst, g, elt, inverse, s);
+  trace_record(1, s);
+  return st;
 }
 
 cpattn_status cpattn_shard(const void *src, void *dst, int B, int H, int T, int d, int cp,
@@ -171,6 +193,16 @@ cpattn_status cpattn_shard(const void *src, void *dst, int B, int H, int T, int 
 cpattn_status cpattn_unshard(const void *src, void *dst, int B, int H, int T, int d, int cp,
                              cpattn_dtype dt, cpattn_stream_t stream) {
   return shard_common(src, dst, B, H, T, d, cp, dt, stream, true);
+}
+
+cpattn_status cpattn_shard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                cpattn_dtype dt, cpattn_stream_t stream) {
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, false, true);
+}
+
+cpattn_status cpattn_unshard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                  cpattn_dtype dt, cpattn_stream_t stream) {
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, true, true);
 }
 
 cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -189,10 +221,14 @@ cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, f
     return fail(CPATTN_ERR_ARG, "outputs overlap inputs");
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  trace_record(0, s);
   if (dt == CPATTN_F32)
-    return launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
-                          static_cast<const float *>(v), static_cast<float *>(o), lse, g, s);
-  return launch_fwd_bf16(q, k, v, o, lse, g, s);
+    st = launch_fwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                        static_cast<const float *>(v), static_cast<float *>(o), lse, g, s);
+  else
+    st = launch_fwd_bf16(q, k, v, o, lse, g, s);
+  trace_record(1, s);
+  return st;
 }
 
 size_t cpattn_bwd_workspace_bytes(int B, int T, int H, int d) {
@@ -229,14 +265,19 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
+  trace_record(0, s);
   st = launch_bwd_preprocess(o, dO, D, (long long)B * H * T, d, dt, s);
+  trace_record(1, s);
   if (st != CPATTN_OK) return st;
   if (dt == CPATTN_F32)
-    return launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+    st = launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                           static_cast<const float *>(v), static_cast<const float *>(o), lse,
                           static_cast<const float *>(dO), static_cast<float *>(dq),
                           static_cast<float *>(dk), static_cast<float *>(dv), D, g, s);
-  return launch_bwd_bf16(q, k, v, o, lse, dO, dq, dk, dv, D, g, s);
+  else
+    st = launch_bwd_bf16(q, k, v, o, lse, dO, dq, dk, dv, D, g, s);
+  trace_record(3, s);
+  return st;
 }
 
 cpattn_status cpattn_merge(const float *const *o_parts, const float *const *lse_parts, int n,

@@ -557,6 +557,7 @@ cpattn_status launch_bwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
     kern<<<grid, threads, smem, s>>>(mq, mk, mv, mdo, bp);
     cpattn_status st = check_launch("tensor-core dK/dV kernel");
     if (st != CPATTN_OK) return st;
+    trace_record(2, s);
   }
   {
     constexpr int smem = DqCfg<D>::SMEM;

@@ -317,6 +317,306 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Paired-tile forward (inputs already rotated, or no RoPE). One CTA owns two
+// consecutive 128-row query tiles Q0, Q1 of one chunk and streams each K/V
+// tile once for both. Two softmax warpgroups (warps 0-3 for Q0, 4-7 for Q1)
+// alternate with the MMA issuer so that while one warpgroup turns S_i into
+// P_i, the tensor core works on the other tile:
+//   S0(n) S1(n) | PV0(n) S0(n+1) | PV1(n) S1(n+1) | PV0(n+1) ...
+// TMEM columns: S0/P0 0, S1/P1 128, O0 256, O1 256 + D (512 allocated).
+// Warp 8: TMA producer (lane 0) and TMEM allocator; warp 9: MMA issuer.
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;   // stages of the K ring and of the V ring
+  static constexpr int TILE = kTile * D * 2;
+  static constexpr int OFF_Q = 0;                 // Q0, Q1
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // q_full, fin, s_full[2], p_full[2], o_done[2], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS]
+  static constexpr int NBAR = 8 + 4 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    fwd2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+  using C = Fwd2Cfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  auto sQ = [&](int i) { return sbase + C::OFF_Q + i * C::TILE; };
+  auto sK = [&](int st) { return sbase + C::OFF_K + st * C::TILE; };
+  auto sV = [&](int st) { return sbase + C::OFF_V + st * C::TILE; };
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_q_full = bar0, bar_fin = bar0 + 8;
+  auto bar_s_full = [&](int i) { return bar0 + 16 + 8 * i; };
+  auto bar_p_full = [&](int i) { return bar0 + 32 + 8 * i; };
+  auto bar_o_done = [&](int i) { return bar0 + 48 + 8 * i; };
+  auto bar_k_full = [&](int st) { return bar0 + 64 + 8 * st; };
+  auto bar_k_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  auto bar_v_full = [&](int st) { return bar0 + 64 + 16 * NS + 8 * st; };
+  auto bar_v_empty = [&](int st) { return bar0 + 64 + 24 * NS + 8 * st; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  constexpr uint32_t colO0 = 256;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cp = p.cp, c = p.c, tpc = p.tpc;
+  const int ppc = (tpc + 1) / 2;                  // tile pairs per chunk
+  const int bh = blockIdx.x % p.BH;
+  const int g = blockIdx.x / p.BH;
+  const int kq = 2 * cp - 1 - g / ppc;            // latest chunks first: they carry the most work
+  const int pq = ppc - 1 - g % ppc;
+  int rq, hq;
+  owner_of(kq, cp, rq, hq);
+  const int q_z = bh * 2 * cp + 2 * rq + hq;
+  const int y0 = pq * 2 * kTile;                  // first row of Q0 inside the chunk
+  const int q_pos0 = kq * c + y0;
+  const int q_rows = min(2 * kTile, c - y0);      // valid rows of the pair
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const uint32_t b = bar0 + 8 * i;
+      tc::mbar_init(b, (b == bar_p_full(0) || b == bar_p_full(1)) ? 128 : 1);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const tc::WaitCtx wc{abort_flag, p.err};
+  const tc::WaitCtx drain{abort_flag + 1, p.err};
+
+  KvSchedule sched;
+  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
+  TileInfo t;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+      tc::mbar_arrive_expect_tx(bar_q_full, 2 * C::TILE);
+      for (int i = 0; i < 2; ++i)
+        for (int blk = 0; blk < D / 64; ++blk)
+          tc::tma_load_3d(sQ(i) + blk * kTile * 128, &tm_q, bar_q_full, blk * 64, y0 + i * kTile, q_z);
+      int n = 0;
+      while (sched.next(t)) {
+        const int st = n % NS;
+        const int z = bh * 2 * cp + t.slot;
+        if (n >= NS && !tc::mbar_wait(bar_k_empty(st), ((n / NS) - 1) & 1, wc)) break;
+        tc::mbar_arrive_expect_tx(bar_k_full(st), C::TILE);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_k_full(st), blk * 64, t.y0, z);
+        if (n >= NS && !tc::mbar_wait(bar_v_empty(st), ((n / NS) - 1) & 1, wc)) break;
+        tc::mbar_arrive_expect_tx(bar_v_full(st), C::TILE);
+        for (int blk = 0; blk < D / 64; ++blk)
+          tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_v_full(st), blk * 64, t.y0, z);
+        ++n;
+      }
+      tc::mbar_wait(bar_q_full, 0, drain);
+      for (int m = (n > NS ? n - NS : 0); m < n; ++m) {
+        tc::mbar_wait(bar_k_full(m % NS), (m / NS) & 1, drain);
+        tc::mbar_wait(bar_v_full(m % NS), (m / NS) & 1, drain);
+      }
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idPV = tc::idesc_bf16(128, D, false, true);
+      auto issue_s = [&](int i, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ss(tmem + i * 128, tc::desc_kmajor(sQ(i), kTile, kk), tc::desc_kmajor(sK(st), kTile, kk), idS,
+                     kk > 0);
+        tc::mma_commit(bar_s_full(i));
+      };
+      auto issue_pv = [&](int i, int st, int n) {
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk)
+          tc::mma_ts(tmem + colO0 + i * D, tmem + i * 128 + kk * 8, tc::desc_mnmajor(sV(st), kTile, kk), idPV,
+                     (n > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(bar_o_done(i));
+      };
+      bool ok = tc::mbar_wait(bar_q_full, 0, wc);
+      if (ok && sched.next(t)) {
+        ok = tc::mbar_wait(bar_k_full(0), 0, wc);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_s(0, 0);
+          issue_s(1, 0);
+          tc::mma_commit(bar_k_empty(0));
+        }
+        for (int n = 0; ok; ++n) {
+          const bool more = sched.next(t);
+          const int st = n % NS, st1 = (n + 1) % NS;
+          // ---- tile 0: PV0(n), then S0(n+1) once PV0(n) has read P0
+          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
+          if (!(ok = tc::mbar_wait(bar_v_full(st), (n / NS) & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_pv(0, st, n);
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_k_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = tc::mbar_wait(bar_o_done(0), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_s(0, st1);
+          }
+          // ---- tile 1: PV1(n), then S1(n+1)
+          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_pv(1, st, n);
+          tc::mma_commit(bar_v_empty(st));
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_o_done(1), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_s(1, st1);
+            tc::mma_commit(bar_k_empty(st1));
+          }
+          if (!more) break;
+        }
+      }
+      tc::mma_commit(bar_fin);
+      tc::mbar_wait(bar_fin, 0, drain);
+    }
+  } else {
+    // ----------------------------------------------- softmax warpgroups 0, 1
+    const int wg = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const int prow = wg * kTile + row;          // row within the pair
+    const int q_pos = q_pos0 + prow;
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t t_s = t_row + wg * 128;
+    const uint32_t t_o = t_row + colO0 + wg * D;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY, l = 0.f;
+    int n = 0;
+    bool ok = true;
+    while (sched.next(t)) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(wg), n & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+      // pass 1: masked row max
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
+        tc::tmem_ld_wait();
+        if (t.need_mask) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int j = cb * 32 + e, kp = t.pos0 + j;
+            const bool keep = (j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos);
+            mx[e & 3] = fmaxf(mx[e & 3], keep ? __uint_as_float(r[e]) : -INFINITY);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[e]));
+        }
+      }
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float m_new = fmaxf(m_run, mt * sl2);
+      bool need = m_new > m_run + 8.f;
+      if (n == 0) {
+        m_run = m_new;
+        need = false;
+      } else if (__any_sync(0xffffffffu, need)) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done(wg), (n - 1) & 1, wc));
+        if (!ok) break;
+        tc::tc_fence_after();
+        const float alpha = need ? tc::ex2(m_run - m_new) : 1.f;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_o + cb * 32, r);
+          tc::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+          tc::tmem_st32(t_o + cb * 32, r);
+        }
+        tc::tmem_st_wait();
+        if (need) {
+          l *= alpha;
+          m_run = m_new;
+        }
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // pass 2: P = 2^(S*scale*log2e - m) -> bf16 over S
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float v0 = __uint_as_float(r[2 * e]), v1 = __uint_as_float(r[2 * e + 1]);
+          if (t.need_mask) {
+            const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
+            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
+            if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
+          }
+          const float p0 = tc::ex2(fmaf(v0, sl2, -m_use)), p1 = tc::ex2(fmaf(v1, sl2, -m_use));
+          ls[(2 * e) & 3] += p0;
+          ls[(2 * e + 1) & 3] += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tc::tmem_st16(t_s + cb * 16, pk);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_p_full(wg));
+      ++n;
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done(wg), (n - 1) & 1, wc));
+      if (ok) {
+        tc::tc_fence_after();
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const bool valid = prow < q_rows;
+        const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y0 + prow);
+        uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
+#pragma unroll 1
+        for (int cb = 0; cb < D / 32; ++cb) {
+          uint32_t r[32];
+          tc::tmem_ld32(t_o + cb * 32, r);
+          tc::tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[cb * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid) p.lse[grow] = l > 0.f ? (m_run + log2f(l)) * 0.693147180559945309f : -INFINITY;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots) {
@@ -333,6 +633,17 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 }
 
 namespace {
+
+template <int D>
+cpattn_status launch_fwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                            const FwdParams &fp, unsigned grid, cudaStream_t s) {
+  constexpr int smem = Fwd2Cfg<D>::SMEM;
+  auto kern = fwd2_tc_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the forward kernel", smem);
+  kern<<<grid, 320, smem, s>>>(mq, mk, mv, fp);
+  return check_launch("tensor-core forward kernel (paired tiles)");
+}
 
 template <int D, bool ROPE>
 cpattn_status launch_fwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
@@ -368,6 +679,12 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   fp.tpc = (g.c + kTile - 1) / kTile;
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
   make_rope_theta(g.d, &fp.theta);
+  if (!g.rope) {   // paired query tiles; q, k are used as given
+    const long long grid2 = BH * 2 * g.cp * ((fp.tpc + 1) / 2);
+    if (grid2 > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
+    return g.d == 128 ? launch_fwd2_t<128>(mq, mk, mv, fp, (unsigned)grid2, s)
+                      : launch_fwd2_t<64>(mq, mk, mv, fp, (unsigned)grid2, s);
+  }
   const long long grid = BH * 2 * g.cp * fp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
   if (g.d == 128)

@@ -39,6 +39,8 @@ struct Geometry {
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------
 cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
                            bool inverse, cudaStream_t s);
+cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
+                                bool inverse, cudaStream_t s);
 cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,
                              float *lse, const Geometry &g, cudaStream_t s);
 cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,
@@ -54,6 +56,10 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
 cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const void *o,
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               float *D, const Geometry &g, cudaStream_t s);
+
+// Tracing events registered by cpattn_set_trace_events for this host thread:
+// records event i on stream s if one is registered (no-op otherwise).
+void trace_record(int i, cudaStream_t s);
 
 // cuTensorMapEncodeTiled, resolved through the runtime's driver entry point.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

@@ -70,6 +70,133 @@ cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int el
   return check_launch(inverse ? "unshard kernel" : "shard kernel");
 }
 
+// ------------------------------------------------------- shard + RoPE ---
+// HeadTail shard fused with RoPE, and its adjoint fused with unshard, so that
+// the rotation runs inside a pass that already reads and writes every element
+// of q and k. Natural row t of chunk kappa has position p = kappa*c + o.
+//   forward  (shard):   dst[sigma(t)] = R(p) src[t]
+//   adjoint  (unshard): dst[t] = R(p)^T src[sigma(t)]
+// A lane owns VEC consecutive frequencies f0..f0+VEC-1 (one 16-byte word from
+// each half of the row) and walks up to 256/RS rows of one chunk with stride
+// RS; its cos/sin are seeded with rope_sincos and advanced by an exact
+// angle-addition step of RS rows (error grows ~1 ulp per step, <= 16 steps).
+template <typename T>
+struct VecOf;
+template <>
+struct VecOf<__nv_bfloat16> { static constexpr int N = 8; };
+template <>
+struct VecOf<float> { static constexpr int N = 4; };
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4 &u, float *x);
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4 &u, float *x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { x[2 * i] = bf16lo_to_f32(w[i]); x[2 * i + 1] = bf16hi_to_f32(w[i]); }
+}
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4 &u, float *x) {
+  x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+  x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+}
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float *x);
+template <>
+__device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float *x) {
+  return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                    pack_bf16x2(x[6], x[7]));
+}
+template <>
+__device__ __forceinline__ uint4 pack16<float>(const float *x) {
+  return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                    __float_as_uint(x[3]));
+}
+
+constexpr int kRopeRowsPerBlock = 256;
+
+// grid: x = row blocks of 256 rows within a chunk, y = (b,h,kappa) chunks.
+// block: 256 threads = (D/2)/VEC frequency groups x the rest as row lanes.
+template <typename T, int D, bool INVERSE>
+__global__ void __launch_bounds__(256) shard_rope_kernel(const T *__restrict__ src, T *__restrict__ dst,
+                                                         int cp, int c, long long n_chunks, RopeTheta th) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int GROUPS = (D / 2) / VEC;       // frequency groups per row
+  constexpr int RS = 256 / GROUPS;            // rows advanced per step
+  const int grp = threadIdx.x % GROUPS, lrow = threadIdx.x / GROUPS;
+  const int f0 = grp * VEC;
+  const int two_cp = 2 * cp;
+  for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
+    const long long bh = ch / two_cp;
+    const int kappa = (int)(ch % two_cp);
+    int r, half;
+    owner_of(kappa, cp, r, half);
+    const long long nat0 = (bh * two_cp + kappa) * (long long)c;       // first natural row of the chunk
+    const long long shd0 = (bh * two_cp + 2 * r + half) * (long long)c;
+    const int row_begin = blockIdx.x * kRopeRowsPerBlock + lrow;
+    const int row_end = min(c, (int)(blockIdx.x + 1) * kRopeRowsPerBlock);
+    if (row_begin >= row_end) continue;
+    float cs[VEC], sn[VEC], cd[VEC], sd[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      rope_sincos(kappa * c + row_begin, th.hi[f0 + v], th.lo[f0 + v], sn[v], cs[v]);
+      rope_sincos(RS, th.hi[f0 + v], th.lo[f0 + v], sd[v], cd[v]);
+    }
+    for (int o = row_begin; o < row_end; o += RS) {
+      const T *in = src + ((INVERSE ? shd0 : nat0) + o) * D;
+      T *out = dst + ((INVERSE ? nat0 : shd0) + o) * D;
+      const uint4 ua = *reinterpret_cast<const uint4 *>(in + f0);
+      const uint4 ub = *reinterpret_cast<const uint4 *>(in + f0 + D / 2);
+      float x[VEC], y[VEC];
+      unpack16<T>(ua, x);
+      unpack16<T>(ub, y);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        const float s_ = INVERSE ? -sn[v] : sn[v];
+        const float xr = fmaf(x[v], cs[v], -y[v] * s_);
+        const float yr = fmaf(y[v], cs[v], x[v] * s_);
+        x[v] = xr;
+        y[v] = yr;
+        const float nc = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
+        const float ns = fmaf(sn[v], cd[v], cs[v] * sd[v]);
+        cs[v] = nc;
+        sn[v] = ns;
+      }
+      *reinterpret_cast<uint4 *>(out + f0) = pack16<T>(x);
+      *reinterpret_cast<uint4 *>(out + f0 + D / 2) = pack16<T>(y);
+    }
+  }
+}
+
+template <typename T, int D>
+static void launch_shard_rope_t(const void *src, void *dst, const Geometry &g, bool inverse,
+                                const RopeTheta &th, cudaStream_t s) {
+  const long long n_chunks = (long long)g.B * g.H * 2 * g.cp;
+  const unsigned gx = (unsigned)((g.c + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock);
+  const unsigned gy = (unsigned)(n_chunks < 65535 ? n_chunks : 65535);
+  dim3 grid(gx, gy);
+  if (inverse)
+    shard_rope_kernel<T, D, true><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
+                                                       g.cp, g.c, n_chunks, th);
+  else
+    shard_rope_kernel<T, D, false><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
+                                                        g.cp, g.c, n_chunks, th);
+}
+
+cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
+                                bool inverse, cudaStream_t s) {
+  RopeTheta th;
+  make_rope_theta(g.d, &th);
+  if (dt == CPATTN_BF16) {
+    if (g.d == 128) launch_shard_rope_t<__nv_bfloat16, 128>(src, dst, g, inverse, th, s);
+    else launch_shard_rope_t<__nv_bfloat16, 64>(src, dst, g, inverse, th, s);
+  } else {
+    if (g.d == 128) launch_shard_rope_t<float, 128>(src, dst, g, inverse, th, s);
+    else launch_shard_rope_t<float, 64>(src, dst, g, inverse, th, s);
+  }
+  return check_launch(inverse ? "unshard+RoPE kernel" : "shard+RoPE kernel");
+}
+
 // ------------------------------------------------------------- D = dO.O ---
 template <typename T>
 __device__ __forceinline__ float ld_f(const T *p);
@@ -424,11 +551,13 @@ cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, con
   const long long rows = (long long)g.B * g.H * g.T;
   const unsigned blocks = (unsigned)((rows + 3) / 4);
   if (g.d == 128) {
-    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
     bwd_dkdv_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    trace_record(2, s);
+    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
   } else {
-    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
     bwd_dkdv_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    trace_record(2, s);
+    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
   }
   return check_launch("fp32 backward kernels");
 }

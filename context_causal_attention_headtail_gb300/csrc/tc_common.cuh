@@ -226,6 +226,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
+// 2^x with the MUFU.EX2 unit (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------ swizzled smem access ---
 // Byte offset of element (row, col) in a 128B-swizzled tile of R rows.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int R) {

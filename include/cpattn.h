@@ -79,6 +79,23 @@ cpattn_status cpattn_shard(const void *src, void *dst, int B, int H, int T, int 
 cpattn_status cpattn_unshard(const void *src, void *dst, int B, int H, int T, int d, int cp,
                              cpattn_dtype dt, cpattn_stream_t stream);
 
+/* HeadTail shard fused with RoPE, and its adjoint fused with unshard. The
+ * rotation (rotate-half pairs (i, i + d/2), theta_i = 10000^(-2i/d)) uses each
+ * token's natural position t, the global position the pages require under
+ * HeadTail (Claude Logs, 2026-05-07 and 2026-06-05: local positions were a
+ * bug; 2026-06-29: cos/sin follow the same permutation as the tokens):
+ *   cpattn_shard_rope   : dst[b,h,sigma(t),:] = R(t)   src[b,h,t,:]
+ *   cpattn_unshard_rope : dst[b,h,t,:]        = R(t)^T src[b,h,sigma(t),:]
+ * With q' = shard_rope(q), k' = shard_rope(k), cpattn_fwd/cpattn_bwd called
+ * with rope = 0 on q', k' give the same O and LSE as rope = 1 on the plain
+ * shards, and unshard_rope of their dq', dk' gives dq, dk: RoPE then runs in
+ * the passes that already read and write q, k and their gradients, and the
+ * attention kernels rotate nothing. Same rules as cpattn_shard; d in {64, 128}. */
+cpattn_status cpattn_shard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                cpattn_dtype dt, cpattn_stream_t stream);
+cpattn_status cpattn_unshard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                  cpattn_dtype dt, cpattn_stream_t stream);
+
 /* Host-only: idx_host[t] = sigma(t) for t in [0, T) (int32, caller-owned,
  * T entries). Launches nothing. */
 cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host);
@@ -137,6 +154,19 @@ const char *cpattn_last_error(void);
  * flag: CPATTN_ERR_TIMEOUT if a kernel's bounded wait expired since the last
  * check, CPATTN_ERR_CUDA if the stream reports an error, else CPATTN_OK. */
 cpattn_status cpattn_sync_status(cpattn_stream_t stream);
+
+/* Tracing hook for timing single kernels inside a longer region. Registers
+ * up to 8 caller-created CUDA events (cudaEvent_t handles, borrowed, never
+ * destroyed here) that later calls from this host thread record on their
+ * stream at kernel boundaries:
+ *   cpattn_fwd : events[0] before the attention kernel, events[1] after it;
+ *   cpattn_bwd : events[0] before the D = rowsum(dO*O) kernel, events[1]
+ *                after it, events[2] after the dK/dV kernel, events[3] after
+ *                the dQ kernel;
+ *   cpattn_shard / cpattn_unshard : events[0] before, events[1] after.
+ * A call records only the events it has (n large enough). n = 0 or
+ * events = NULL turns tracing off. Errors: CPATTN_ERR_ARG if n < 0 or n > 8. */
+cpattn_status cpattn_set_trace_events(void *const *events, int n);
 
 /* Library version, e.g. "cpattn 0.1 sm_103a". */
 const char *cpattn_version(void);

@@ -22,29 +22,40 @@ TOL = {
 }
 
 
-def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1) -> dict:
-    dt = w.torch_dtype
+def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
+            rope_mode: str = "kernel") -> dict:
+    """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd;
+    "shard" rotates q, k in cpattn_shard_rope, runs the attention with rope=0
+    and takes dq, dk back through cpattn_unshard_rope."""
     dev = torch.device(device)
     stream = torch.cuda.current_stream(dev)
+    fused = w.rope and rope_mode == "shard"
+    rope_flag = w.rope and not fused
     nat = {k: v.to(dev).contiguous() for k, v in inp.items()}
     sh = {k: torch.empty_like(v) for k, v in nat.items()}
     for k in nat:
-        cpattn.shard(nat[k], sh[k], w.cp, stream)
+        if fused and k in ("q", "k"):
+            cpattn.shard_rope(nat[k], sh[k], w.cp, stream)
+        else:
+            cpattn.shard(nat[k], sh[k], w.cp, stream)
     o = torch.empty_like(sh["q"])
     lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
     out = {}
     for _ in range(repeat):
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, w.rope, stream)
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream)
     if with_bwd:
         dq, dk, dv = (torch.empty_like(sh["q"]) for _ in range(3))
         ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
                          device=dev)
         for _ in range(repeat):
             cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
-                       w.causal, w.rope, stream)
+                       w.causal, rope_flag, stream)
         for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
             nt = torch.empty_like(t)
-            cpattn.unshard(t, nt, w.cp, stream)
+            if fused and name in ("dq", "dk"):
+                cpattn.unshard_rope(t, nt, w.cp, stream)
+            else:
+                cpattn.unshard(t, nt, w.cp, stream)
             out[name] = nt
     on = torch.empty_like(o)
     cpattn.unshard(o, on, w.cp, stream)

@@ -57,12 +57,37 @@ def test_shard_unshard_bit_exact(dtype, B, H, T, d, cp):
     assert torch.equal(zs.cpu(), x)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,T,d,cp", [(1, 2, 8, 64, 2), (2, 1, 1200, 128, 2), (1, 2, 32768, 128, 2),
+                                        (1, 1, 12296, 64, 4)])
+def test_shard_rope_against_oracle(dtype, B, H, T, d, cp):
+    x = (torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(T + d)) * 0.5).to(dtype)
+    xs = x.cuda()
+    ys, zs = torch.empty_like(xs), torch.empty_like(xs)
+    cpattn.shard_rope(xs, ys, cp)
+    cpattn.unshard_rope(ys, zs, cp)
+    torch.cuda.synchronize()
+    xd = x.double().numpy()
+    want = HT.shard(A.rope(xd, np.arange(T)), cp)
+    # Bounds: the GPU rotates the same stored values with angles good to ~1e-6
+    # rad and rounds once to the storage type (unit roundoff u); the round trip
+    # adds a second rounding, which R^T spreads over each (i, i + d/2) pair.
+    u = 2.0 ** -9 if dtype == torch.bfloat16 else 2.0 ** -24
+    pair = np.sqrt(xd[..., : d // 2] ** 2 + xd[..., d // 2:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    assert np.all(np.abs(ys.double().cpu().numpy() - want) <= u * np.abs(want) + 2e-6 * HT.shard(pair, cp) + 1e-7)
+    back = zs.double().cpu().numpy()
+    assert np.all(np.abs(back - xd) <= 3 * u * pair + 4e-6 * pair + 1e-7)
+
+
 def test_shard_index_matches_oracle():
     for T, cp in [(8, 2), (24, 3), (32768, 2), (12296, 4)]:
         assert cpattn.cpattn_shard_index(T, cp) == HT.shard_index(T, cp).tolist()
 
 
 # -------------------------------------------------- small, full compare ----
+
+ROPE_MODES = ["kernel", "shard"]
 
 SMALL_F32 = [
     WORKLOADS["tiny_fp32"],
@@ -84,16 +109,22 @@ SMALL_BF16 = [
 ]
 
 
+@pytest.mark.parametrize("mode", ROPE_MODES)
 @pytest.mark.parametrize("w", SMALL_F32, ids=lambda w: w.name)
-def test_fp32_path_full(w):
+def test_fp32_path_full(w, mode):
+    if mode == "shard" and not w.rope:
+        pytest.skip("no RoPE: one path")
     inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
-    _check_full(w, run_gpu(w, inp), _oracle_full(w, inp))
+    _check_full(w, run_gpu(w, inp, rope_mode=mode), _oracle_full(w, inp))
 
 
+@pytest.mark.parametrize("mode", ROPE_MODES)
 @pytest.mark.parametrize("w", SMALL_BF16, ids=lambda w: w.name)
-def test_bf16_path_full(w):
+def test_bf16_path_full(w, mode):
+    if mode == "shard" and not w.rope:
+        pytest.skip("no RoPE: one path")
     inp = make_inputs(w, seed=7 + w.T + w.cp)
-    got = run_gpu(w, inp)
+    got = run_gpu(w, inp, rope_mode=mode)
     want = _oracle_full(w, inp)
     _check_full(w, got, want)
     if w.T_valid < w.T:   # pad rows: dO = 0 there, so every gradient row is exactly zero
@@ -101,10 +132,11 @@ def test_bf16_path_full(w):
             assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0
 
 
-def test_bf16_deterministic():
+@pytest.mark.parametrize("mode", ROPE_MODES)
+def test_bf16_deterministic(mode):
     w = make_workload("det", B=1, T=1024, T_valid=1020, H=2, d=128, cp=2, rope=True)
     inp = make_inputs(w, seed=5)
-    a, b = run_gpu(w, inp), run_gpu(w, inp)
+    a, b = run_gpu(w, inp, rope_mode=mode), run_gpu(w, inp, rope_mode=mode)
     for k in a:
         assert torch.equal(a[k], b[k]), k
 
@@ -154,11 +186,13 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
     compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
 
 
-@pytest.mark.parametrize("name", ["gpt2_small", "long_16k", "window_32k", "padded_12289"])
-def test_workload_full_size_sampled(name):
+@pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
+                                       ("long_16k", "shard"), ("window_32k", "shard"),
+                                       ("window_32k", "kernel"), ("padded_12289", "shard")])
+def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])
-    got = run_gpu(w, inp)
+    got = run_gpu(w, inp, rope_mode=mode)
     for g in ("o", "lse", "dq", "dk", "dv"):
         assert torch.isfinite(got[g][:, :, : w.T_valid]).all(), g
     heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
