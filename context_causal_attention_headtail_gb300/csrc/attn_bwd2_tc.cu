@@ -1,0 +1,592 @@
+// Ring attention backward, pipelined form (inputs already rotated, or no
+// RoPE). Same mathematics and ring order as the kernels in attn_bwd_tc.cu
+// (P from the saved LSE, dS = P * (dP - D), dK/dV and dQ each owned by one
+// CTA, no atomics); the difference is scheduling. Each 128-wide tile of the
+// streamed operand is cut into two 64-wide halves handled by two softmax
+// warpgroups, and the MMA issuer interleaves them
+//   S_a S_b | acc_a(n) S_a(n+1) | acc_b(n) S_b(n+1) | ...
+// so one warpgroup's exponentials overlap the other half's matrix products.
+//  * dq2_tc_kernel (query-stationary): Q and dO are the A operands of
+//    S = Q K^T and dP = dO V^T straight from TMEM, so those products read
+//    only K and V from shared memory.
+//  * dkdv2_tc_kernel (key-stationary): dK and dV stay in TMEM across every
+//    ring step of every rank (the ring's travelling accumulator).
+#include <math.h>
+
+#include "attn_common.cuh"
+
+namespace cpattn {
+namespace {
+
+constexpr float kLog2eB = 1.4426950408889634f;
+
+struct Bwd2Params {
+  const __nv_bfloat16 *q, *dO;  // sharded [BH, T, D] (dq kernel: TMEM operands)
+  const float *lse, *D;         // [BH, T]
+  __nv_bfloat16 *dq, *dk, *dv;
+  int *err;
+  int BH, T, T_valid, c, cp, causal, tpc;
+  float scale, scale_log2;
+};
+
+// Scales 32-column chunks [c0, c0 + n*32) of a TMEM row and stores them as
+// bf16 at dst + c0 (every lane of the warp must call this).
+__device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchunks, float scale,
+                                                __nv_bfloat16 *dst, bool valid) {
+#pragma unroll 1
+  for (int cb = 0; cb < nchunks; ++cb) {
+    uint32_t r[32];
+    tc::tmem_ld32(t_row + c0 + cb * 32, r);
+    tc::tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      pk[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * scale, __uint_as_float(r[2 * e + 1]) * scale);
+    if (valid) {
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0 + cb * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) d4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+  }
+}
+
+// ================================================================== dQ
+template <int D>
+struct Dq2Cfg {
+  static constexpr int NS = (D == 128) ? 3 : 4;  // K/V stages
+  static constexpr int TILE = kTile * D * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = NS * TILE;
+  static constexpr int OFF_BAR = 2 * NS * TILE;
+  // qdo_ready, fin, s_full[2], p_full[2], dq_done[2], kv_full[NS], kv_empty[NS]
+  static constexpr int NBAR = 8 + 2 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  // TMEM columns: Q and dO as bf16 A operands, S and dP (two 64-key halves each), dQ.
+  static constexpr uint32_t colQ = 0, colDO = 64, colS = 128, colDP = 256, colDQ = 384;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    dq2_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ Bwd2Params p) {
+  using C = Dq2Cfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  auto sK = [&](int st) { return sbase + C::OFF_K + st * C::TILE; };
+  auto sV = [&](int st) { return sbase + C::OFF_V + st * C::TILE; };
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_qdo = bar0, bar_fin = bar0 + 8;
+  auto bar_s_full = [&](int h) { return bar0 + 16 + 8 * h; };
+  auto bar_p_full = [&](int h) { return bar0 + 32 + 8 * h; };
+  auto bar_dq_done = [&](int h) { return bar0 + 48 + 8 * h; };
+  auto bar_kv_full = [&](int st) { return bar0 + 64 + 8 * st; };
+  auto bar_kv_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cp = p.cp, c = p.c, tpc = p.tpc;
+  const int bh = blockIdx.x % p.BH;
+  const int g = blockIdx.x / p.BH;
+  const int kq = 2 * cp - 1 - g / tpc;
+  const int qt = tpc - 1 - g % tpc;
+  int rq, hq;
+  owner_of(kq, cp, rq, hq);
+  const int q_pos0 = kq * c + qt * kTile;
+  const int q_rows = min(kTile, c - qt * kTile);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const uint32_t b = bar0 + 8 * i;
+      uint32_t cnt = 1;
+      if (b == bar_qdo) cnt = 256;
+      if (b == bar_p_full(0) || b == bar_p_full(1)) cnt = 128;
+      tc::mbar_init(b, cnt);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const tc::WaitCtx wc{abort_flag, p.err};
+  const tc::WaitCtx drain{abort_flag + 1, p.err};
+
+  KvSchedule sched;
+  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
+  TileInfo t;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_k);
+      tc::tma_prefetch_desc(&tm_v);
+      int n = 0;
+      while (sched.next(t)) {
+        const int st = n % NS;
+        if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
+        tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
+        const int z = bh * 2 * cp + t.slot;
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_kv_full(st), blk * 64, t.y0, z);
+          tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_kv_full(st), blk * 64, t.y0, z);
+        }
+        ++n;
+      }
+      for (int m = (n > NS ? n - NS : 0); m < n; ++m) tc::mbar_wait(bar_kv_full(m % NS), (m / NS) & 1, drain);
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idQ = tc::idesc_bf16(128, D, false, true);
+      auto issue_sdp = [&](int h, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ts(tmem + C::colS + 64 * h, tmem + C::colQ + kk * 8,
+                     tc::desc_kmajor(sK(st) + h * 8192, kTile, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ts(tmem + C::colDP + 64 * h, tmem + C::colDO + kk * 8,
+                     tc::desc_kmajor(sV(st) + h * 8192, kTile, kk), idS, kk > 0);
+        tc::mma_commit(bar_s_full(h));
+      };
+      auto issue_dq = [&](int h, int st, int n) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_ts(tmem + C::colDQ, tmem + C::colS + 64 * h + kk * 8,
+                     tc::desc_mnmajor(sK(st), kTile, 4 * h + kk), idQ, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(bar_dq_done(h));
+      };
+      bool ok = tc::mbar_wait(bar_qdo, 0, wc);
+      if (ok && sched.next(t)) {
+        ok = tc::mbar_wait(bar_kv_full(0), 0, wc);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_sdp(0, 0);
+          issue_sdp(1, 0);
+        }
+        for (int n = 0; ok; ++n) {
+          const bool more = sched.next(t);
+          const int st = n % NS, st1 = (n + 1) % NS;
+          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_dq(0, st, n);
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = tc::mbar_wait(bar_dq_done(0), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_sdp(0, st1);
+          }
+          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_dq(1, st, n);
+          tc::mma_commit(bar_kv_empty(st));
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_dq_done(1), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_sdp(1, st1);
+          }
+          if (!more) break;
+        }
+      }
+      tc::mma_commit(bar_fin);
+      tc::mbar_wait(bar_fin, 0, drain);
+    }
+  } else {
+    // ------------------------------------------- softmax warpgroups (key halves)
+    const int h = warp >> 2;
+    const int row = threadIdx.x & 127;
+    const int q_pos = q_pos0 + row;
+    const bool valid = row < q_rows;
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + qt * kTile + row);
+    const float lse2 = valid ? p.lse[grow] * kLog2eB : INFINITY;
+    const float Drow = valid ? p.D[grow] : 0.f;
+    {  // this thread's row of Q (warpgroup 0) or dO (warpgroup 1) into TMEM
+      const uint4 *src = reinterpret_cast<const uint4 *>((h == 0 ? p.q : p.dO) + grow * D);
+#pragma unroll 1
+      for (int cb = 0; cb < D / 64; ++cb) {
+        uint32_t r[32];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const uint4 x = valid ? src[cb * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+        }
+        tc::tmem_st32(t_row + (h == 0 ? C::colQ : C::colDO) + cb * 32, r);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_qdo);
+    }
+    const float sl2 = p.scale_log2;
+    int n = 0;
+    bool ok = true;
+    while (sched.next(t)) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t rs[32], rd[32];
+        tc::tmem_ld32(t_row + C::colS + 64 * h + cb * 32, rs);
+        tc::tmem_ld32(t_row + C::colDP + 64 * h + cb * 32, rd);
+        tc::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          float ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int j = 64 * h + cb * 32 + 2 * e + u;
+            float pr = tc::ex2(fmaf(__uint_as_float(rs[2 * e + u]), sl2, -lse2));
+            if (t.need_mask) {
+              const int kp = t.pos0 + j;
+              if (j >= t.nvalid || kp >= p.T_valid || (p.causal && kp > q_pos)) pr = 0.f;
+            }
+            ds[u] = pr * (__uint_as_float(rd[2 * e + u]) - Drow);
+          }
+          pk[e] = pack_bf16x2(ds[0], ds[1]);
+        }
+        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_p_full(h));
+      ++n;
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done(1), (n - 1) & 1, wc));
+      if (ok) {
+        tc::tc_fence_after();
+        store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================== dK / dV
+template <int D>
+struct Dkdv2Cfg {
+  static constexpr int NS = (D == 128) ? 2 : 4;  // Q/dO stages
+  static constexpr int TILE = kTile * D * 2;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_Q = 2 * TILE;
+  static constexpr int OFF_DO = OFF_Q + NS * TILE;
+  static constexpr int OFF_LD = OFF_DO + NS * TILE;  // per stage: lse*log2e [128], D [128]
+  static constexpr int OFF_BAR = OFF_LD + NS * 1024;
+  // kv_full, fin, s_full[2], p_full[2], acc_done[2], qd_full[NS], qd_empty[NS]
+  static constexpr int NBAR = 8 + 2 * NS;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    dkdv2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ Bwd2Params p) {
+  using C = Dkdv2Cfg<D>;
+  constexpr int NS = C::NS;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = tc::smem_u32(smem);
+  const uint32_t sK = sbase + C::OFF_K, sV = sbase + C::OFF_V;
+  auto sQ = [&](int st) { return sbase + C::OFF_Q + st * C::TILE; };
+  auto sDO = [&](int st) { return sbase + C::OFF_DO + st * C::TILE; };
+  auto ld_lse = [&](int st) { return reinterpret_cast<float *>(smem + C::OFF_LD + st * 1024); };
+  auto ld_D = [&](int st) { return reinterpret_cast<float *>(smem + C::OFF_LD + st * 1024 + 512); };
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t bar_kv_full = bar0, bar_fin = bar0 + 8;
+  auto bar_s_full = [&](int h) { return bar0 + 16 + 8 * h; };
+  auto bar_p_full = [&](int h) { return bar0 + 32 + 8 * h; };
+  auto bar_acc_done = [&](int h) { return bar0 + 48 + 8 * h; };
+  auto bar_qd_full = [&](int st) { return bar0 + 64 + 8 * st; };
+  auto bar_qd_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cp = p.cp, c = p.c, tpc = p.tpc;
+  const int bh = blockIdx.x % p.BH;
+  const int g = blockIdx.x / p.BH;
+  const int kk_chunk = g / tpc;     // earliest keys first: they are seen by the most queries
+  const int kt = g % tpc;
+  int rk, hk;
+  owner_of(kk_chunk, cp, rk, hk);
+  const int k_z = bh * 2 * cp + 2 * rk + hk;
+  const int k_pos0 = kk_chunk * c + kt * kTile;
+  const int k_rows = min(kTile, c - kt * kTile);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const uint32_t b = bar0 + 8 * i;
+      uint32_t cnt = 1;
+      if (b == bar_p_full(0) || b == bar_p_full(1)) cnt = 128;
+      for (int st = 0; st < NS; ++st)
+        if (b == bar_qd_full(st)) cnt = 33;   // expect_tx arrive + 32 producer lanes
+      tc::mbar_init(b, cnt);
+    }
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    tc::mbar_fence_init();
+  }
+  if (warp == 8) {
+    tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const tc::WaitCtx wc{abort_flag, p.err};
+  const tc::WaitCtx drain{abort_flag + 1, p.err};
+
+  QSchedule sched;
+  sched.init(cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1);
+  const int k_ragged = k_rows < kTile;
+  TileInfo t;
+
+  if (warp == 8) {
+    if (lane == 0) {
+      tc::tma_prefetch_desc(&tm_q);
+      tc::tma_prefetch_desc(&tm_do);
+      tc::mbar_arrive_expect_tx(bar_kv_full, 2 * C::TILE);
+      for (int blk = 0; blk < D / 64; ++blk) {
+        tc::tma_load_3d(sK + blk * kTile * 128, &tm_k, bar_kv_full, blk * 64, kt * kTile, k_z);
+        tc::tma_load_3d(sV + blk * kTile * 128, &tm_v, bar_kv_full, blk * 64, kt * kTile, k_z);
+      }
+    }
+    int n = 0;
+    while (sched.next(t, k_ragged)) {
+      const int st = n % NS;
+      if (n >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(bar_qd_empty(st), ((n / NS) - 1) & 1, wc))) break;
+      const int z = bh * 2 * cp + t.slot;
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(bar_qd_full(st), 2 * C::TILE);
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tc::tma_load_3d(sQ(st) + blk * kTile * 128, &tm_q, bar_qd_full(st), blk * 64, t.y0, z);
+          tc::tma_load_3d(sDO(st) + blk * kTile * 128, &tm_do, bar_qd_full(st), blk * 64, t.y0, z);
+        }
+      }
+      const long long row0 = (long long)bh * p.T + (long long)t.slot * c + t.y0;
+      float *sl = ld_lse(st), *sd = ld_D(st);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = lane + 32 * i;
+        const bool v = r < t.nvalid;
+        sl[r] = v ? p.lse[row0 + r] * kLog2eB : INFINITY;   // ragged query rows get P = 0
+        sd[r] = v ? p.D[row0 + r] : 0.f;
+      }
+      tc::mbar_arrive(bar_qd_full(st));
+      ++n;
+    }
+    if (lane == 0) {
+      tc::mbar_wait(bar_kv_full, 0, drain);
+      for (int m = (n > NS ? n - NS : 0); m < n; ++m) tc::mbar_wait(bar_qd_full(m % NS), (m / NS) & 1, drain);
+    }
+  } else if (warp == 9) {
+    if (lane == 0) {
+      constexpr uint32_t idS = tc::idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idA = tc::idesc_bf16(128, D, false, true);
+      auto issue_sdp = [&](int h, int st) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ss(tmem + C::colS + 64 * h, tc::desc_kmajor(sK, kTile, kk),
+                     tc::desc_kmajor(sQ(st) + h * 8192, kTile, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ss(tmem + C::colDP + 64 * h, tc::desc_kmajor(sV, kTile, kk),
+                     tc::desc_kmajor(sDO(st) + h * 8192, kTile, kk), idS, kk > 0);
+        tc::mma_commit(bar_s_full(h));
+      };
+      auto issue_acc = [&](int h, int st, int n) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
+          tc::mma_ts(tmem + C::colDV, tmem + C::colS + 64 * h + kk * 8,
+                     tc::desc_mnmajor(sDO(st), kTile, 4 * h + kk), idA, acc);
+          tc::mma_ts(tmem + C::colDK, tmem + C::colDP + 64 * h + kk * 8,
+                     tc::desc_mnmajor(sQ(st), kTile, 4 * h + kk), idA, acc);
+        }
+        tc::mma_commit(bar_acc_done(h));
+      };
+      bool ok = tc::mbar_wait(bar_kv_full, 0, wc);
+      if (ok && sched.next(t, k_ragged)) {
+        ok = tc::mbar_wait(bar_qd_full(0), 0, wc);
+        if (ok) {
+          tc::tc_fence_after();
+          issue_sdp(0, 0);
+          issue_sdp(1, 0);
+        }
+        for (int n = 0; ok; ++n) {
+          const bool more = sched.next(t, k_ragged);
+          const int st = n % NS, st1 = (n + 1) % NS;
+          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_acc(0, st, n);
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = tc::mbar_wait(bar_acc_done(0), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_sdp(0, st1);
+          }
+          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          tc::tc_fence_after();
+          issue_acc(1, st, n);
+          tc::mma_commit(bar_qd_empty(st));
+          if (more) {
+            if (!(ok = tc::mbar_wait(bar_acc_done(1), n & 1, wc))) break;
+            tc::tc_fence_after();
+            issue_sdp(1, st1);
+          }
+          if (!more) break;
+        }
+      }
+      tc::mma_commit(bar_fin);
+      tc::mbar_wait(bar_fin, 0, drain);
+    }
+  } else {
+    // ------------------------------------------- softmax warpgroups (query halves)
+    const int h = warp >> 2;
+    const int row = threadIdx.x & 127;     // key row of the tile
+    const int k_pos = k_pos0 + row;
+    const bool valid = row < k_rows;
+    const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const long long grow = (long long)bh * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
+    const float sl2 = p.scale_log2;
+    int n = 0;
+    bool ok = true;
+    while (sched.next(t, k_ragged)) {
+      const int st = n % NS;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+      const float2 *sl = reinterpret_cast<const float2 *>(ld_lse(st));
+      const float2 *sd = reinterpret_cast<const float2 *>(ld_D(st));
+#pragma unroll 1
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t rs[32], rd[32];
+        tc::tmem_ld32(t_row + C::colS + 64 * h + cb * 32, rs);
+        tc::tmem_ld32(t_row + C::colDP + 64 * h + cb * 32, rd);
+        tc::tmem_ld_wait();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int q = 64 * h + cb * 32 + 2 * e;
+          const float2 l2 = sl[q >> 1], d2 = sd[q >> 1];
+          float p0 = tc::ex2(fmaf(__uint_as_float(rs[2 * e]), sl2, -l2.x));
+          float p1 = tc::ex2(fmaf(__uint_as_float(rs[2 * e + 1]), sl2, -l2.y));
+          if (t.need_mask) {
+            const int qp = t.pos0 + q;
+            if ((p.causal && k_pos > qp) || k_pos >= p.T_valid) p0 = 0.f;
+            if ((p.causal && k_pos > qp + 1) || k_pos >= p.T_valid) p1 = 0.f;
+          }
+          pk[e] = pack_bf16x2(p0, p1);
+          dk[e] = pack_bf16x2(p0 * (__uint_as_float(rd[2 * e]) - d2.x), p1 * (__uint_as_float(rd[2 * e + 1]) - d2.y));
+        }
+        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colDP + 64 * h + cb * 16, dk);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_p_full(h));
+      ++n;
+    }
+    if (ok) {
+      __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
+      if (n > 0) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_acc_done(1), (n - 1) & 1, wc));
+        if (ok) {
+          tc::tc_fence_after();
+          store_tmem_cols(t_row + (h == 0 ? C::colDV : C::colDK), 0, D / 32, h == 0 ? 1.f : p.scale, dst, valid);
+        }
+      } else if (valid) {   // no query sees these keys (all padding): zero gradients
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) d4[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                            const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
+  {
+    constexpr int smem = Dkdv2Cfg<D>::SMEM;
+    auto kern = dkdv2_tc_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
+    kern<<<grid, 320, smem, s>>>(mq, mk, mv, mdo, bp);
+    cpattn_status st = check_launch("tensor-core dK/dV kernel (pipelined)");
+    if (st != CPATTN_OK) return st;
+    trace_record(2, s);
+  }
+  constexpr int smem = Dq2Cfg<D>::SMEM;
+  auto kern = dq2_tc_kernel<D>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dQ kernel", smem);
+  kern<<<grid, 320, smem, s>>>(mk, mv, bp);
+  return check_launch("tensor-core dQ kernel (pipelined)");
+}
+
+}  // namespace
+
+cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, const float *lse,
+                               const void *dO, void *dq, void *dk, void *dv, float *D,
+                               const Geometry &g, cudaStream_t s) {
+  const long long BH = (long long)g.B * g.H;
+  const long long n_slots = BH * 2 * g.cp;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_slots) ||
+      !make_tile_map(&mv, v, g.d, g.c, n_slots) || !make_tile_map(&mdo, dO, g.d, g.c, n_slots))
+    return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
+  Bwd2Params bp;
+  bp.q = static_cast<const __nv_bfloat16 *>(q);
+  bp.dO = static_cast<const __nv_bfloat16 *>(dO);
+  bp.lse = lse;
+  bp.D = D;
+  bp.dq = static_cast<__nv_bfloat16 *>(dq);
+  bp.dk = static_cast<__nv_bfloat16 *>(dk);
+  bp.dv = static_cast<__nv_bfloat16 *>(dv);
+  bp.err = device_err_flag();
+  bp.BH = (int)BH;
+  bp.T = g.T;
+  bp.T_valid = g.T_valid;
+  bp.c = g.c;
+  bp.cp = g.cp;
+  bp.causal = g.causal;
+  bp.tpc = (g.c + kTile - 1) / kTile;
+  bp.scale = (float)(1.0 / sqrt((double)g.d));
+  bp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
+  const long long grid = BH * 2 * g.cp * bp.tpc;
+  if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
+  return g.d == 128 ? launch_bwd2_t<128>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
+                    : launch_bwd2_t<64>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
+}
+
+}  // namespace cpattn

@@ -57,6 +57,11 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               float *D, const Geometry &g, cudaStream_t s);
 
+// Pipelined backward (no in-kernel RoPE): dK/dV and dQ kernels of attn_bwd2_tc.cu.
+cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, const float *lse,
+                               const void *dO, void *dq, void *dk, void *dv, float *D,
+                               const Geometry &g, cudaStream_t s);
+
 // Tracing events registered by cpattn_set_trace_events for this host thread:
 // records event i on stream s if one is registered (no-op otherwise).
 void trace_record(int i, cudaStream_t s);

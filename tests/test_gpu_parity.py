@@ -72,7 +72,7 @@ def test_shard_rope_against_oracle(dtype, B, H, T, d, cp):
     # Bounds: the GPU rotates the same stored values with angles good to ~1e-6
     # rad and rounds once to the storage type (unit roundoff u); the round trip
     # adds a second rounding, which R^T spreads over each (i, i + d/2) pair.
-    u = 2.0 ** -9 if dtype == torch.bfloat16 else 2.0 ** -24
+    u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -24
     pair = np.sqrt(xd[..., : d // 2] ** 2 + xd[..., d // 2:] ** 2)
     pair = np.concatenate([pair, pair], axis=-1)
     assert np.all(np.abs(ys.double().cpu().numpy() - want) <= u * np.abs(want) + 2e-6 * HT.shard(pair, cp) + 1e-7)
