@@ -233,29 +233,36 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-#pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t rs[32], rd[32];
-        tc::tmem_ld32(t_row + C::colS + 64 * h + cb * 32, rs);
-        tc::tmem_ld32(t_row + C::colDP + 64 * h + cb * 32, rd);
-        tc::tmem_ld_wait();
-        uint32_t pk[16];
+      const uint32_t tS = t_row + C::colS + 64 * h, tP = t_row + C::colDP + 64 * h;
+      uint32_t rs[2][16], rd[2][16];
+      tc::tmem_ld16(tS, rs[0]);
+      tc::tmem_ld16(tP, rd[0]);
+      tc::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+      for (int cb = 0; cb < 4; ++cb) {
+        const int cur = cb & 1;
+        if (cb < 3) {
+          tc::tmem_ld16(tS + (cb + 1) * 16, rs[cur ^ 1]);
+          tc::tmem_ld16(tP + (cb + 1) * 16, rd[cur ^ 1]);
+        }
+        uint32_t pk[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
           float ds[2];
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const int j = 64 * h + cb * 32 + 2 * e + u;
-            float pr = tc::ex2(fmaf(__uint_as_float(rs[2 * e + u]), sl2, -lse2));
+            const int j = 64 * h + cb * 16 + 2 * e + u;
+            float pr = tc::ex2(fmaf(__uint_as_float(rs[cur][2 * e + u]), sl2, -lse2));
             if (t.need_mask) {
               const int kp = t.pos0 + j;
               if (j >= t.nvalid || kp >= p.T_valid || (p.causal && kp > q_pos)) pr = 0.f;
             }
-            ds[u] = pr * (__uint_as_float(rd[2 * e + u]) - Drow);
+            ds[u] = pr * (__uint_as_float(rd[cur][2 * e + u]) - Drow);
           }
           pk[e] = pack_bf16x2(ds[0], ds[1]);
         }
-        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
+        tc::tmem_st8(tS + cb * 8, pk);
+        tc::tmem_ld_wait();
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -478,31 +485,45 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-      const float2 *sl = reinterpret_cast<const float2 *>(ld_lse(st));
-      const float2 *sd = reinterpret_cast<const float2 *>(ld_D(st));
-#pragma unroll 1
-      for (int cb = 0; cb < 2; ++cb) {
-        uint32_t rs[32], rd[32];
-        tc::tmem_ld32(t_row + C::colS + 64 * h + cb * 32, rs);
-        tc::tmem_ld32(t_row + C::colDP + 64 * h + cb * 32, rd);
-        tc::tmem_ld_wait();
-        uint32_t pk[16], dk[16];
+      const uint32_t sl = tc::smem_u32(ld_lse(st)) + 4u * (64 * h), sd = tc::smem_u32(ld_D(st)) + 4u * (64 * h);
+      const uint32_t tS = t_row + C::colS + 64 * h, tP = t_row + C::colDP + 64 * h;
+      // Four 16-column chunks; the TMEM loads of chunk cb+1 are in flight
+      // while chunk cb is processed.
+      uint32_t rs[2][16], rd[2][16];
+      tc::tmem_ld16(tS, rs[0]);
+      tc::tmem_ld16(tP, rd[0]);
+      tc::tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int q = 64 * h + cb * 32 + 2 * e;
-          const float2 l2 = sl[q >> 1], d2 = sd[q >> 1];
-          float p0 = tc::ex2(fmaf(__uint_as_float(rs[2 * e]), sl2, -l2.x));
-          float p1 = tc::ex2(fmaf(__uint_as_float(rs[2 * e + 1]), sl2, -l2.y));
-          if (t.need_mask) {
-            const int qp = t.pos0 + q;
-            if ((p.causal && k_pos > qp) || k_pos >= p.T_valid) p0 = 0.f;
-            if ((p.causal && k_pos > qp + 1) || k_pos >= p.T_valid) p1 = 0.f;
-          }
-          pk[e] = pack_bf16x2(p0, p1);
-          dk[e] = pack_bf16x2(p0 * (__uint_as_float(rd[2 * e]) - d2.x), p1 * (__uint_as_float(rd[2 * e + 1]) - d2.y));
+      for (int cb = 0; cb < 4; ++cb) {
+        const int cur = cb & 1;
+        if (cb < 3) {
+          tc::tmem_ld16(tS + (cb + 1) * 16, rs[cur ^ 1]);
+          tc::tmem_ld16(tP + (cb + 1) * 16, rd[cur ^ 1]);
         }
-        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
-        tc::tmem_st16(t_row + C::colDP + 64 * h + cb * 16, dk);
+        uint32_t pk[8], dk[8];
+#pragma unroll
+        for (int e4 = 0; e4 < 4; ++e4) {
+          const int q0 = cb * 16 + 4 * e4;        // query column within the half
+          const float4 l4 = tc::lds_f4(sl + 4u * q0), d4 = tc::lds_f4(sd + 4u * q0);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pr[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pr[u] = tc::ex2(fmaf(__uint_as_float(rs[cur][4 * e4 + u]), sl2, -lv[u]));
+            if (t.need_mask) {
+              const int qp = t.pos0 + 64 * h + q0 + u;
+              if ((p.causal && k_pos > qp) || k_pos >= p.T_valid) pr[u] = 0.f;
+            }
+            ds[u] = pr[u] * (__uint_as_float(rd[cur][4 * e4 + u]) - dv4[u]);
+          }
+          pk[2 * e4] = pack_bf16x2(pr[0], pr[1]);
+          pk[2 * e4 + 1] = pack_bf16x2(pr[2], pr[3]);
+          dk[2 * e4] = pack_bf16x2(ds[0], ds[1]);
+          dk[2 * e4 + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+        tc::tmem_st8(tS + cb * 8, pk);
+        tc::tmem_st8(tP + cb * 8, dk);
+        tc::tmem_ld_wait();
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();

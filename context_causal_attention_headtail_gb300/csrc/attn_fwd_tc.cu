@@ -506,23 +506,29 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(wg), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-      // pass 1: masked row max
+      // pass 1: masked row max; the TMEM load of chunk cb+1 is in flight
+      // while chunk cb is reduced.
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_s + cb * 32, r);
+      {
+        uint32_t r[2][32];
+        tc::tmem_ld32(t_s, r[0]);
         tc::tmem_ld_wait();
-        if (t.need_mask) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int j = cb * 32 + e, kp = t.pos0 + j;
-            const bool keep = (j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos);
-            mx[e & 3] = fmaxf(mx[e & 3], keep ? __uint_as_float(r[e]) : -INFINITY);
+        for (int cb = 0; cb < 4; ++cb) {
+          const int cur = cb & 1;
+          if (cb < 3) tc::tmem_ld32(t_s + (cb + 1) * 32, r[cur ^ 1]);
+          if (t.need_mask) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int j = cb * 32 + e, kp = t.pos0 + j;
+              const bool keep = (j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos);
+              mx[e & 3] = fmaxf(mx[e & 3], keep ? __uint_as_float(r[cur][e]) : -INFINITY);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[cur][e]));
           }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[e]));
+          tc::tmem_ld_wait();
         }
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -552,28 +558,34 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(S*scale*log2e - m) -> bf16 over S
+      // pass 2: P = 2^(S*scale*log2e - m) -> bf16 over S; the TMEM load of
+      // chunk cb+1 is in flight while chunk cb is processed.
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_s + cb * 32, r);
+      {
+        uint32_t r[2][32];
+        tc::tmem_ld32(t_s, r[0]);
         tc::tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float v0 = __uint_as_float(r[2 * e]), v1 = __uint_as_float(r[2 * e + 1]);
-          if (t.need_mask) {
-            const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
-            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
-            if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
+        for (int cb = 0; cb < 4; ++cb) {
+          const int cur = cb & 1;
+          if (cb < 3) tc::tmem_ld32(t_s + (cb + 1) * 32, r[cur ^ 1]);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float v0 = __uint_as_float(r[cur][2 * e]), v1 = __uint_as_float(r[cur][2 * e + 1]);
+            if (t.need_mask) {
+              const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
+              if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
+              if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
+            }
+            const float p0 = tc::ex2(fmaf(v0, sl2, -m_use)), p1 = tc::ex2(fmaf(v1, sl2, -m_use));
+            ls[(2 * e) & 3] += p0;
+            ls[(2 * e + 1) & 3] += p1;
+            pk[e] = pack_bf16x2(p0, p1);
           }
-          const float p0 = tc::ex2(fmaf(v0, sl2, -m_use)), p1 = tc::ex2(fmaf(v1, sl2, -m_use));
-          ls[(2 * e) & 3] += p0;
-          ls[(2 * e + 1) & 3] += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          tc::tmem_st16(t_s + cb * 16, pk);
+          tc::tmem_ld_wait();
         }
-        tc::tmem_st16(t_s + cb * 16, pk);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc::tmem_st_wait();
