@@ -1,14 +1,14 @@
 // Ring attention backward, pipelined form (inputs already rotated, or no
 // RoPE). Same mathematics and ring order as the kernels in attn_bwd_tc.cu
 // (P from the saved LSE, dS = P * (dP - D), dK/dV and dQ each owned by one
-// CTA, no atomics); the difference is scheduling. Each 128-wide tile of the
-// streamed operand is cut into two 64-wide halves handled by two softmax
-// warpgroups, and the MMA issuer interleaves them
-//   S_a S_b | acc_a(n) S_a(n+1) | acc_b(n) S_b(n+1) | ...
-// so one warpgroup's exponentials overlap the other half's matrix products.
+// CTA, no atomics); the difference is scheduling. Every tcgen05.mma is
+// 128 x 128 (or 128 x D) so the tensor core runs at full rate, and the two
+// softmax warpgroups split each tile's 128 columns. The work on a tile is cut
+// into a P phase (exponentials) and a dS phase, and the MMA issuer starts the
+// products that need only one of them as soon as it is ready, so softmax
+// work overlaps the matrix products of the same and of the next tile.
 //  * dq2_tc_kernel (query-stationary): Q and dO are the A operands of
-//    S = Q K^T and dP = dO V^T straight from TMEM, so those products read
-//    only K and V from shared memory.
+//    S = Q K^T and dP = dO V^T straight from TMEM.
 //  * dkdv2_tc_kernel (key-stationary): dK and dV stay in TMEM across every
 //    ring step of every rank (the ring's travelling accumulator).
 #include <math.h>
@@ -51,18 +51,22 @@ __device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchu
 }
 
 // ================================================================== dQ
+// Query-stationary. TMEM: Q (bf16 A operand) 0, dO 64, S 128, dP 256 (dS is
+// written over its first 64 columns), dQ 384. Per key tile n the MMA issuer
+// runs S(n+1) as soon as both softmax warpgroups have read S(n), then dQ(n)
+// once dS(n) is in TMEM, then dP(n+1) once dQ(n) has consumed dS(n).
+// Warpgroup h owns key columns [64h, 64h+64) of each tile.
 template <int D>
-struct Dq2Cfg {
+struct Dq3Cfg {
   static constexpr int NS = (D == 128) ? 3 : 4;  // K/V stages
   static constexpr int TILE = kTile * D * 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NS * TILE;
   static constexpr int OFF_BAR = 2 * NS * TILE;
-  // qdo_ready, fin, s_full[2], p_full[2], dq_done[2], kv_full[NS], kv_empty[NS]
+  // qdo_ready, fin, s_full, dp_full, s_free, dp_read, ds_ready, dq_done, kv_full[NS], kv_empty[NS]
   static constexpr int NBAR = 8 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
-  // TMEM columns: Q and dO as bf16 A operands, S and dP (two 64-key halves each), dQ.
   static constexpr uint32_t colQ = 0, colDO = 64, colS = 128, colDP = 256, colDQ = 384;
 };
 
@@ -70,7 +74,7 @@ template <int D>
 __global__ void __launch_bounds__(320, 1)
     dq2_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ Bwd2Params p) {
-  using C = Dq2Cfg<D>;
+  using C = Dq3Cfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -78,10 +82,8 @@ __global__ void __launch_bounds__(320, 1)
   auto sK = [&](int st) { return sbase + C::OFF_K + st * C::TILE; };
   auto sV = [&](int st) { return sbase + C::OFF_V + st * C::TILE; };
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t bar_qdo = bar0, bar_fin = bar0 + 8;
-  auto bar_s_full = [&](int h) { return bar0 + 16 + 8 * h; };
-  auto bar_p_full = [&](int h) { return bar0 + 32 + 8 * h; };
-  auto bar_dq_done = [&](int h) { return bar0 + 48 + 8 * h; };
+  const uint32_t bar_qdo = bar0, bar_fin = bar0 + 8, bar_s_full = bar0 + 16, bar_dp_full = bar0 + 24,
+                 bar_s_free = bar0 + 32, bar_dp_read = bar0 + 40, bar_ds_ready = bar0 + 48, bar_dq_done = bar0 + 56;
   auto bar_kv_full = [&](int st) { return bar0 + 64 + 8 * st; };
   auto bar_kv_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -101,10 +103,8 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
-      uint32_t cnt = 1;
-      if (b == bar_qdo) cnt = 256;
-      if (b == bar_p_full(0) || b == bar_p_full(1)) cnt = 128;
-      tc::mbar_init(b, cnt);
+      const bool by_threads = b == bar_qdo || b == bar_s_free || b == bar_dp_read || b == bar_ds_ready;
+      tc::mbar_init(b, by_threads ? 256 : 1);
     }
     abort_flag[0] = 0;
     abort_flag[1] = 0;
@@ -145,63 +145,61 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idQ = tc::idesc_bf16(128, D, false, true);
-      auto issue_sdp = [&](int h, int st) {
+      auto issue_s = [&](int st) {
+        const uint64_t bk = tc::kdesc0(sK(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ts(tmem + C::colS + 64 * h, tmem + C::colQ + kk * 8,
-                     tc::desc_kmajor(sK(st) + h * 8192, kTile, kk), idS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ts(tmem + C::colDP + 64 * h, tmem + C::colDO + kk * 8,
-                     tc::desc_kmajor(sV(st) + h * 8192, kTile, kk), idS, kk > 0);
-        tc::mma_commit(bar_s_full(h));
+          tc::mma_ts(tmem + C::colS, tmem + C::colQ + kk * 8, bk + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(bar_s_full);
       };
-      auto issue_dq = [&](int h, int st, int n) {
+      auto issue_dp = [&](int st) {
+        const uint64_t bv = tc::kdesc0(sV(st));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_ts(tmem + C::colDQ, tmem + C::colS + 64 * h + kk * 8,
-                     tc::desc_mnmajor(sK(st), kTile, 4 * h + kk), idQ, (n > 0 || h > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_commit(bar_dq_done(h));
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ts(tmem + C::colDP, tmem + C::colDO + kk * 8, bv + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(bar_dp_full);
       };
       bool ok = tc::mbar_wait(bar_qdo, 0, wc);
       if (ok && sched.next(t)) {
         ok = tc::mbar_wait(bar_kv_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
-          issue_sdp(0, 0);
-          issue_sdp(1, 0);
+          issue_s(0);
+          issue_dp(0);
         }
         for (int n = 0; ok; ++n) {
           const bool more = sched.next(t);
           const int st = n % NS, st1 = (n + 1) % NS;
-          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
-          tc::tc_fence_after();
-          issue_dq(0, st, n);
-          if (more) {
+          if (more) {   // S(n+1) once S(n) has been read
             if (!(ok = tc::mbar_wait(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
-            if (!(ok = tc::mbar_wait(bar_dq_done(0), n & 1, wc))) break;
+            if (!(ok = tc::mbar_wait(bar_s_free, n & 1, wc))) break;
             tc::tc_fence_after();
-            issue_sdp(0, st1);
+            issue_s(st1);
           }
-          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          if (!(ok = tc::mbar_wait(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
-          issue_dq(1, st, n);
-          tc::mma_commit(bar_kv_empty(st));
-          if (more) {
-            if (!(ok = tc::mbar_wait(bar_dq_done(1), n & 1, wc))) break;
-            tc::tc_fence_after();
-            issue_sdp(1, st1);
+          {   // dQ += dS(n) K(n); dS is 128 keys = 64 packed columns
+            const uint64_t bk = tc::mndesc0(sK(st), kTile);
+            const uint32_t acc0 = n > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc::mma_ts(tmem + C::colDQ, tmem + C::colDP + kk * 8, bk + tc::mnoff(kk), idQ, kk > 0 ? 1u : acc0);
+            tc::mma_commit(bar_dq_done);
+            tc::mma_commit(bar_kv_empty(st));
           }
           if (!more) break;
+          if (!(ok = tc::mbar_wait(bar_dq_done, n & 1, wc))) break;   // dP(n+1) overwrites dS(n)
+          tc::tc_fence_after();
+          issue_dp(st1);
         }
       }
       tc::mma_commit(bar_fin);
       tc::mbar_wait(bar_fin, 0, drain);
     }
   } else {
-    // ------------------------------------------- softmax warpgroups (key halves)
+    // ---------------------------------------------- softmax warpgroups (key halves)
     const int h = warp >> 2;
     const int row = threadIdx.x & 127;
     const int q_pos = q_pos0 + row;
@@ -230,47 +228,58 @@ __global__ void __launch_bounds__(320, 1)
     int n = 0;
     bool ok = true;
     while (sched.next(t)) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full, n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-      const uint32_t tS = t_row + C::colS + 64 * h, tP = t_row + C::colDP + 64 * h;
-      uint32_t rs[2][16], rd[2][16];
-      tc::tmem_ld16(tS, rs[0]);
-      tc::tmem_ld16(tP, rd[0]);
-      tc::tmem_ld_wait();
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const int cur = cb & 1;
-        if (cb < 3) {
-          tc::tmem_ld16(tS + (cb + 1) * 16, rs[cur ^ 1]);
-          tc::tmem_ld16(tP + (cb + 1) * 16, rd[cur ^ 1]);
-        }
-        uint32_t pk[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int j = 64 * h + cb * 16 + 2 * e + u;
-            float pr = tc::ex2(fmaf(__uint_as_float(rs[cur][2 * e + u]), sl2, -lse2));
-            if (t.need_mask) {
-              const int kp = t.pos0 + j;
-              if (j >= t.nvalid || kp >= p.T_valid || (p.causal && kp > q_pos)) pr = 0.f;
-            }
-            ds[u] = pr * (__uint_as_float(rd[cur][2 * e + u]) - Drow);
-          }
-          pk[e] = pack_bf16x2(ds[0], ds[1]);
-        }
-        tc::tmem_st8(tS + cb * 8, pk);
+      float pr[64];
+      {
+        uint32_t r[2][32];
+        tc::tmem_ld32(t_row + C::colS + 64 * h, r[0]);
+        tc::tmem_ld32(t_row + C::colS + 64 * h + 32, r[1]);
         tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar_s_free);                 // S may now be overwritten by S(n+1)
+        int lim = kTile;
+        if (t.need_mask) {
+          lim = min(t.nvalid, p.T_valid - t.pos0);
+          if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
+        }
+        lim -= 64 * h;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float e = tc::ex2(fmaf(__uint_as_float(r[j >> 5][j & 31]), sl2, -lse2));
+          pr[j] = j < lim ? e : 0.f;
+        }
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_full, n & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+      uint32_t rd[2][32];
+      tc::tmem_ld32(t_row + C::colDP + 64 * h, rd[0]);
+      tc::tmem_ld32(t_row + C::colDP + 64 * h + 32, rd[1]);
+      tc::tmem_ld_wait();
+      // Both warpgroups must have read dP before either writes dS over it.
+      tc::mbar_arrive(bar_dp_read);
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));
+      if (!ok) break;
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int j = cb * 32 + 2 * e;
+          pk[e] = pack_bf16x2(pr[j] * (__uint_as_float(rd[cb][2 * e]) - Drow),
+                              pr[j + 1] * (__uint_as_float(rd[cb][2 * e + 1]) - Drow));
+        }
+        tc::tmem_st16(t_row + C::colDP + 32 * h + cb * 16, pk);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar_p_full(h));
+      tc::mbar_arrive(bar_ds_ready);
       ++n;
     }
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done(1), (n - 1) & 1, wc));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done, (n - 1) & 1, wc));
       if (ok) {
         tc::tc_fence_after();
         store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
@@ -287,8 +296,13 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ============================================================== dK / dV
+// Key-stationary. TMEM: S^T 0 (P^T written over its first 64 columns),
+// dP^T 128 (dS^T over its first 64), dV 256, dK 256 + D. Per query tile n:
+//   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | dK(n) once dS^T(n)
+//   is | S^T(n+1) once dV(n) has consumed P^T | dP^T(n+1) once dK(n) has
+// consumed dS^T; warpgroup h owns query columns [64h, 64h+64).
 template <int D>
-struct Dkdv2Cfg {
+struct Dkdv3Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;  // Q/dO stages
   static constexpr int TILE = kTile * D * 2;
   static constexpr int OFF_K = 0;
@@ -297,8 +311,8 @@ struct Dkdv2Cfg {
   static constexpr int OFF_DO = OFF_Q + NS * TILE;
   static constexpr int OFF_LD = OFF_DO + NS * TILE;  // per stage: lse*log2e [128], D [128]
   static constexpr int OFF_BAR = OFF_LD + NS * 1024;
-  // kv_full, fin, s_full[2], p_full[2], acc_done[2], qd_full[NS], qd_empty[NS]
-  static constexpr int NBAR = 8 + 2 * NS;
+  // kv_full, fin, s_full, dp_full, s_read, dp_read, p_ready, ds_ready, dv_done, dk_done, qd_full[NS], qd_empty[NS]
+  static constexpr int NBAR = 10 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(320, 1)
     dkdv2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ Bwd2Params p) {
-  using C = Dkdv2Cfg<D>;
+  using C = Dkdv3Cfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -320,12 +334,11 @@ __global__ void __launch_bounds__(320, 1)
   auto ld_lse = [&](int st) { return reinterpret_cast<float *>(smem + C::OFF_LD + st * 1024); };
   auto ld_D = [&](int st) { return reinterpret_cast<float *>(smem + C::OFF_LD + st * 1024 + 512); };
   const uint32_t bar0 = sbase + C::OFF_BAR;
-  const uint32_t bar_kv_full = bar0, bar_fin = bar0 + 8;
-  auto bar_s_full = [&](int h) { return bar0 + 16 + 8 * h; };
-  auto bar_p_full = [&](int h) { return bar0 + 32 + 8 * h; };
-  auto bar_acc_done = [&](int h) { return bar0 + 48 + 8 * h; };
-  auto bar_qd_full = [&](int st) { return bar0 + 64 + 8 * st; };
-  auto bar_qd_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  const uint32_t bar_kv_full = bar0, bar_fin = bar0 + 8, bar_s_full = bar0 + 16, bar_dp_full = bar0 + 24,
+                 bar_s_read = bar0 + 32, bar_dp_read = bar0 + 40, bar_p_ready = bar0 + 48,
+                 bar_ds_ready = bar0 + 56, bar_dv_done = bar0 + 64, bar_dk_done = bar0 + 72;
+  auto bar_qd_full = [&](int st) { return bar0 + 80 + 8 * st; };
+  auto bar_qd_empty = [&](int st) { return bar0 + 80 + 8 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -345,7 +358,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
       uint32_t cnt = 1;
-      if (b == bar_p_full(0) || b == bar_p_full(1)) cnt = 128;
+      if (b == bar_s_read || b == bar_dp_read || b == bar_p_ready || b == bar_ds_ready) cnt = 256;
       for (int st = 0; st < NS; ++st)
         if (b == bar_qd_full(st)) cnt = 33;   // expect_tx arrive + 32 producer lanes
       tc::mbar_init(b, cnt);
@@ -393,13 +406,20 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       const long long row0 = (long long)bh * p.T + (long long)t.slot * c + t.y0;
-      float *sl = ld_lse(st), *sd = ld_D(st);
+      // All eight loads are issued before any store so their latencies overlap.
+      float lv[4], dv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane + 32 * i;
         const bool v = r < t.nvalid;
-        sl[r] = v ? p.lse[row0 + r] * kLog2eB : INFINITY;   // ragged query rows get P = 0
-        sd[r] = v ? p.D[row0 + r] : 0.f;
+        lv[i] = v ? __ldg(p.lse + row0 + r) * kLog2eB : INFINITY;   // ragged query rows get P = 0
+        dv[i] = v ? __ldg(p.D + row0 + r) : 0.f;
+      }
+      float *sl = ld_lse(st), *sd = ld_D(st);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sl[lane + 32 * i] = lv[i];
+        sd[lane + 32 * i] = dv[i];
       }
       tc::mbar_arrive(bar_qd_full(st));
       ++n;
@@ -410,67 +430,69 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else if (warp == 9) {
     if (lane == 0) {
-      constexpr uint32_t idS = tc::idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idA = tc::idesc_bf16(128, D, false, true);
-      auto issue_sdp = [&](int h, int st) {
+      const uint64_t ak0 = tc::kdesc0(sK), av0 = tc::kdesc0(sV);
+      auto issue_s = [&](int st) {
+        const uint64_t bq = tc::kdesc0(sQ(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + C::colS + 64 * h, tc::desc_kmajor(sK, kTile, kk),
-                     tc::desc_kmajor(sQ(st) + h * 8192, kTile, kk), idS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + C::colDP + 64 * h, tc::desc_kmajor(sV, kTile, kk),
-                     tc::desc_kmajor(sDO(st) + h * 8192, kTile, kk), idS, kk > 0);
-        tc::mma_commit(bar_s_full(h));
+          tc::mma_ss(tmem + C::colS, ak0 + tc::koff(kTile, kk), bq + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(bar_s_full);
       };
-      auto issue_acc = [&](int h, int st, int n) {
+      auto issue_dp = [&](int st) {
+        const uint64_t bo = tc::kdesc0(sDO(st));
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint32_t acc = (n > 0 || h > 0 || kk > 0) ? 1u : 0u;
-          tc::mma_ts(tmem + C::colDV, tmem + C::colS + 64 * h + kk * 8,
-                     tc::desc_mnmajor(sDO(st), kTile, 4 * h + kk), idA, acc);
-          tc::mma_ts(tmem + C::colDK, tmem + C::colDP + 64 * h + kk * 8,
-                     tc::desc_mnmajor(sQ(st), kTile, 4 * h + kk), idA, acc);
-        }
-        tc::mma_commit(bar_acc_done(h));
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc::mma_ss(tmem + C::colDP, av0 + tc::koff(kTile, kk), bo + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit(bar_dp_full);
       };
       bool ok = tc::mbar_wait(bar_kv_full, 0, wc);
       if (ok && sched.next(t, k_ragged)) {
         ok = tc::mbar_wait(bar_qd_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
-          issue_sdp(0, 0);
-          issue_sdp(1, 0);
+          issue_s(0);
+          issue_dp(0);
         }
         for (int n = 0; ok; ++n) {
           const bool more = sched.next(t, k_ragged);
           const int st = n % NS, st1 = (n + 1) % NS;
-          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
+          const uint32_t acc0 = n > 0 ? 1u : 0u;
+          if (!(ok = tc::mbar_wait(bar_p_ready, n & 1, wc))) break;
           tc::tc_fence_after();
-          issue_acc(0, st, n);
-          if (more) {
-            if (!(ok = tc::mbar_wait(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
-            if (!(ok = tc::mbar_wait(bar_acc_done(0), n & 1, wc))) break;
-            tc::tc_fence_after();
-            issue_sdp(0, st1);
+          {   // dV += P^T(n) dO(n)
+            const uint64_t bo = tc::mndesc0(sDO(st), kTile);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc::mma_ts(tmem + C::colDV, tmem + C::colS + kk * 8, bo + tc::mnoff(kk), idA, kk > 0 ? 1u : acc0);
+            tc::mma_commit(bar_dv_done);
           }
-          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          if (!(ok = tc::mbar_wait(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
-          issue_acc(1, st, n);
-          tc::mma_commit(bar_qd_empty(st));
-          if (more) {
-            if (!(ok = tc::mbar_wait(bar_acc_done(1), n & 1, wc))) break;
-            tc::tc_fence_after();
-            issue_sdp(1, st1);
+          {   // dK += dS^T(n) Q(n)
+            const uint64_t bq = tc::mndesc0(sQ(st), kTile);
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk)
+              tc::mma_ts(tmem + C::colDK, tmem + C::colDP + kk * 8, bq + tc::mnoff(kk), idA, kk > 0 ? 1u : acc0);
+            tc::mma_commit(bar_dk_done);
+            tc::mma_commit(bar_qd_empty(st));
           }
           if (!more) break;
+          if (!(ok = tc::mbar_wait(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
+          if (!(ok = tc::mbar_wait(bar_dv_done, n & 1, wc))) break;     // S^T(n+1) overwrites P^T(n)
+          tc::tc_fence_after();
+          issue_s(st1);
+          if (!(ok = tc::mbar_wait(bar_dk_done, n & 1, wc))) break;     // dP^T(n+1) overwrites dS^T(n)
+          tc::tc_fence_after();
+          issue_dp(st1);
         }
       }
       tc::mma_commit(bar_fin);
       tc::mbar_wait(bar_fin, 0, drain);
     }
   } else {
-    // ------------------------------------------- softmax warpgroups (query halves)
+    // -------------------------------------------- softmax warpgroups (query halves)
     const int h = warp >> 2;
     const int row = threadIdx.x & 127;     // key row of the tile
     const int k_pos = k_pos0 + row;
@@ -482,58 +504,88 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     while (sched.next(t, k_ragged)) {
       const int st = n % NS;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(h), n & 1, wc));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full, n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
       const uint32_t sl = tc::smem_u32(ld_lse(st)) + 4u * (64 * h), sd = tc::smem_u32(ld_D(st)) + 4u * (64 * h);
-      const uint32_t tS = t_row + C::colS + 64 * h, tP = t_row + C::colDP + 64 * h;
-      // Four 16-column chunks; the TMEM loads of chunk cb+1 are in flight
-      // while chunk cb is processed.
-      uint32_t rs[2][16], rd[2][16];
-      tc::tmem_ld16(tS, rs[0]);
-      tc::tmem_ld16(tP, rd[0]);
-      tc::tmem_ld_wait();
+      // Queries kept: column q with q >= lo (causal) and none for padding keys;
+      // ragged query columns carry LSE = +inf, so their P is 0 already.
+      int lo = 0;
+      if (t.need_mask) {
+        if (k_pos >= p.T_valid) lo = kTile;
+        else if (p.causal) lo = max(0, k_pos - t.pos0);
+      }
+      lo -= 64 * h;
+      float pr[64];
+      {
+        uint32_t r[2][32];
+        tc::tmem_ld32(t_row + C::colS + 64 * h, r[0]);
+        tc::tmem_ld32(t_row + C::colS + 64 * h + 32, r[1]);
+        tc::tmem_ld_wait();
+        // Both warpgroups must have read S^T before either writes P^T over it.
+        tc::mbar_arrive(bar_s_read);
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const int cur = cb & 1;
-        if (cb < 3) {
-          tc::tmem_ld16(tS + (cb + 1) * 16, rs[cur ^ 1]);
-          tc::tmem_ld16(tP + (cb + 1) * 16, rd[cur ^ 1]);
-        }
-        uint32_t pk[8], dk[8];
-#pragma unroll
-        for (int e4 = 0; e4 < 4; ++e4) {
-          const int q0 = cb * 16 + 4 * e4;        // query column within the half
-          const float4 l4 = tc::lds_f4(sl + 4u * q0), d4 = tc::lds_f4(sd + 4u * q0);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pr[4], ds[4];
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 l4 = tc::lds_f4(sl + 16u * q4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            pr[u] = tc::ex2(fmaf(__uint_as_float(rs[cur][4 * e4 + u]), sl2, -lv[u]));
-            if (t.need_mask) {
-              const int qp = t.pos0 + 64 * h + q0 + u;
-              if ((p.causal && k_pos > qp) || k_pos >= p.T_valid) pr[u] = 0.f;
-            }
-            ds[u] = pr[u] * (__uint_as_float(rd[cur][4 * e4 + u]) - dv4[u]);
+            const int q = 4 * q4 + u;
+            const float e = tc::ex2(fmaf(__uint_as_float(r[q >> 5][q & 31]), sl2, -lv[u]));
+            pr[q] = q >= lo ? e : 0.f;
           }
-          pk[2 * e4] = pack_bf16x2(pr[0], pr[1]);
-          pk[2 * e4 + 1] = pack_bf16x2(pr[2], pr[3]);
-          dk[2 * e4] = pack_bf16x2(ds[0], ds[1]);
-          dk[2 * e4 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        tc::tmem_st8(tS + cb * 8, pk);
-        tc::tmem_st8(tP + cb * 8, dk);
-        tc::tmem_ld_wait();
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_read, n & 1, wc));
+      if (!ok) break;
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
+        tc::tmem_st16(t_row + C::colS + 32 * h + cb * 16, pk);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar_p_full(h));
+      tc::mbar_arrive(bar_p_ready);
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_full, n & 1, wc));
+      if (!ok) break;
+      tc::tc_fence_after();
+      {
+        uint32_t rd[2][32];
+        tc::tmem_ld32(t_row + C::colDP + 64 * h, rd[0]);
+        tc::tmem_ld32(t_row + C::colDP + 64 * h + 32, rd[1]);
+        tc::tmem_ld_wait();
+        tc::mbar_arrive(bar_dp_read);
+#pragma unroll
+        for (int q4 = 0; q4 < 16; ++q4) {
+          const float4 d4 = tc::lds_f4(sd + 16u * q4);
+          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int q = 4 * q4 + u;
+            pr[q] *= __uint_as_float(rd[q >> 5][q & 31]) - dvv[u];
+          }
+        }
+      }
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));
+      if (!ok) break;
+#pragma unroll
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
+        tc::tmem_st16(t_row + C::colDP + 32 * h + cb * 16, pk);
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar_ds_ready);
       ++n;
     }
     if (ok) {
       __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
       if (n > 0) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_acc_done(1), (n - 1) & 1, wc));
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dk_done, (n - 1) & 1, wc));
         if (ok) {
           tc::tc_fence_after();
           store_tmem_cols(t_row + (h == 0 ? C::colDV : C::colDK), 0, D / 32, h == 0 ? 1.f : p.scale, dst, valid);
@@ -558,7 +610,7 @@ template <int D>
 cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
   {
-    constexpr int smem = Dkdv2Cfg<D>::SMEM;
+    constexpr int smem = Dkdv3Cfg<D>::SMEM;
     auto kern = dkdv2_tc_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
@@ -567,7 +619,7 @@ cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
     if (st != CPATTN_OK) return st;
     trace_record(2, s);
   }
-  constexpr int smem = Dq2Cfg<D>::SMEM;
+  constexpr int smem = Dq3Cfg<D>::SMEM;
   auto kern = dq2_tc_kernel<D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dQ kernel", smem);

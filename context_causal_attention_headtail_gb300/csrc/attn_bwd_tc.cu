@@ -195,13 +195,19 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         }
       }
       const long long row0 = (long long)bh * p.T + (long long)t.slot * c + t.y0;
-      float *sl = ld_lse(st), *sd = ld_D(st);
+      float lv[4], dv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int r = lane + 32 * i;
         const bool v = r < t.nvalid;
-        sl[r] = v ? p.lse[row0 + r] * kLog2e : INFINITY;   // ragged query rows get P = 0
-        sd[r] = v ? p.D[row0 + r] : 0.f;
+        lv[i] = v ? __ldg(p.lse + row0 + r) * kLog2e : INFINITY;   // ragged query rows get P = 0
+        dv[i] = v ? __ldg(p.D + row0 + r) : 0.f;
+      }
+      float *sl = ld_lse(st), *sd = ld_D(st);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sl[lane + 32 * i] = lv[i];
+        sd[lane + 32 * i] = dv[i];
       }
       tc::mbar_arrive(bar_qd_full(st));
       ++n;

@@ -435,18 +435,22 @@ __global__ void __launch_bounds__(320, 1)
     if (lane == 0) {
       constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = tc::idesc_bf16(128, D, false, true);
+      const uint64_t dq0[2] = {tc::kdesc0(sQ(0)), tc::kdesc0(sQ(1))};
       auto issue_s = [&](int i, int st) {
+        const uint64_t a0 = dq0[i], b0 = tc::kdesc0(sK(st));
+        const uint32_t d = tmem + i * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + i * 128, tc::desc_kmajor(sQ(i), kTile, kk), tc::desc_kmajor(sK(st), kTile, kk), idS,
-                     kk > 0);
+          tc::mma_ss(d, a0 + tc::koff(kTile, kk), b0 + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
         tc::mma_commit(bar_s_full(i));
       };
       auto issue_pv = [&](int i, int st, int n) {
+        const uint64_t b0 = tc::mndesc0(sV(st), kTile);
+        const uint32_t d = tmem + colO0 + i * D, a = tmem + i * 128;
+        const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc::mma_ts(tmem + colO0 + i * D, tmem + i * 128 + kk * 8, tc::desc_mnmajor(sV(st), kTile, kk), idPV,
-                     (n > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_ts(d, a + kk * 8, b0 + tc::mnoff(kk), idPV, kk > 0 ? 1u : acc0);
         tc::mma_commit(bar_o_done(i));
       };
       bool ok = tc::mbar_wait(bar_q_full, 0, wc);
@@ -506,30 +510,29 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(wg), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-      // pass 1: masked row max; the TMEM load of chunk cb+1 is in flight
-      // while chunk cb is reduced.
+      // Every mask of a row is an upper bound on the key column j inside the
+      // tile: j < nvalid (ragged tile), pos0 + j < T_valid (padding) and
+      // pos0 + j <= q_pos (causal). Keep j < lim.
+      int lim = kTile;
+      if (t.need_mask) {
+        lim = min(t.nvalid, p.T_valid - t.pos0);
+        if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
+      }
+      const bool masked = __any_sync(0xffffffffu, lim < kTile);
+      // pass 1: row max over the kept columns.
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      {
-        uint32_t r[2][32];
-        tc::tmem_ld32(t_s, r[0]);
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
         tc::tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          const int cur = cb & 1;
-          if (cb < 3) tc::tmem_ld32(t_s + (cb + 1) * 32, r[cur ^ 1]);
-          if (t.need_mask) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int j = cb * 32 + e, kp = t.pos0 + j;
-              const bool keep = (j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos);
-              mx[e & 3] = fmaxf(mx[e & 3], keep ? __uint_as_float(r[cur][e]) : -INFINITY);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[cur][e]));
-          }
-          tc::tmem_ld_wait();
+          for (int e = 0; e < 32; ++e)
+            if (cb * 32 + e >= lim) r[e] = 0xff800000u;   // -inf
         }
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[e]));
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_new = fmaxf(m_run, mt * sl2);
@@ -558,34 +561,28 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(S*scale*log2e - m) -> bf16 over S; the TMEM load of
-      // chunk cb+1 is in flight while chunk cb is processed.
+      // pass 2: P = 2^(S*scale*log2e - m), rounded to bf16 and written over S.
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        uint32_t r[2][32];
-        tc::tmem_ld32(t_s, r[0]);
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t r[32];
+        tc::tmem_ld32(t_s + cb * 32, r);
         tc::tmem_ld_wait();
+        if (masked) {
 #pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-          const int cur = cb & 1;
-          if (cb < 3) tc::tmem_ld32(t_s + (cb + 1) * 32, r[cur ^ 1]);
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float v0 = __uint_as_float(r[cur][2 * e]), v1 = __uint_as_float(r[cur][2 * e + 1]);
-            if (t.need_mask) {
-              const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
-              if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
-              if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
-            }
-            const float p0 = tc::ex2(fmaf(v0, sl2, -m_use)), p1 = tc::ex2(fmaf(v1, sl2, -m_use));
-            ls[(2 * e) & 3] += p0;
-            ls[(2 * e + 1) & 3] += p1;
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tc::tmem_st16(t_s + cb * 16, pk);
-          tc::tmem_ld_wait();
+          for (int e = 0; e < 32; ++e)
+            if (cb * 32 + e >= lim) r[e] = 0xff800000u;
         }
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = tc::ex2(fmaf(__uint_as_float(r[2 * e]), sl2, -m_use));
+          const float p1 = tc::ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, -m_use));
+          ls[(2 * e) & 3] += p0;
+          ls[(2 * e + 1) & 3] += p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tc::tmem_st16(t_s + cb * 16, pk);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc::tmem_st_wait();

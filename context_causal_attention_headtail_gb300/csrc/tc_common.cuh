@@ -216,6 +216,17 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int R, int kk) {
   return sdesc_sw128(addr, (uint32_t)R * 128u, 1024u);
 }
 
+// Descriptor of a K-major / MN-major tile at k-step 0. The start address is
+// the descriptor's low 14 bits (address >> 4); every k-step offset used here
+// keeps it inside shared memory (< 256 KB), so a later k-step's descriptor is
+// the base plus a compile-time constant (no carry out of the field).
+__device__ __forceinline__ uint64_t kdesc0(uint32_t base) { return sdesc_sw128(base, 16u, 1024u); }
+__device__ __forceinline__ uint64_t mndesc0(uint32_t base, int R) { return sdesc_sw128(base, (uint32_t)R * 128u, 1024u); }
+__host__ __device__ constexpr uint64_t koff(int R, int kk) {
+  return (uint64_t)((((kk >> 2) * R * 128) + (kk & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnoff(int kk) { return (uint64_t)((kk * 2048) >> 4); }
+
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
