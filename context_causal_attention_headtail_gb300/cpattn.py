@@ -22,7 +22,7 @@ F32, BF16 = 0, 1
 EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshard_rope",
            "cpattn_shard_index", "cpattn_fwd",
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
-           "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events")
+           "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc")
 
 
 class CpattnError(RuntimeError):
@@ -45,6 +45,7 @@ def _declare(lib):
         "cpattn_shard_index": [_i, _i, _c.POINTER(_c.c_int32)],
         "cpattn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp],
         "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
+        "cpattn_bwd_noalloc": [_vp] * 9 + [_i] * 9 + [_vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
@@ -114,6 +115,12 @@ def cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, 
                dt, stream=None):
     _check(lib().cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, cp,
                             causal, rope, dt, stream))
+
+
+def cpattn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, T, T_valid, H, d, cp, causal, rope, dt,
+                       stream=None):
+    _check(lib().cpattn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, T, T_valid, H, d, cp,
+                                    causal, rope, dt, stream))
 
 
 def cpattn_merge(o_parts, lse_parts, o, lse, B, H, T, d, dt, stream=None):

@@ -280,6 +280,46 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
   return st;
 }
 
+// --------------------------------------------------- allocation-free backward
+// D = rowsum(dO * O) for cpattn_bwd_noalloc lives in this file-scope array
+// instead of a caller workspace. Every GPU that loads the library holds it
+// (CPATTN_NOALLOC_MAX_ROWS floats) until the process exits.
+static __device__ __align__(256) float g_noalloc_scratch[CPATTN_NOALLOC_MAX_ROWS];
+
+// Device address of this device's copy of the array. Host code must not pass
+// the symbol itself to a kernel (on the host it names a stand-in, not device
+// memory), so the address is resolved once per device, with that device
+// current, and cached.
+static float *noalloc_scratch() {
+  static std::mutex mu;
+  static float *addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<float *>(ptr);
+  }
+  return addr[dev];
+}
+
+cpattn_status cpattn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                 const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                 int B, int T, int T_valid, int H, int d, int cp, int causal,
+                                 int rope, cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (B < 1 || H < 1 || T < 1) return fail(CPATTN_ERR_SHAPE, "sizes must be >= 1");
+  const long long rows = (long long)B * H * T;
+  if (rows > (long long)CPATTN_NOALLOC_MAX_ROWS)
+    return fail(CPATTN_ERR_SHAPE, "B*H*T=%lld exceeds the static scratch of %u rows", rows,
+                (unsigned)CPATTN_NOALLOC_MAX_ROWS);
+  float *scratch = noalloc_scratch();
+  if (!scratch) return fail(CPATTN_ERR_CUDA, "cannot resolve the device address of the static scratch");
+  return cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, scratch, B, T, T_valid, H, d, cp, causal, rope,
+                    dt, stream);
+}
+
 cpattn_status cpattn_merge(const float *const *o_parts, const float *const *lse_parts, int n,
                            void *o, float *lse, int B, int H, int T, int d, cpattn_dtype dt,
                            cpattn_stream_t stream) {

@@ -132,6 +132,31 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
                          void *workspace, int B, int T, int T_valid, int H, int d, int cp,
                          int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
 
+/* --------------------------------------------- allocation-free backward ---
+ * Not from the pages: an addition of this library for callers that cannot
+ * allocate device memory when they call it -- for example a plugin inside a
+ * host runtime that owns all device memory and gives its plugins no
+ * allocator, or a latency-bound loop that forbids cudaMalloc/cudaFree after
+ * start-up because those calls can synchronise the device and fragment its
+ * memory. Same computation, arguments, layouts and errors as cpattn_bwd, but
+ * without `workspace`: the D = rowsum(dO * O) scratch is a file-scope device
+ * array of CPATTN_NOALLOC_MAX_ROWS floats (8 MiB) that every GPU loading the
+ * library holds until the process exits. The call itself allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *  - B*H*T must be <= CPATTN_NOALLOC_MAX_ROWS, else CPATTN_ERR_SHAPE.
+ *  - The first call on each device resolves the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array. Each call overwrites the rows it uses
+ *    before reading them, so nothing stale leaks into a result, but calls
+ *    whose kernels overlap on the GPU (different streams, or different host
+ *    threads on one device) race on it: serialise them. */
+#define CPATTN_NOALLOC_MAX_ROWS (1u << 21)
+cpattn_status cpattn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                                 const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                 int B, int T, int T_valid, int H, int d, int cp, int causal,
+                                 int rope, cpattn_dtype dt, cpattn_stream_t stream);
+
 /* --------------------------------------------------------------- merge ---
  * Standalone SDPAMerger (Claude Logs, 2026-03-20; 2026-03-26 on keeping P
  * and LSE consistent; 2026-05-20 partial-merge fix): merges n partial
