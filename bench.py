@@ -75,6 +75,37 @@ def workload_config(w):
                   % (4 * w.B * w.H * w.T * w.d * 2 // 2 ** 20)}
 
 
+# ----------------------------------------------------------- rank logic ----
+# Every rank runs its own replica on its own batch (the (b, h) problems are
+# independent), so the only cross-rank traffic is timing: a barrier around the
+# timed region and the max of the per-rank step times.
+
+def rank_env():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(w, rank: int) -> int:
+    """Seed of rank `rank`'s batch: the workload's seed, shifted per rank."""
+    from context_causal_attention_headtail_gb300.synth import SEEDS
+    return SEEDS.get(w.name, 1234) + rank
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world: int, flops_per_rank: float, ms_max: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's step time."""
+    return world * flops_per_rank / (ms_max * 1e-3) / 1e12
+
+
 # --------------------------------------------------------------- clocks ----
 
 class ClockSampler:
@@ -181,7 +212,7 @@ def cpu_baseline_entry(w, s):
 
 def run_reference(args):
     """--impl reference: the oracle, timed as it stands on the host cores."""
-    rank = int(os.environ.get("RANK", "0"))
+    world, rank, _ = rank_env()
     if rank != 0:
         return
     from context_causal_attention_headtail_gb300.synth import WORKLOADS
@@ -218,9 +249,7 @@ def run_ours(args):
     from context_causal_attention_headtail_gb300 import cpattn
     from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make_inputs
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
@@ -229,7 +258,7 @@ def run_ours(args):
     if w.dtype != "bf16":
         raise SystemExit("bench runs the bf16 tensor-core path; pick a bf16 workload")
 
-    inp = make_inputs(w, SEEDS[w.name] + rank)
+    inp = make_inputs(w, rank_seed(w, rank))
     if rank == 0:
         _INPUT_CACHE[w.name] = inp
     host_in = {k: v.pin_memory() for k, v in inp.items()}
@@ -292,13 +321,6 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize(dev)
@@ -322,7 +344,7 @@ def run_ours(args):
     clocks = sampler.stop()
     cpattn.cpattn_sync_status(stream.cuda_stream)
     ms_local = start.elapsed_time(end) / args.steps
-    ms = max_over_ranks(ms_local)
+    ms = max_over_ranks(ms_local, world, dev)
 
     # per-kernel device time per step (averaged over the timed steps)
     ker_ms = {k: 0.0 for k in kernels}
@@ -355,10 +377,10 @@ def run_ours(args):
         e2.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
-        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps)
+        e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
-        e2e = {"value": world * w.fwdbwd_flops() / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": weak_scaling_value(world, w.fwdbwd_flops(), e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "tokens_per_s": world * w.B * w.T_valid / (e2e_ms * 1e-3)}
 
@@ -400,7 +422,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_entry(w, oracle_sample(w))
 
-    value = world * w.fwdbwd_flops() / (ms * 1e-3) / 1e12
+    value = weak_scaling_value(world, w.fwdbwd_flops(), ms)
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
