@@ -36,10 +36,14 @@ METRIC = "causal attn fwd+bwd TFLOP/s & tokens/s at T=32k, % of GB300 BF16 TC pe
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "window_32k"
 
-# DRAM bytes (read + write) per launch from ncu captures of the named kernel on
-# the 32k workload, by the command written in profiles/; None when no capture
-# of the current kernel exists.
-NCU_TRAFFIC_BYTES = {}
+# DRAM bytes (read + write) per launch from one ncu capture of the named kernel
+# on the 32k workload (profiles/tc_kernels_window_32k.md); a kernel missing
+# here has no capture of its current version. Only valid for that workload.
+NCU_TRAFFIC_BYTES = {
+    ("window_32k", "fwd"): 2.213885e9 + 0.115291e9,
+    ("window_32k", "bwd_dkdv"): 4.799820e9 + 0.238431e9,
+    ("window_32k", "bwd_dq"): 4.065538e9 + 0.119980e9,
+}
 
 
 def parse_args():
@@ -412,7 +416,8 @@ def run_ours(args):
     d = ker_rep[dom]
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"],
                 "peak": peaks["bf16_tflops_sustained"] if d["bound"] == "tensor" else peaks["hbm_gbs"],
-                "unit": d["unit"], "frac": d["frac"], "traffic": NCU_TRAFFIC_BYTES.get(dom),
+                "unit": d["unit"], "frac": d["frac"],
+                "traffic": NCU_TRAFFIC_BYTES.get((w.name, dom)) if not rope_flag else None,
                 "peak_source": f"{peaks['source']} "
                                + ("bf16_tflops_sustained (kernel timed inside a long step)"
                                   if d["bound"] == "tensor" else "hbm_gbs"),
