@@ -245,10 +245,19 @@ __global__ void __launch_bounds__(320, 1)
           if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
         }
         lim -= 64 * h;
+        const uint64_t sl2x2 = tc::f2(sl2, sl2), nl2 = tc::f2(-lse2, -lse2);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float e = tc::ex2(fmaf(__uint_as_float(r[j >> 5][j & 31]), sl2, -lse2));
-          pr[j] = j < lim ? e : 0.f;
+        for (int j = 0; j < 64; j += 2) {
+          float x0, x1;
+          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[j >> 5][j & 31]), __uint_as_float(r[j >> 5][(j & 31) + 1])),
+                             sl2x2, nl2), x0, x1);
+          pr[j] = tc::ex2(x0);
+          pr[j + 1] = tc::ex2(x1);
+        }
+        if (__any_sync(0xffffffffu, lim < 64)) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (j >= lim) pr[j] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_full, n & 1, wc));
@@ -262,14 +271,15 @@ __global__ void __launch_bounds__(320, 1)
       tc::mbar_arrive(bar_dp_read);
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));
       if (!ok) break;
+      const uint64_t nD2 = tc::f2(-Drow, -Drow);
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int j = cb * 32 + 2 * e;
-          pk[e] = pack_bf16x2(pr[j] * (__uint_as_float(rd[cb][2 * e]) - Drow),
-                              pr[j + 1] * (__uint_as_float(rd[cb][2 * e + 1]) - Drow));
+          const uint64_t dp = tc::fadd2(tc::f2(__uint_as_float(rd[cb][2 * e]), __uint_as_float(rd[cb][2 * e + 1])), nD2);
+          pk[e] = tc::pack_bf16x2_2(tc::fmul2(tc::f2(pr[j], pr[j + 1]), dp));
         }
         tc::tmem_st16(t_row + C::colDP + 32 * h + cb * 16, pk);
       }
@@ -524,16 +534,25 @@ __global__ void __launch_bounds__(320, 1)
         tc::tmem_ld_wait();
         // Both warpgroups must have read S^T before either writes P^T over it.
         tc::mbar_arrive(bar_s_read);
+        const uint64_t sl2x2 = tc::f2(sl2, sl2);
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
           const float4 l4 = tc::lds_f4(sl + 16u * q4);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const int q = 4 * q4;
+          float x0, x1, x2, x3;
+          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[q >> 5][q & 31]), __uint_as_float(r[q >> 5][(q & 31) + 1])),
+                             sl2x2, tc::f2(-l4.x, -l4.y)), x0, x1);
+          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[q >> 5][(q & 31) + 2]), __uint_as_float(r[q >> 5][(q & 31) + 3])),
+                             sl2x2, tc::f2(-l4.z, -l4.w)), x2, x3);
+          pr[q] = tc::ex2(x0);
+          pr[q + 1] = tc::ex2(x1);
+          pr[q + 2] = tc::ex2(x2);
+          pr[q + 3] = tc::ex2(x3);
+        }
+        if (__any_sync(0xffffffffu, lo > 0)) {
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = 4 * q4 + u;
-            const float e = tc::ex2(fmaf(__uint_as_float(r[q >> 5][q & 31]), sl2, -lv[u]));
-            pr[q] = q >= lo ? e : 0.f;
-          }
+          for (int q = 0; q < 64; ++q)
+            if (q < lo) pr[q] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_read, n & 1, wc));
@@ -560,12 +579,15 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
           const float4 d4 = tc::lds_f4(sd + 16u * q4);
-          const float dvv[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int q = 4 * q4 + u;
-            pr[q] *= __uint_as_float(rd[q >> 5][q & 31]) - dvv[u];
-          }
+          const int q = 4 * q4;
+          const uint64_t a = tc::fmul2(tc::f2(pr[q], pr[q + 1]),
+                                       tc::fadd2(tc::f2(__uint_as_float(rd[q >> 5][q & 31]), __uint_as_float(rd[q >> 5][(q & 31) + 1])),
+                                                 tc::f2(-d4.x, -d4.y)));
+          const uint64_t b = tc::fmul2(tc::f2(pr[q + 2], pr[q + 3]),
+                                       tc::fadd2(tc::f2(__uint_as_float(rd[q >> 5][(q & 31) + 2]), __uint_as_float(rd[q >> 5][(q & 31) + 3])),
+                                                 tc::f2(-d4.z, -d4.w)));
+          tc::unf2(a, pr[q], pr[q + 1]);
+          tc::unf2(b, pr[q + 2], pr[q + 3]);
         }
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));

@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(320, 1)
         if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
       }
       const bool masked = __any_sync(0xffffffffu, lim < kTile);
-      // pass 1: row max over the kept columns.
+      // pass 1: row max over the kept columns (three-input max).
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
@@ -532,7 +532,12 @@ __global__ void __launch_bounds__(320, 1)
             if (cb * 32 + e >= lim) r[e] = 0xff800000u;   // -inf
         }
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(r[e]));
+        for (int e = 0; e < 32; e += 8) {
+          mx[0] = tc::fmax3(mx[0], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+          mx[1] = tc::fmax3(mx[1], __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
+          mx[2] = tc::fmax3(mx[2], __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
+          mx[3] = tc::fmax3(mx[3], __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+        }
       }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_new = fmaxf(m_run, mt * sl2);
@@ -561,8 +566,10 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(S*scale*log2e - m), rounded to bf16 and written over S.
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // pass 2: P = 2^(S*scale*log2e - m), rounded to bf16 and written over S;
+      // the argument and the row sum use packed fp32 pairs.
+      const uint64_t sl2x2 = tc::f2(sl2, sl2), negm2 = tc::f2(-m_use, -m_use);
+      uint64_t ls2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t r[32];
@@ -576,14 +583,17 @@ __global__ void __launch_bounds__(320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = tc::ex2(fmaf(__uint_as_float(r[2 * e]), sl2, -m_use));
-          const float p1 = tc::ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl2, -m_use));
-          ls[(2 * e) & 3] += p0;
-          ls[(2 * e + 1) & 3] += p1;
-          pk[e] = pack_bf16x2(p0, p1);
+          float x0, x1;
+          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sl2x2, negm2), x0, x1);
+          const uint64_t p01 = tc::f2(tc::ex2(x0), tc::ex2(x1));
+          ls2[e & 1] = tc::fadd2(ls2[e & 1], p01);
+          pk[e] = tc::pack_bf16x2_2(p01);
         }
         tc::tmem_st16(t_s + cb * 16, pk);
       }
+      float ls[4];
+      tc::unf2(ls2[0], ls[0], ls[1]);
+      tc::unf2(ls2[1], ls[2], ls[3]);
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       tc::tmem_st_wait();
       tc::tc_fence_before();
