@@ -66,7 +66,8 @@ struct Dq3Cfg {
   // qdo_ready, fin, s_full, dp_full, s_free, dp_read, ds_ready, dq_done, kv_full[NS], kv_empty[NS]
   static constexpr int NBAR = 8 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
+  static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
   static constexpr uint32_t colQ = 0, colDO = 64, colS = 128, colDP = 256, colDQ = 384;
 };
 
@@ -88,6 +89,8 @@ __global__ void __launch_bounds__(320, 1)
   auto bar_kv_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
+  TileEntry *tab = reinterpret_cast<TileEntry *>(smem + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
@@ -113,16 +116,19 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
     tc::tmem_relinquish();
+    {
+      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, lane);
+      if (lane == 0) *ntiles_slot = nt;
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int ntiles = *ntiles_slot;
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
-  KvSchedule sched;
-  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
   TileInfo t;
 
   if (warp == 8) {
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(320, 1)
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
       int n = 0;
-      while (sched.next(t)) {
+      while (n < ntiles && (decode_tile(tab[n], t), true)) {
         const int st = n % NS;
         if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
         tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
@@ -162,7 +168,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::mma_commit(bar_dp_full);
       };
       bool ok = tc::mbar_wait(bar_qdo, 0, wc);
-      if (ok && sched.next(t)) {
+      if (ok && ntiles > 0) {
         ok = tc::mbar_wait(bar_kv_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(320, 1)
           issue_dp(0);
         }
         for (int n = 0; ok; ++n) {
-          const bool more = sched.next(t);
+          const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           if (more) {   // S(n+1) once S(n) has been read
             if (!(ok = tc::mbar_wait(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = p.scale_log2;
     int n = 0;
     bool ok = true;
-    while (sched.next(t)) {
+    while (n < ntiles && (decode_tile(tab[n], t), true)) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full, n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
@@ -324,7 +330,8 @@ struct Dkdv3Cfg {
   // kv_full, fin, s_full, dp_full, s_read, dp_read, p_ready, ds_ready, dv_done, dk_done, qd_full[NS], qd_empty[NS]
   static constexpr int NBAR = 10 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
+  static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
   static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
 };
 
@@ -351,6 +358,8 @@ __global__ void __launch_bounds__(320, 1)
   auto bar_qd_empty = [&](int st) { return bar0 + 80 + 8 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
+  TileEntry *tab = reinterpret_cast<TileEntry *>(smem + C::OFF_MISC + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
@@ -380,16 +389,19 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
     tc::tmem_relinquish();
+    {
+      const int nt = build_q_table(tab, cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1, k_rows < kTile, lane);
+      if (lane == 0) *ntiles_slot = nt;
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int ntiles = *ntiles_slot;
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
-  QSchedule sched;
-  sched.init(cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1);
   const int k_ragged = k_rows < kTile;
   TileInfo t;
 
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
     int n = 0;
-    while (sched.next(t, k_ragged)) {
+    while (n < ntiles && (decode_tile(tab[n], t), true)) {
       const int st = n % NS;
       if (n >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(bar_qd_empty(st), ((n / NS) - 1) & 1, wc))) break;
       const int z = bh * 2 * cp + t.slot;
@@ -458,7 +470,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::mma_commit(bar_dp_full);
       };
       bool ok = tc::mbar_wait(bar_kv_full, 0, wc);
-      if (ok && sched.next(t, k_ragged)) {
+      if (ok && ntiles > 0) {
         ok = tc::mbar_wait(bar_qd_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
@@ -466,7 +478,7 @@ __global__ void __launch_bounds__(320, 1)
           issue_dp(0);
         }
         for (int n = 0; ok; ++n) {
-          const bool more = sched.next(t, k_ragged);
+          const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
           if (!(ok = tc::mbar_wait(bar_p_ready, n & 1, wc))) break;
@@ -512,7 +524,7 @@ __global__ void __launch_bounds__(320, 1)
     const float sl2 = p.scale_log2;
     int n = 0;
     bool ok = true;
-    while (sched.next(t, k_ragged)) {
+    while (n < ntiles && (decode_tile(tab[n], t), true)) {
       const int st = n % NS;
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full, n & 1, wc));
       if (!ok) break;

@@ -583,7 +583,9 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               float *D, const Geometry &g, cudaStream_t s) {
   (void)o;
-  if (!g.rope) return launch_bwd2_bf16(q, k, v, lse, dO, dq, dk, dv, D, g, s);
+  // Pipelined kernels with a tile table in shared memory, where the schedule fits it.
+  if (!g.rope && 2LL * g.cp * ((g.c + kTile - 1) / kTile) <= kMaxTiles)
+    return launch_bwd2_bf16(q, k, v, lse, dO, dq, dk, dv, D, g, s);
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
   CUtensorMap mq, mk, mv, mdo;

@@ -337,7 +337,8 @@ struct Fwd2Cfg {
   // q_full, fin, s_full[2], p_full[2], o_done[2], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS]
   static constexpr int NBAR = 8 + 4 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
+  static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
 };
 
 template <int D>
@@ -363,6 +364,8 @@ __global__ void __launch_bounds__(320, 1)
   auto bar_v_empty = [&](int st) { return bar0 + 64 + 24 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
+  TileEntry *tab = reinterpret_cast<TileEntry *>(smem + C::OFF_MISC + 16);
   constexpr uint32_t colO0 = 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,16 +394,19 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 8) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
+    {
+      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, lane);
+      if (lane == 0) *ntiles_slot = nt;
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int ntiles = *ntiles_slot;
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
-  KvSchedule sched;
-  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
   TileInfo t;
 
   if (warp == 8) {
@@ -412,7 +418,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int blk = 0; blk < D / 64; ++blk)
           tc::tma_load_3d(sQ(i) + blk * kTile * 128, &tm_q, bar_q_full, blk * 64, y0 + i * kTile, q_z);
       int n = 0;
-      while (sched.next(t)) {
+      while (n < ntiles && (decode_tile(tab[n], t), true)) {
         const int st = n % NS;
         const int z = bh * 2 * cp + t.slot;
         if (n >= NS && !tc::mbar_wait(bar_k_empty(st), ((n / NS) - 1) & 1, wc)) break;
@@ -454,7 +460,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::mma_commit(bar_o_done(i));
       };
       bool ok = tc::mbar_wait(bar_q_full, 0, wc);
-      if (ok && sched.next(t)) {
+      if (ok && ntiles > 0) {
         ok = tc::mbar_wait(bar_k_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
@@ -463,7 +469,7 @@ __global__ void __launch_bounds__(320, 1)
           tc::mma_commit(bar_k_empty(0));
         }
         for (int n = 0; ok; ++n) {
-          const bool more = sched.next(t);
+          const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           // ---- tile 0: PV0(n), then S0(n+1) once PV0(n) has read P0
           if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
@@ -506,7 +512,7 @@ __global__ void __launch_bounds__(320, 1)
     float m_run = -INFINITY, l = 0.f;
     int n = 0;
     bool ok = true;
-    while (sched.next(t)) {
+    while (n < ntiles && (decode_tile(tab[n], t), true)) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(wg), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
@@ -698,7 +704,9 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   fp.tpc = (g.c + kTile - 1) / kTile;
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
   make_rope_theta(g.d, &fp.theta);
-  if (!g.rope) {   // paired query tiles; q, k are used as given
+  // Paired query tiles with a tile table in shared memory; q, k are used as
+  // given. Longer schedules take the one-tile kernel below.
+  if (!g.rope && 2LL * g.cp * fp.tpc <= kMaxTiles) {
     const long long grid2 = BH * 2 * g.cp * ((fp.tpc + 1) / 2);
     if (grid2 > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
     return g.d == 128 ? launch_fwd2_t<128>(mq, mk, mv, fp, (unsigned)grid2, s)

@@ -218,6 +218,56 @@ def test_workload_full_size_sampled(name, mode):
         compare("dq_vs_unpadded", got["dq"][b, h, rows], dq_u, TOL["bf16"]["grad"], TOL["bf16"]["cos"])
 
 
+# Schedules longer than the pipelined kernels' shared-memory tile table
+# (2*cp*ceil(c/128) > 1024 entries) run on the one-tile kernels. cp=128 and
+# c=513 give 1280 entries per CTA, and every chunk ends in a one-row tile.
+LONG_SCHEDULE = dict(B=1, T=2 * 128 * 513, H=1, d=64, cp=128, rope=False)
+
+
+def test_long_schedule_sampled_rows():
+    w = make_workload("long_schedule", T_valid=LONG_SCHEDULE["T"] - 5, **LONG_SCHEDULE)
+    inp = make_inputs(w, seed=77)
+    got = run_gpu(w, inp)
+    c = w.chunk
+    kappas = [0, 1, 2, w.cp - 1, w.cp, w.cp + 1, 2 * w.cp - 2, 2 * w.cp - 1]
+    rows = {0, w.T_valid - 1, w.T - 1}
+    for kap in kappas:
+        rows |= {kap * c, kap * c + 127, kap * c + 128, kap * c + c - 1}
+    rows |= set(np.random.default_rng(5).integers(0, w.T, size=24).tolist())
+    rows = np.array(sorted(rows))
+    real = rows[rows < w.T_valid]
+    tol = TOL[w.dtype]
+    o_r, l_r = A.forward_rows(inp["q"], inp["k"], inp["v"], 0, 0, rows, w.causal, w.T_valid, w.rope)
+    compare("o", got["o"][0, 0, rows], o_r, tol["o"], tol["cos"])
+    compare("lse", got["lse"][0, 0, rows], l_r, tol["lse"])
+    dq_r = A.backward_dq_rows(inp["q"], inp["k"], inp["v"], inp["do"], 0, 0, real, w.causal,
+                              w.T_valid, w.rope)
+    compare("dq", got["dq"][0, 0, real], dq_r, tol["grad"], tol["cos"])
+    # dK, dV at this size through identities of the exact gradient (no RoPE):
+    # each row of dS sums to zero, so sum_k dK_k = 0; each row of P sums to
+    # one, so sum_k dV_k = sum_i dO_i over the real query rows.
+    dk = got["dk"][0, 0].double().numpy()
+    dv = got["dv"][0, 0].double().numpy()
+    do = inp["do"][0, 0, : w.T_valid].double().numpy()
+    assert np.linalg.norm(dk.sum(0)) <= 5e-2 * np.sqrt((dk ** 2).sum())
+    assert np.linalg.norm(dv.sum(0) - do.sum(0)) <= 5e-2 * np.sqrt((dv ** 2).sum())
+    for g in ("dq", "dk", "dv"):
+        assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
+
+
+def test_long_schedule_padded_against_unpadded_oracle():
+    """Only the first 3000 tokens are real; the real rows must equal the oracle
+    on those 3000 tokens alone, for every output and gradient."""
+    w = make_workload("long_schedule_pad", T_valid=3000, **LONG_SCHEDULE)
+    inp = make_inputs(w, seed=78)
+    got = run_gpu(w, inp)
+    wu = make_workload("unpadded", B=1, T=w.T_valid, H=1, d=w.d, cp=1, rope=False)
+    want = _oracle_full(wu, {k: t[:, :, : w.T_valid] for k, t in inp.items()})
+    _check_full(wu, {k: t[:, :, : w.T_valid] for k, t in got.items()}, want)
+    for g in ("dq", "dk", "dv"):
+        assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
+
+
 def test_error_codes_on_device_buffers():
     x = torch.zeros(1, 1, 10, 64, dtype=torch.bfloat16, device="cuda")
     y = torch.empty_like(x)
