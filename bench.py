@@ -40,9 +40,9 @@ DEFAULT_WORKLOAD = "window_32k"
 # on the 32k workload (profiles/tc_kernels_window_32k.md); a kernel missing
 # here has no capture of its current version. Only valid for that workload.
 NCU_TRAFFIC_BYTES = {
-    ("window_32k", "fwd"): 2.213885e9 + 0.115291e9,
-    ("window_32k", "bwd_dkdv"): 4.799820e9 + 0.238431e9,
-    ("window_32k", "bwd_dq"): 4.065538e9 + 0.119980e9,
+    ("window_32k", "fwd"): 2.216601e9 + 0.115951e9,
+    ("window_32k", "bwd_dkdv"): 4.111218e9 + 0.238513e9,
+    ("window_32k", "bwd_dq"): 4.069039e9 + 0.120629e9,
 }
 
 
