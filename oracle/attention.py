@@ -113,6 +113,21 @@ def _heads(x):
     return x, B, H
 
 
+def kv_head(h: int, H: int, H_kv: int) -> int:
+    """K/V head read by query head h when H query heads share H_kv K/V heads.
+
+    "Claude Logs", 2026-06-29 (keep GQA-grouped K/V in the ring) and
+    2026-07-01 (GQA/MQA: K/V heads broadcast to their query heads by a
+    repeat-interleave, whose adjoint is a sum over each group). Under a
+    repeat-interleave, consecutive query heads share a K/V head: query head h
+    reads K/V head h // (H / H_kv). H_kv = H is multi-head attention, H_kv = 1
+    multi-query attention.
+    """
+    if H_kv < 1 or H % H_kv:
+        raise ValueError(f"H_kv={H_kv} must divide H={H}")
+    return h // (H // H_kv)
+
+
 def _rotated(xh: np.ndarray, rope_on: bool) -> np.ndarray:
     if not rope_on:
         return xh
@@ -120,7 +135,8 @@ def _rotated(xh: np.ndarray, rope_on: bool) -> np.ndarray:
 
 
 def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool = False):
-    """Single-pass attention over natural-order [B, H, T, d] inputs.
+    """Single-pass attention over natural-order inputs: q [B, H, T, d], k and v
+    [B, H_kv, T, d] (H_kv divides H; see ``kv_head``).
 
     Returns O [B, H, T, d] and LSE [B, H, T] (float64). RoPE, when on, is applied
     to q and k at their natural (global) positions.
@@ -134,11 +150,12 @@ def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: b
     L = np.zeros(q.shape[:3])
     for b in range(B):
         for h in range(H):
-            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, h], rope_on)
+            hk = kv_head(h, H, k.shape[1])
+            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, hk], rope_on)
             for r0 in range(0, T, _ROW_BLOCK):
                 rows = pos[r0:r0 + _ROW_BLOCK]
                 O[b, h, rows], L[b, h, rows] = partial_attention(
-                    qh[rows], kh, v[b, h], rows, pos, causal, T_valid)
+                    qh[rows], kh, v[b, hk], rows, pos, causal, T_valid)
     return O, L
 
 
@@ -146,7 +163,8 @@ def forward_rows(q, k, v, b: int, h: int, rows, causal: bool = True,
                  T_valid: int | None = None, rope_on: bool = False):
     """O and LSE of selected natural rows of one head (each row is independent)."""
     rows = np.asarray(rows, dtype=np.int64)
-    qh, kh, vh = as_f64(q[b, h]), as_f64(k[b, h]), as_f64(v[b, h])
+    hk = kv_head(h, q.shape[1], k.shape[1])
+    qh, kh, vh = as_f64(q[b, h]), as_f64(k[b, hk]), as_f64(v[b, hk])
     T = kh.shape[0]
     T_valid = T if T_valid is None else T_valid
     qr = rope(qh[rows], rows) if rope_on else qh[rows]
@@ -190,8 +208,11 @@ def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = Non
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     for b in range(B):
         for h in range(H):
-            dq[b, h], dk[b, h], dv[b, h] = _backward_head(
-                q[b, h], k[b, h], v[b, h], o[b, h], lse[b, h], do[b, h], causal, T_valid, rope_on)
+            hk = kv_head(h, H, k.shape[1])
+            dq[b, h], dk_h, dv_h = _backward_head(
+                q[b, h], k[b, hk], v[b, hk], o[b, h], lse[b, h], do[b, h], causal, T_valid, rope_on)
+            dk[b, hk] += dk_h           # a shared K/V head gathers its group's gradients
+            dv[b, hk] += dv_h
     return dq, dk, dv
 
 
@@ -199,7 +220,8 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
                      T_valid: int | None = None, rope_on: bool = False):
     """dq of selected natural rows of one head; each needs only its own row of P."""
     rows = np.asarray(rows, dtype=np.int64)
-    kh, vh, doh = as_f64(k[b, h]), as_f64(v[b, h]), as_f64(do[b, h])
+    hk = kv_head(h, q.shape[1], k.shape[1])
+    kh, vh, doh = as_f64(k[b, hk]), as_f64(v[b, hk]), as_f64(do[b, h])
     T, d = kh.shape
     T_valid = T if T_valid is None else T_valid
     o_r, lse_r = forward_rows(q, k, v, b, h, rows, causal, T_valid, rope_on)
@@ -216,31 +238,39 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
 
 def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
                        T_valid: int | None = None, rope_on: bool = False):
-    """dk, dv of selected natural key rows of one head.
+    """dk, dv of selected natural key rows of K/V head h.
 
-    Needs O and LSE of every query row of the head (computed here, row by row as
-    in ``forward``), then one column of P, dP and dS per selected key.
+    For each query head that reads K/V head h (one head without grouping, see
+    ``kv_head``): O and LSE of every query row of that head (computed here, row
+    by row as in ``forward``), then one column of P, dP and dS per selected
+    key; the group's contributions are summed.
     """
     cols = np.asarray(cols, dtype=np.int64)
-    qh, kh, vh, doh = (as_f64(x[b, h]) for x in (q, k, v, do))
-    T, d = qh.shape
+    H, H_kv = q.shape[1], k.shape[1]
+    kh, vh = as_f64(k[b, h]), as_f64(v[b, h])
+    T, d = kh.shape
     T_valid = T if T_valid is None else T_valid
     pos = np.arange(T)
-    O = np.zeros_like(qh)
-    L = np.zeros(T)
-    qr, kr = _rotated(qh, rope_on), _rotated(kh, rope_on)
-    for r0 in range(0, T, _ROW_BLOCK):
-        rows = pos[r0:r0 + _ROW_BLOCK]
-        O[rows], L[rows] = partial_attention(qr[rows], kr, vh, rows, pos, causal, T_valid)
-    D = np.sum(doh * O, axis=1)
-    ok = allowed(pos, cols, causal, T_valid)            # [T, n_cols]
-    S = (qr @ kr[cols].T) / math.sqrt(d)
-    P = np.where(ok, np.exp(np.where(ok, S, 0.0) - L[:, None]), 0.0)
-    dV = P.T @ doh
-    dP = doh @ vh[cols].T
-    dS = P * (dP - D[:, None])
-    dKr = dS.T @ qr / math.sqrt(d)
-    return (rope_transpose(dKr, cols) if rope_on else dKr), dV
+    kr = _rotated(kh, rope_on)
+    dK = np.zeros((len(cols), d))
+    dV = np.zeros((len(cols), d))
+    for hq in (x for x in range(H) if kv_head(x, H, H_kv) == h):
+        qh, doh = as_f64(q[b, hq]), as_f64(do[b, hq])
+        qr = _rotated(qh, rope_on)
+        O = np.zeros_like(qh)
+        L = np.zeros(T)
+        for r0 in range(0, T, _ROW_BLOCK):
+            rows = pos[r0:r0 + _ROW_BLOCK]
+            O[rows], L[rows] = partial_attention(qr[rows], kr, vh, rows, pos, causal, T_valid)
+        D = np.sum(doh * O, axis=1)
+        ok = allowed(pos, cols, causal, T_valid)            # [T, n_cols]
+        S = (qr @ kr[cols].T) / math.sqrt(d)
+        P = np.where(ok, np.exp(np.where(ok, S, 0.0) - L[:, None]), 0.0)
+        dV += P.T @ doh
+        dP = doh @ vh[cols].T
+        dS = P * (dP - D[:, None])
+        dK += dS.T @ qr / math.sqrt(d)
+    return (rope_transpose(dK, cols) if rope_on else dK), dV
 
 
 # ---------------------------------------------------------- LSE merge ----
@@ -294,7 +324,8 @@ def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = No
     L = np.zeros(q.shape[:3])
     for b in range(B):
         for h in range(H):
-            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, h], rope_on)
+            hk = kv_head(h, H, k.shape[1])
+            qh, kh = _rotated(q[b, h], rope_on), _rotated(k[b, hk], rope_on)
             for r in range(cp):
                 rows = headtail.rank_tokens(T, cp, r)
                 o_run = np.zeros((len(rows), q.shape[3]))
@@ -302,7 +333,7 @@ def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = No
                 for s in range(cp):
                     j = (r - s) % cp
                     keys = headtail.rank_tokens(T, cp, j)
-                    o_s, l_s = partial_attention(qh[rows], kh[keys], v[b, h][keys], rows, keys,
+                    o_s, l_s = partial_attention(qh[rows], kh[keys], v[b, hk][keys], rows, keys,
                                                  causal, T_valid)
                     o_run, l_run = merge(o_run, l_run, o_s, l_s)
                 O[b, h, rows], L[b, h, rows] = o_run, l_run

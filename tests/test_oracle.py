@@ -359,3 +359,100 @@ def test_padding_is_invisible_to_real_rows():
     for a, b in zip(gp, gu):
         assert np.abs(a[:, :, :Tr] - b).max() < 1e-13
         assert np.all(a[:, :, Tr:] == 0.0)                 # pad-row grads are exactly zero
+
+
+# --------------------------------------------- grouped K/V heads (GQA) ----
+
+def test_kv_head_is_repeat_interleave():
+    # repeat-interleave of K/V heads: query heads 0..g-1 read K/V head 0, ...
+    assert [A.kv_head(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [A.kv_head(h, 6, 3) for h in range(6)] == [0, 0, 1, 1, 2, 2]
+    assert [A.kv_head(h, 4, 4) for h in range(4)] == [0, 1, 2, 3]
+    assert [A.kv_head(h, 4, 1) for h in range(4)] == [0, 0, 0, 0]
+    with pytest.raises(ValueError):
+        A.kv_head(0, 6, 4)
+
+
+def _gqa_case(H=6, H_kv=2, T=24, d=8, T_valid=21):
+    q, do = rnd(2, H, T, d), rnd(2, H, T, d)
+    k, v = rnd(2, H_kv, T, d), rnd(2, H_kv, T, d)
+    do[:, :, T_valid:] = 0
+    return q, k, v, do, T_valid
+
+
+def _check_gqa_equals_repeated_mha(rope_on):
+    """GQA == multi-head attention on K/V repeated along heads (np.repeat is a
+    repeat-interleave); the GQA gradient of a K/V head is the sum of the
+    repeated copies' gradients."""
+    q, k, v, do, Tv = _gqa_case()
+    g = q.shape[1] // k.shape[1]
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    O, L = A.forward(q, k, v, True, Tv, rope_on)
+    Om, Lm = A.forward(q, kr, vr, True, Tv, rope_on)
+    err = max(np.abs(O - Om).max(), np.abs(L - Lm).max())
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, Tv, rope_on)
+    dqm, dkm, dvm = A.backward(q, kr, vr, Om, Lm, do, True, Tv, rope_on)
+    B, H_kv, T, d = k.shape
+    err = max(err, np.abs(dq - dqm).max(),
+              np.abs(dk - dkm.reshape(B, H_kv, g, T, d).sum(2)).max(),
+              np.abs(dv - dvm.reshape(B, H_kv, g, T, d).sum(2)).max())
+    return err
+
+
+@pytest.mark.parametrize("rope_on", [False, True])
+def test_gqa_equals_mha_with_repeated_kv(rope_on):
+    assert _check_gqa_equals_repeated_mha(rope_on) < 1e-12
+
+
+def test_planted_gqa_head_map_is_caught(monkeypatch):
+    # the other common grouping (query head h -> K/V head h mod H_kv) must fail
+    monkeypatch.setattr(A, "kv_head", lambda h, H, H_kv: h % H_kv)
+    assert _check_gqa_equals_repeated_mha(False) > 1e-3
+
+
+def test_gqa_backward_against_finite_differences():
+    H, H_kv, T, d, h = 4, 2, 5, 4, 1e-6
+    q, do = rnd(1, H, T, d), rnd(1, H, T, d)
+    k, v = rnd(1, H_kv, T, d), rnd(1, H_kv, T, d)
+
+    def loss(q_, k_, v_):
+        return np.sum(do * A.forward(q_, k_, v_, True, T, True)[0])
+
+    O, L = A.forward(q, k, v, True, T, True)
+    grads = A.backward(q, k, v, O, L, do, True, T, True)
+    worst = 0.0
+    for which, g in enumerate(grads):
+        fd = np.zeros_like(g)
+        for idx in np.ndindex(g.shape):
+            args_p, args_m = [q.copy(), k.copy(), v.copy()], [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        worst = max(worst, np.abs(g - fd).max() / max(np.abs(fd).max(), 1e-3))
+    assert worst <= 1e-6
+
+
+def test_mqa_invariants_and_sampled_match_full():
+    q, k, v, do, Tv = _gqa_case(H=4, H_kv=1)
+    O, L = A.forward(q, k, v, True, Tv)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, Tv)
+    # each softmax row sums to one and each row of dS to zero, over all 4 query heads
+    assert np.allclose(dv.sum(axis=2)[:, 0], do.sum(axis=(1, 2)), atol=1e-12)
+    assert np.abs(dk.sum(axis=2)).max() < 1e-12
+    rows = [0, 5, 20, 23]
+    for b, hq in [(0, 0), (1, 3)]:
+        Or, Lr = A.forward_rows(q, k, v, b, hq, rows, True, Tv)
+        assert np.abs(Or - O[b, hq, rows]).max() < 1e-13 and np.abs(Lr - L[b, hq, rows]).max() < 1e-13
+        assert np.abs(A.backward_dq_rows(q, k, v, do, b, hq, rows, True, Tv) - dq[b, hq, rows]).max() < 1e-12
+    q, k, v, do, Tv = _gqa_case()
+    O, L = A.forward(q, k, v, True, Tv, True)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, Tv, True)
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 1, 1, rows, True, Tv, True)
+    assert np.abs(dk_c - dk[1, 1, rows]).max() < 1e-12 and np.abs(dv_c - dv[1, 1, rows]).max() < 1e-12
+
+
+def test_gqa_ring_equals_single_pass():
+    q, k, v, _, Tv = _gqa_case()
+    O, L = A.forward(q, k, v, True, Tv, True)
+    Or, Lr = A.ring_forward(q, k, v, 3, True, Tv, True)
+    assert np.abs(O - Or).max() < 1e-12 and np.abs(L - Lr).max() < 1e-12
