@@ -72,11 +72,19 @@ def measured_peaks():
             "source": "fallback"}
 
 
+def input_bytes(w, elt=2):
+    """Bytes of q, k, v, dO (and of o, dq, dk, dv) in the storage dtype."""
+    return 2 * (w.H + w.kv_heads) * w.B * w.T * w.d * elt
+
+
 def workload_config(w):
-    return {"workload": w.name, "B": w.B, "T": w.T, "T_valid": w.T_valid, "H": w.H, "d": w.d,
-            "cp": w.cp, "causal": w.causal, "rope": w.rope,
-            "l2": "inputs larger than L2: q,k,v,dO = %d MiB per step vs 129 MB L2"
-                  % (4 * w.B * w.H * w.T * w.d * 2 // 2 ** 20)}
+    cfg = {"workload": w.name, "B": w.B, "T": w.T, "T_valid": w.T_valid, "H": w.H, "d": w.d,
+           "cp": w.cp, "causal": w.causal, "rope": w.rope,
+           "l2": "inputs larger than L2: q,k,v,dO = %d MiB per step vs 129 MB L2"
+                 % (input_bytes(w) // 2 ** 20)}
+    if w.kv_heads != w.H:
+        cfg["H_kv"] = w.kv_heads
+    return cfg
 
 
 # ----------------------------------------------------------- rank logic ----
@@ -193,8 +201,10 @@ def oracle_sample(w, seconds_target=12.0, max_heads=8):
     heads, t0 = 0, time.perf_counter()
     while heads < min(max_heads, w.H):
         sl = slice(heads, heads + 1)
-        O, L = A.forward(q[:, sl], k[:, sl], v[:, sl], w.causal, T_s, w.rope)
-        A.backward(q[:, sl], k[:, sl], v[:, sl], O, L, do[:, sl], w.causal, T_s, w.rope)
+        hk = heads // (w.H // w.kv_heads)     # the K/V head this query head reads
+        kl = slice(hk, hk + 1)
+        O, L = A.forward(q[:, sl], k[:, kl], v[:, kl], w.causal, T_s, w.rope)
+        A.backward(q[:, sl], k[:, kl], v[:, kl], O, L, do[:, sl], w.causal, T_s, w.rope)
         heads += 1
         if time.perf_counter() - t0 >= seconds_target:
             break
@@ -268,7 +278,8 @@ def run_ours(args):
     host_in = {k: v.pin_memory() for k, v in inp.items()}
     nat = {k: v.to(dev) for k, v in inp.items()}
     sh = {k: torch.empty_like(v) for k, v in nat.items()}
-    o, dq, dk, dv = (torch.empty_like(sh["q"]) for _ in range(4))
+    o, dq = torch.empty_like(sh["q"]), torch.empty_like(sh["q"])
+    dk, dv = torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
     lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
     ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8, device=dev)
     outs = {"o": o, "dq": dq, "dk": dk, "dv": dv}
@@ -397,8 +408,8 @@ def run_ours(args):
         "bwd_dkdv": ("tensor", 4 * unit_flops),
         "bwd_dq": ("tensor", 1 * unit_flops),     # S and dP recomputation is not credited
         "bwd_D": ("hbm", 2 * tensor_bytes + w.B * w.H * w.T * 4),
-        "shard": ("hbm", 4 * 2 * tensor_bytes),
-        "unshard": ("hbm", 4 * 2 * tensor_bytes),
+        "shard": ("hbm", 2 * input_bytes(w, elt)),     # read + write of q, k, v, dO
+        "unshard": ("hbm", 2 * input_bytes(w, elt)),   # of o, dq, dk, dv
     }
     ker_rep = {}
     for name, (bound, work) in ker_work.items():

@@ -22,7 +22,8 @@ F32, BF16 = 0, 1
 EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshard_rope",
            "cpattn_shard_index", "cpattn_fwd",
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
-           "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc")
+           "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
+           "cpattn_fwd_gqa", "cpattn_bwd_gqa")
 
 
 class CpattnError(RuntimeError):
@@ -46,6 +47,8 @@ def _declare(lib):
         "cpattn_fwd": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _vp],
         "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
         "cpattn_bwd_noalloc": [_vp] * 9 + [_i] * 9 + [_vp],
+        "cpattn_fwd_gqa": [_vp] * 5 + [_i] * 10 + [_vp],
+        "cpattn_bwd_gqa": [_vp] * 10 + [_i] * 10 + [_vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
@@ -107,6 +110,11 @@ def cpattn_fwd(q, k, v, o, lse, B, T, T_valid, H, d, cp, causal, rope, dt, strea
     _check(lib().cpattn_fwd(q, k, v, o, lse, B, T, T_valid, H, d, cp, causal, rope, dt, stream))
 
 
+def cpattn_fwd_gqa(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, rope, dt, stream=None):
+    _check(lib().cpattn_fwd_gqa(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, rope, dt,
+                                stream))
+
+
 def cpattn_bwd_workspace_bytes(B, T, H, d):
     return int(lib().cpattn_bwd_workspace_bytes(B, T, H, d))
 
@@ -115,6 +123,12 @@ def cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, 
                dt, stream=None):
     _check(lib().cpattn_bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, d, cp,
                             causal, rope, dt, stream))
+
+
+def cpattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal,
+                   rope, dt, stream=None):
+    _check(lib().cpattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d,
+                                cp, causal, rope, dt, stream))
 
 
 def cpattn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, T, T_valid, H, d, cp, causal, rope, dt,
@@ -192,18 +206,41 @@ def unshard_rope(src, dst, cp, stream=None):
     cpattn_unshard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
 
 
-def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None):
+def _kv_heads(q, *kv):
+    """K/V head count of [B,H_kv,T,d] tensors that go with q [B,H,T,d]."""
     B, H, T, d = q.shape
-    cpattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, T if T_valid is None else T_valid,
-               H, d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
+    H_kv = kv[0].shape[1]
+    for t in kv:
+        if tuple(t.shape) != (B, H_kv, T, d):
+            raise CpattnError(ERR_SHAPE, f"K/V-side tensor of shape {tuple(t.shape)} does not match "
+                                         f"q {tuple(q.shape)} with {H_kv} K/V heads")
+    return H_kv
+
+
+def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None):
+    """o, lse = attention(q, k, v); k, v may have fewer heads than q (grouped K/V)."""
+    B, H, T, d = q.shape
+    H_kv = _kv_heads(q, k, v)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, T if T_valid is None else T_valid)
+    tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
+    if H_kv == H:
+        cpattn_fwd(*args, H, *tail)
+    else:
+        cpattn_fwd_gqa(*args, H, H_kv, *tail)
 
 
 def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=True, rope=False,
         stream=None):
+    """dq, dk, dv of sum(dO * o); k, v, dk, dv may have fewer heads than q."""
     B, H, T, d = q.shape
-    cpattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
-               _ptr(dv), _ptr(workspace), B, T, T if T_valid is None else T_valid, H, d, cp,
-               int(causal), int(rope), _dtype_code(q), _stream(stream))
+    H_kv = _kv_heads(q, k, v, dk, dv)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
+            _ptr(workspace), B, T, T if T_valid is None else T_valid)
+    tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
+    if H_kv == H:
+        cpattn_bwd(*args, H, *tail)
+    else:
+        cpattn_bwd_gqa(*args, H, H_kv, *tail)
 
 
 def merge(o_parts, lse_parts, o, lse, stream=None):

@@ -103,11 +103,19 @@ static cpattn_status check_attn(int B, int T, int T_valid, int H, int d, int cp,
   return CPATTN_OK;
 }
 
-static Geometry geometry(int B, int H, int T, int T_valid, int d, int cp, int causal, int rope) {
+static Geometry geometry(int B, int H, int T, int T_valid, int d, int cp, int causal, int rope,
+                         int Hkv = 0) {
   Geometry g;
   g.B = B; g.H = H; g.T = T; g.T_valid = T_valid; g.d = d; g.cp = cp;
   g.c = T / (2 * cp); g.causal = causal; g.rope = rope;
+  g.Hkv = Hkv > 0 ? Hkv : H;
   return g;
+}
+
+static cpattn_status check_heads(int H, int H_kv) {
+  if (H_kv < 1 || H_kv > H || H % H_kv != 0)
+    return fail(CPATTN_ERR_SHAPE, "H_kv=%d must divide H=%d", H_kv, H);
+  return CPATTN_OK;
 }
 
 static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
@@ -208,18 +216,26 @@ cpattn_status cpattn_unshard_rope(const void *src, void *dst, int B, int H, int 
 cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                          int B, int T, int T_valid, int H, int d, int cp, int causal, int rope,
                          cpattn_dtype dt, cpattn_stream_t stream) {
+  return cpattn_fwd_gqa(q, k, v, o, lse, B, T, T_valid, H, H, d, cp, causal, rope, dt, stream);
+}
+
+cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                             int rope, cpattn_dtype dt, cpattn_stream_t stream) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
   if (st != CPATTN_OK) return st;
+  if ((st = check_heads(H, H_kv)) != CPATTN_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
   const size_t elt = dt == CPATTN_F32 ? 4 : 2;
   const size_t tb = (size_t)B * H * T * d * elt;
-  if (overlaps(o, tb, q, tb) || overlaps(o, tb, k, tb) || overlaps(o, tb, v, tb) ||
+  const size_t tkv = (size_t)B * H_kv * T * d * elt;
+  if (overlaps(o, tb, q, tb) || overlaps(o, tb, k, tkv) || overlaps(o, tb, v, tkv) ||
       overlaps(lse, (size_t)B * H * T * 4, o, tb))
     return fail(CPATTN_ERR_ARG, "outputs overlap inputs");
-  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
+  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   trace_record(0, s);
   if (dt == CPATTN_F32)
@@ -242,27 +258,41 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
                          const float *lse, const void *dO, void *dq, void *dk, void *dv,
                          void *workspace, int B, int T, int T_valid, int H, int d, int cp,
                          int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream) {
+  return cpattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H, d, cp,
+                        causal, rope, dt, stream);
+}
+
+cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                             void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                             int cp, int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
   if (st != CPATTN_OK) return st;
+  if ((st = check_heads(H, H_kv)) != CPATTN_OK) return st;
   const void *ptrs[] = {q, k, v, o, lse, dO, dq, dk, dv, workspace};
   for (const void *p : ptrs)
     if (!aligned16(p)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
   const size_t elt = dt == CPATTN_F32 ? 4 : 2;
-  const size_t tb = (size_t)B * H * T * d * elt;
+  const size_t tq = (size_t)B * H * T * d * elt;
+  const size_t tkv = (size_t)B * H_kv * T * d * elt;
   const size_t wb = cpattn_bwd_workspace_bytes(B, T, H, d);
   const void *outs[] = {dq, dk, dv};
+  const size_t out_b[] = {tq, tkv, tkv};
   const void *ins[] = {q, k, v, o, dO};
-  for (const void *a : outs) {
-    for (const void *b : ins)
-      if (overlaps(a, tb, b, tb)) return fail(CPATTN_ERR_ARG, "gradient outputs overlap inputs");
-    for (const void *b : outs)
-      if (a != b && overlaps(a, tb, b, tb)) return fail(CPATTN_ERR_ARG, "gradient outputs overlap");
-    if (overlaps(a, tb, workspace, wb)) return fail(CPATTN_ERR_ARG, "workspace overlaps outputs");
+  const size_t in_b[] = {tq, tkv, tkv, tq, tq};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 5; ++j)
+      if (overlaps(outs[i], out_b[i], ins[j], in_b[j]))
+        return fail(CPATTN_ERR_ARG, "gradient outputs overlap inputs");
+    for (int j = 0; j < 3; ++j)
+      if (i != j && overlaps(outs[i], out_b[i], outs[j], out_b[j]))
+        return fail(CPATTN_ERR_ARG, "gradient outputs overlap");
+    if (overlaps(outs[i], out_b[i], workspace, wb)) return fail(CPATTN_ERR_ARG, "workspace overlaps outputs");
   }
-  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope);
+  Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
   trace_record(0, s);

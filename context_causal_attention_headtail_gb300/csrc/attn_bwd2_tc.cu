@@ -26,6 +26,7 @@ struct Bwd2Params {
   __nv_bfloat16 *dq, *dk, *dv;
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
+  int group;   // query heads per K/V head
   float scale, scale_log2;
 };
 
@@ -95,6 +96,7 @@ __global__ void __launch_bounds__(320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int bh = blockIdx.x % p.BH;
+  const int bkv = bh / p.group;                   // K/V head of this query head
   const int g = blockIdx.x / p.BH;
   const int kq = 2 * cp - 1 - g / tpc;
   const int qt = tpc - 1 - g % tpc;
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(320, 1)
         const int st = n % NS;
         if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
         tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
-        const int z = bh * 2 * cp + t.slot;
+        const int z = bkv * 2 * cp + t.slot;
         for (int blk = 0; blk < D / 64; ++blk) {
           tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_kv_full(st), blk * 64, t.y0, z);
           tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_kv_full(st), blk * 64, t.y0, z);
@@ -363,13 +365,14 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
-  const int bh = blockIdx.x % p.BH;
-  const int g = blockIdx.x / p.BH;
+  const int BHkv = p.BH / p.group;
+  const int bkv = blockIdx.x % BHkv;  // K/V head; its group's query heads are bkv*group + [0, group)
+  const int g = blockIdx.x / BHkv;
   const int kk_chunk = g / tpc;     // earliest keys first: they are seen by the most queries
   const int kt = g % tpc;
   int rk, hk;
   owner_of(kk_chunk, cp, rk, hk);
-  const int k_z = bh * 2 * cp + 2 * rk + hk;
+  const int k_z = bkv * 2 * cp + 2 * rk + hk;
   const int k_pos0 = kk_chunk * c + kt * kTile;
   const int k_rows = min(kTile, c - kt * kTile);
 
@@ -399,6 +402,7 @@ __global__ void __launch_bounds__(320, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = *ntiles_slot;
+  const int ntot = ntiles * p.group;   // the table once per query head of the group
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
@@ -415,11 +419,13 @@ __global__ void __launch_bounds__(320, 1)
         tc::tma_load_3d(sV + blk * kTile * 128, &tm_v, bar_kv_full, blk * 64, kt * kTile, k_z);
       }
     }
-    int n = 0;
-    while (n < ntiles && (decode_tile(tab[n], t), true)) {
+    int n = 0, ent = 0, gi = 0;
+    while (n < ntot) {
+      decode_tile(tab[ent], t);
       const int st = n % NS;
       if (n >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(bar_qd_empty(st), ((n / NS) - 1) & 1, wc))) break;
-      const int z = bh * 2 * cp + t.slot;
+      const int bq = bkv * p.group + gi;   // query head
+      const int z = bq * 2 * cp + t.slot;
       if (lane == 0) {
         tc::mbar_arrive_expect_tx(bar_qd_full(st), 2 * C::TILE);
         for (int blk = 0; blk < D / 64; ++blk) {
@@ -427,7 +433,7 @@ __global__ void __launch_bounds__(320, 1)
           tc::tma_load_3d(sDO(st) + blk * kTile * 128, &tm_do, bar_qd_full(st), blk * 64, t.y0, z);
         }
       }
-      const long long row0 = (long long)bh * p.T + (long long)t.slot * c + t.y0;
+      const long long row0 = (long long)bq * p.T + (long long)t.slot * c + t.y0;
       // All eight loads are issued before any store so their latencies overlap.
       float lv[4], dv[4];
 #pragma unroll
@@ -445,6 +451,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc::mbar_arrive(bar_qd_full(st));
       ++n;
+      if (++ent == ntiles) { ent = 0; ++gi; }
     }
     if (lane == 0) {
       tc::mbar_wait(bar_kv_full, 0, drain);
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(320, 1)
         tc::mma_commit(bar_dp_full);
       };
       bool ok = tc::mbar_wait(bar_kv_full, 0, wc);
-      if (ok && ntiles > 0) {
+      if (ok && ntot > 0) {
         ok = tc::mbar_wait(bar_qd_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
@@ -478,7 +485,7 @@ __global__ void __launch_bounds__(320, 1)
           issue_dp(0);
         }
         for (int n = 0; ok; ++n) {
-          const bool more = n + 1 < ntiles;
+          const bool more = n + 1 < ntot;
           const int st = n % NS, st1 = (n + 1) % NS;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
           if (!(ok = tc::mbar_wait(bar_p_ready, n & 1, wc))) break;
@@ -520,11 +527,12 @@ __global__ void __launch_bounds__(320, 1)
     const int k_pos = k_pos0 + row;
     const bool valid = row < k_rows;
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const long long grow = (long long)bh * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
+    const long long grow = (long long)bkv * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
     const float sl2 = p.scale_log2;
-    int n = 0;
+    int n = 0, ent = 0;
     bool ok = true;
-    while (n < ntiles && (decode_tile(tab[n], t), true)) {
+    while (n < ntot) {
+      decode_tile(tab[ent], t);
       const int st = n % NS;
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full, n & 1, wc));
       if (!ok) break;
@@ -615,6 +623,7 @@ __global__ void __launch_bounds__(320, 1)
       tc::tc_fence_before();
       tc::mbar_arrive(bar_ds_ready);
       ++n;
+      if (++ent == ntiles) ent = 0;
     }
     if (ok) {
       __nv_bfloat16 *dst = (h == 0 ? p.dv : p.dk) + grow * D;
@@ -648,7 +657,7 @@ cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const 
     auto kern = dkdv2_tc_kernel<D>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
-    kern<<<grid, 320, smem, s>>>(mq, mk, mv, mdo, bp);
+    kern<<<grid / bp.group, 320, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
     cpattn_status st = check_launch("tensor-core dK/dV kernel (pipelined)");
     if (st != CPATTN_OK) return st;
     trace_record(2, s);
@@ -668,9 +677,10 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
                                const Geometry &g, cudaStream_t s) {
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
+  const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_slots) ||
-      !make_tile_map(&mv, v, g.d, g.c, n_slots) || !make_tile_map(&mdo, dO, g.d, g.c, n_slots))
+  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_kv_slots) ||
+      !make_tile_map(&mv, v, g.d, g.c, n_kv_slots) || !make_tile_map(&mdo, dO, g.d, g.c, n_slots))
     return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
   Bwd2Params bp;
   bp.q = static_cast<const __nv_bfloat16 *>(q);
@@ -682,6 +692,7 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   bp.dv = static_cast<__nv_bfloat16 *>(dv);
   bp.err = device_err_flag();
   bp.BH = (int)BH;
+  bp.group = g.H / g.Hkv;
   bp.T = g.T;
   bp.T_valid = g.T_valid;
   bp.c = g.c;

@@ -31,6 +31,7 @@ struct BwdParams {
   __nv_bfloat16 *out0, *out1;  // dkdv: dK, dV ; dq: dQ, unused
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
+  int group;   // query heads per K/V head
   float scale;       // 1/sqrt(d)
   float scale_log2;  // log2(e)/sqrt(d)
   RopeTheta theta;
@@ -130,13 +131,14 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   // Key tile: earliest natural position first (it is seen by the most queries).
-  const int bh = blockIdx.x % p.BH;
-  const int g = blockIdx.x / p.BH;
+  const int BHkv = p.BH / p.group;
+  const int bkv = blockIdx.x % BHkv;               // K/V head
+  const int g = blockIdx.x / BHkv;
   const int kk_chunk = g / tpc;
   const int kt = g % tpc;
   int rk, hk;
   owner_of(kk_chunk, cp, rk, hk);
-  const int k_z = bh * 2 * cp + 2 * rk + hk;
+  const int k_z = bkv * 2 * cp + 2 * rk + hk;
   const int k_pos0 = kk_chunk * c + kt * kTile;
   const int k_rows = min(kTile, c - kt * kTile);
 
@@ -166,8 +168,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
-  QSchedule sched;
-  sched.init(cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1);
+  GroupQSchedule sched;
+  sched.init(p.group, cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1);
   const int k_ragged = k_rows < kTile;
   TileInfo t;
 
@@ -186,7 +188,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     while (sched.next(t, k_ragged)) {
       const int st = n % NS;
       if (n >= NS && !__all_sync(0xffffffffu, tc::mbar_wait(bar_qd_empty(st), ((n / NS) - 1) & 1, wc))) break;
-      const int z = bh * 2 * cp + t.slot;
+      const int bq = bkv * p.group + sched.gi;   // query head
+      const int z = bq * 2 * cp + t.slot;
       if (lane == 0) {
         tc::mbar_arrive_expect_tx(bar_qd_full(st), 2 * C::TILE);
         for (int blk = 0; blk < D / 64; ++blk) {
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
           tc::tma_load_3d(sDO(st) + blk * kTile * 128, &tm_do, bar_qd_full(st), blk * 64, t.y0, z);
         }
       }
-      const long long row0 = (long long)bh * p.T + (long long)t.slot * c + t.y0;
+      const long long row0 = (long long)bq * p.T + (long long)t.slot * c + t.y0;
       float lv[4], dv[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     }
     if (ok) {
       const bool valid = row < k_rows;
-      const long long grow = (long long)bh * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
+      const long long grow = (long long)bkv * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
       if (n > 0) {
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_mma_done, (n - 1) & 1, wc));
         if (ok) {
@@ -381,6 +384,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int bh = blockIdx.x % p.BH;
+  const int bkv = bh / p.group;                    // K/V head of this query head
   const int g = blockIdx.x / p.BH;
   const int kq = 2 * cp - 1 - g / tpc;
   const int qt = tpc - 1 - g % tpc;
@@ -431,7 +435,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         const int st = n % NS;
         if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
         tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
-        const int z = bh * 2 * cp + t.slot;
+        const int z = bkv * 2 * cp + t.slot;
         for (int blk = 0; blk < D / 64; ++blk) {
           tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_kv_full(st), blk * 64, t.y0, z);
           tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_kv_full(st), blk * 64, t.y0, z);
@@ -560,7 +564,7 @@ cpattn_status launch_bwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
     bp.out0 = dk;
     bp.out1 = dv;
-    kern<<<grid, threads, smem, s>>>(mq, mk, mv, mdo, bp);
+    kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
     cpattn_status st = check_launch("tensor-core dK/dV kernel");
     if (st != CPATTN_OK) return st;
     trace_record(2, s);
@@ -588,9 +592,10 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
     return launch_bwd2_bf16(q, k, v, lse, dO, dq, dk, dv, D, g, s);
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
+  const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;
   CUtensorMap mq, mk, mv, mdo;
-  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_slots) ||
-      !make_tile_map(&mv, v, g.d, g.c, n_slots) || !make_tile_map(&mdo, dO, g.d, g.c, n_slots))
+  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_kv_slots) ||
+      !make_tile_map(&mv, v, g.d, g.c, n_kv_slots) || !make_tile_map(&mdo, dO, g.d, g.c, n_slots))
     return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
   BwdParams bp;
   bp.lse = lse;
@@ -598,6 +603,7 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
   bp.out0 = bp.out1 = nullptr;
   bp.err = device_err_flag();
   bp.BH = (int)BH;
+  bp.group = g.H / g.Hkv;
   bp.T = g.T;
   bp.T_valid = g.T_valid;
   bp.c = g.c;

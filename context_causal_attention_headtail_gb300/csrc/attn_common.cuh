@@ -94,6 +94,28 @@ struct QSchedule {
   }
 };
 
+// With grouped K/V heads a key tile is seen by the query tiles of every query
+// head of its group: QSchedule's list for each of them, head by head; gi is
+// the current head's index inside the group.
+struct GroupQSchedule {
+  QSchedule q;
+  int group, gi;
+
+  __device__ __forceinline__ void init(int group_, int cp_, int c_, int j_, int causal_, int T_valid_,
+                                       int kmin_, int kmax_) {
+    group = group_;
+    gi = 0;
+    q.init(cp_, c_, j_, causal_, T_valid_, kmin_, kmax_);
+  }
+  __device__ __forceinline__ bool next(TileInfo &t, int k_ragged) {
+    while (!q.next(t, k_ragged)) {
+      if (++gi >= group) return false;
+      q.s = 0; q.half = 0; q.qt = -1;
+    }
+    return true;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // Precomputed schedules. The pipelined kernels build their whole tile list
 // once per CTA in shared memory (one warp, lanes in parallel), so the MMA

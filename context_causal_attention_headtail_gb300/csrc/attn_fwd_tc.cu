@@ -31,6 +31,7 @@ struct FwdParams {
   float *lse;
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
+  int group;   // query heads per K/V head
   float scale_log2;  // log2(e) / sqrt(d)
   RopeTheta theta;
 };
@@ -78,6 +79,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   // ---- which query tile: heaviest (latest natural position) first, heads interleaved
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int bh = blockIdx.x % p.BH;
+  const int bkv = bh / p.group;                   // K/V head of this query head
   const int g = blockIdx.x / p.BH;
   const int kq = 2 * cp - 1 - g / tpc;
   const int qt = tpc - 1 - g % tpc;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         const int st = n % NS;
         if (n >= NS && !tc::mbar_wait(bar_kv_empty(st), ((n / NS) - 1) & 1, wc)) break;
         tc::mbar_arrive_expect_tx(bar_kv_full(st), 2 * C::TILE);
-        const int z = bh * 2 * cp + t.slot;
+        const int z = bkv * 2 * cp + t.slot;
         for (int blk = 0; blk < D / 64; ++blk) {
           tc::tma_load_3d(sK(st) + blk * kTile * 128, &tm_k, bar_kv_full(st), blk * 64, t.y0, z);
           tc::tma_load_3d(sV(st) + blk * kTile * 128, &tm_v, bar_kv_full(st), blk * 64, t.y0, z);
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(320, 1)
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int ppc = (tpc + 1) / 2;                  // tile pairs per chunk
   const int bh = blockIdx.x % p.BH;
+  const int bkv = bh / p.group;                   // K/V head of this query head
   const int g = blockIdx.x / p.BH;
   const int kq = 2 * cp - 1 - g / ppc;            // latest chunks first: they carry the most work
   const int pq = ppc - 1 - g % ppc;
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(320, 1)
       int n = 0;
       while (n < ntiles && (decode_tile(tab[n], t), true)) {
         const int st = n % NS;
-        const int z = bh * 2 * cp + t.slot;
+        const int z = bkv * 2 * cp + t.slot;
         if (n >= NS && !tc::mbar_wait(bar_k_empty(st), ((n / NS) - 1) & 1, wc)) break;
         tc::mbar_arrive_expect_tx(bar_k_full(st), C::TILE);
         for (int blk = 0; blk < D / 64; ++blk)
@@ -687,15 +690,17 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
                               const Geometry &g, cudaStream_t s) {
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
+  const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;
   CUtensorMap mq, mk, mv;
-  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_slots) ||
-      !make_tile_map(&mv, v, g.d, g.c, n_slots))
+  if (!make_tile_map(&mq, q, g.d, g.c, n_slots) || !make_tile_map(&mk, k, g.d, g.c, n_kv_slots) ||
+      !make_tile_map(&mv, v, g.d, g.c, n_kv_slots))
     return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
   FwdParams fp;
   fp.o = static_cast<__nv_bfloat16 *>(o);
   fp.lse = lse;
   fp.err = device_err_flag();
   fp.BH = (int)BH;
+  fp.group = g.H / g.Hkv;
   fp.T = g.T;
   fp.T_valid = g.T_valid;
   fp.c = g.c;

@@ -34,6 +34,7 @@ void make_rope_theta(int d, RopeTheta *t);
 struct Geometry {
   int B, H, T, T_valid, d, cp, c;  // c = T / (2 cp)
   int causal, rope;
+  int Hkv;                         // K/V heads; query head h reads K/V head h / (H / Hkv)
 };
 
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------

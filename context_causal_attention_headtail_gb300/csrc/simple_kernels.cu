@@ -375,7 +375,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float *__restrict__ 
   const int r = i / (2 * g.c);
   const int qp = natural_pos(i, g.c, g.cp);
   const float scale = 1.f / sqrtf((float)D);
-  const float *kb = k + bh * g.T * D, *vb = v + bh * g.T * D;
+  const long long bkv = bh / (g.H / g.Hkv);   // K/V head of this query head's group
+  const float *kb = k + bkv * g.T * D, *vb = v + bkv * g.T * D;
   float qr[V];
   load_row<D>(q + row * D, lane, qr);
   if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
@@ -440,7 +441,8 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
   const int r = i / (2 * g.c);
   const int qp = natural_pos(i, g.c, g.cp);
   const float scale = 1.f / sqrtf((float)D);
-  const float *kb = k + bh * g.T * D, *vb = v + bh * g.T * D;
+  const long long bkv = bh / (g.H / g.Hkv);
+  const float *kb = k + bkv * g.T * D, *vb = v + bkv * g.T * D;
   float qr[V], dor[V], acc[V];
   load_row<D>(q + row * D, lane, qr);
   if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
@@ -474,8 +476,10 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
   for (int e = 0; e < V; ++e) dq[row * D + lane + 32 * e] = acc[e];
 }
 
-// dK, dV: one warp per sharded key row. Its K/V travel the ring: at step s
-// they sit on rank (j + s) mod cp, whose queries add their contributions.
+// dK, dV: one warp per sharded key row of one K/V head. Its K/V travel the
+// ring: at step s they sit on rank (j + s) mod cp, whose queries add their
+// contributions; with grouped K/V heads, the group's query heads add theirs
+// one after another.
 template <int D>
 __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restrict__ q,
                                                            const float *__restrict__ k,
@@ -488,39 +492,43 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restri
   constexpr int V = D / 32;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= (long long)g.B * g.H * g.T) return;
-  const long long bh = row / g.T;
+  if (row >= (long long)g.B * g.Hkv * g.T) return;
+  const long long bkv = row / g.T;
   const int i = (int)(row % g.T);
   const int j = i / (2 * g.c);
   const int kp = natural_pos(i, g.c, g.cp);
   const float scale = 1.f / sqrtf((float)D);
-  const float *qb = q + bh * g.T * D, *dob = dO + bh * g.T * D;
-  const float *lb = lse + bh * g.T, *Db = Dv + bh * g.T;
+  const int group = g.H / g.Hkv;
   float kr[V], vr[V], adk[V], adv[V];
   load_row<D>(k + row * D, lane, kr);
   if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
   load_row<D>(v + row * D, lane, vr);
 #pragma unroll
   for (int e = 0; e < V; ++e) { adk[e] = 0.f; adv[e] = 0.f; }
-  for (int s = 0; s < g.cp; ++s) {
-    const int r = (j + s) % g.cp;
-    for (int half = 0; half < 2; ++half) {
-      const int kappa = chunk_of(r, half, g.cp);
-      const int row0 = 2 * g.c * r + half * g.c;
-      for (int u = 0; u < g.c; ++u) {
-        const int qp = kappa * g.c + u;
-        if (!pair_allowed(qp, kp, g)) continue;
-        const int t = row0 + u;
-        float qr[V], dor[V];
-        load_row<D>(qb + (long long)t * D, lane, qr);
-        if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
-        load_row<D>(dob + (long long)t * D, lane, dor);
-        const float p = expf(warp_dot<D>(qr, kr) * scale - lb[t]);
-        const float ds = p * (warp_dot<D>(dor, vr) - Db[t]);
+  for (int gi = 0; gi < group; ++gi) {
+    const long long bh = bkv * group + gi;
+    const float *qb = q + bh * g.T * D, *dob = dO + bh * g.T * D;
+    const float *lb = lse + bh * g.T, *Db = Dv + bh * g.T;
+    for (int s = 0; s < g.cp; ++s) {
+      const int r = (j + s) % g.cp;
+      for (int half = 0; half < 2; ++half) {
+        const int kappa = chunk_of(r, half, g.cp);
+        const int row0 = 2 * g.c * r + half * g.c;
+        for (int u = 0; u < g.c; ++u) {
+          const int qp = kappa * g.c + u;
+          if (!pair_allowed(qp, kp, g)) continue;
+          const int t = row0 + u;
+          float qr[V], dor[V];
+          load_row<D>(qb + (long long)t * D, lane, qr);
+          if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+          load_row<D>(dob + (long long)t * D, lane, dor);
+          const float p = expf(warp_dot<D>(qr, kr) * scale - lb[t]);
+          const float ds = p * (warp_dot<D>(dor, vr) - Db[t]);
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          adv[e] = fmaf(p, dor[e], adv[e]);
-          adk[e] = fmaf(ds, qr[e], adk[e]);
+          for (int e = 0; e < V; ++e) {
+            adv[e] = fmaf(p, dor[e], adv[e]);
+            adk[e] = fmaf(ds, qr[e], adk[e]);
+          }
         }
       }
     }
@@ -550,12 +558,13 @@ cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, con
   (void)o;
   const long long rows = (long long)g.B * g.H * g.T;
   const unsigned blocks = (unsigned)((rows + 3) / 4);
+  const unsigned kv_blocks = (unsigned)(((long long)g.B * g.Hkv * g.T + 3) / 4);
   if (g.d == 128) {
-    bwd_dkdv_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    bwd_dkdv_f32_kernel<128><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
     trace_record(2, s);
     bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
   } else {
-    bwd_dkdv_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    bwd_dkdv_f32_kernel<64><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
     trace_record(2, s);
     bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
   }

@@ -32,6 +32,11 @@ class Workload:
     rope: bool
     dtype: str      # "f32" or "bf16": storage and input dtype of q, k, v, dO
     qkv_std: float
+    H_kv: int = 0   # K/V heads (grouped-query attention); 0 means H
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv or self.H
 
     @property
     def chunk(self) -> int:
@@ -55,7 +60,7 @@ class Workload:
         return 3.5 * self.fwd_flops()
 
 
-# The five workloads of the benchmark description.
+# The five workloads of the benchmark description, then the grouped-K/V one.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", B=1, T=512, T_valid=512, H=4, d=64, cp=2,
                           causal=True, rope=False, dtype="f32", qkv_std=1.0),
@@ -67,6 +72,9 @@ WORKLOADS = {
                            causal=True, rope=True, dtype="bf16", qkv_std=0.5),
     "padded_12289": Workload("padded_12289", B=2, T=12296, T_valid=12289, H=8, d=128, cp=4,
                              causal=True, rope=True, dtype="bf16", qkv_std=0.5),
+    # Grouped K/V heads at 32k: 32 query heads over 8 K/V heads of d=128.
+    "gqa_32k": Workload("gqa_32k", B=1, T=32768, T_valid=32768, H=32, d=128, cp=2,
+                        causal=True, rope=True, dtype="bf16", qkv_std=0.5, H_kv=8),
 }
 
 # Seeds: 1234 + the workload's position in the list above (1-based).
@@ -75,19 +83,21 @@ SEEDS = {name: 1234 + i + 1 for i, name in enumerate(WORKLOADS)}
 
 def make_workload(name: str = "custom", *, B: int, T: int, H: int, d: int, cp: int,
                   T_valid: int | None = None, causal: bool = True, rope: bool = False,
-                  dtype: str = "bf16", qkv_std: float = 0.5) -> Workload:
+                  dtype: str = "bf16", qkv_std: float = 0.5, H_kv: int = 0) -> Workload:
     return Workload(name, B=B, T=T, T_valid=T if T_valid is None else T_valid, H=H, d=d,
-                    cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std)
+                    cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std, H_kv=H_kv)
 
 
 def make_inputs(w: Workload, seed: int) -> dict[str, torch.Tensor]:
-    """q, k, v, dO in natural token order, shape [B, H, T, d], CPU, storage dtype."""
+    """q, k, v, dO in natural token order, CPU, storage dtype: q and dO [B, H, T, d],
+    k and v [B, H_kv, T, d]."""
     g = torch.Generator(device="cpu")
     g.manual_seed(seed)
     shape = (w.B, w.H, w.T, w.d)
     out = {}
     for name in ("q", "k", "v"):
-        out[name] = (torch.randn(shape, generator=g, dtype=torch.float32) * w.qkv_std).to(w.torch_dtype)
+        sh = shape if name == "q" else (w.B, w.kv_heads, w.T, w.d)
+        out[name] = (torch.randn(sh, generator=g, dtype=torch.float32) * w.qkv_std).to(w.torch_dtype)
     do = torch.randn(shape, generator=g, dtype=torch.float32)
     if w.T_valid < w.T:
         do[:, :, w.T_valid:, :] = 0.0

@@ -132,6 +132,26 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
                          void *workspace, int B, int T, int T_valid, int H, int d, int cp,
                          int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ------------------------------------------ grouped K/V heads (GQA/MQA) ---
+ * cpattn_fwd / cpattn_bwd with H query heads sharing H_kv K/V heads: query
+ * head h attends with K/V head h / (H / H_kv), the repeat-interleave grouping
+ * (Claude Logs, 2026-06-29: keep GQA-grouped K/V in the ring; 2026-07-01:
+ * GQA/MQA as a local broadcast of K/V heads whose backward is a group sum).
+ * The gradient of a K/V head is the sum of what its H / H_kv query heads give
+ * it. H_kv = H is cpattn_fwd / cpattn_bwd; H_kv = 1 is multi-query attention.
+ *   q, o, dO, dq : [B,H,T,d]    sharded, dtype dt
+ *   k, v, dk, dv : [B,H_kv,T,d] sharded, dtype dt
+ *   lse          : [B,H,T] fp32; workspace as for cpattn_bwd (B*H*T rows)
+ * H_kv must divide H, else CPATTN_ERR_SHAPE. Everything else (layouts,
+ * validation, ownership, asynchrony, errors) is as for cpattn_fwd/cpattn_bwd. */
+cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                             int rope, cpattn_dtype dt, cpattn_stream_t stream);
+cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                             void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                             int cp, int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
+
 /* --------------------------------------------- allocation-free backward ---
  * Not from the pages: an addition of this library for callers that cannot
  * allocate device memory when they call it -- for example a plugin inside a

@@ -44,7 +44,7 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     for _ in range(repeat):
         cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream)
     if with_bwd:
-        dq, dk, dv = (torch.empty_like(sh["q"]) for _ in range(3))
+        dq, dk, dv = torch.empty_like(sh["q"]), torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
         ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
                          device=dev)
         for _ in range(repeat):

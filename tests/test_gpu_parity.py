@@ -102,6 +102,11 @@ SMALL_F32 = [
                   qkv_std=1.0),
 ]
 
+SMALL_GQA_F32 = [
+    make_workload("f32_gqa_rope", B=1, T=256, T_valid=253, H=4, H_kv=2, d=64, cp=2, rope=True,
+                  dtype="f32", qkv_std=1.0),
+]
+
 SMALL_BF16 = [
     make_workload("two_tiles_rope", B=1, T=1024, H=2, d=128, cp=2, rope=True),
     make_workload("ragged_d64_pad", B=2, T=800, T_valid=797, H=1, d=64, cp=2, rope=False),
@@ -111,11 +116,16 @@ SMALL_BF16 = [
     make_workload("ragged_c300", B=1, T=1200, T_valid=1195, H=2, d=128, cp=2, rope=True),
     make_workload("noncausal_pad_d128", B=1, T=640, T_valid=600, H=1, d=128, cp=2, causal=False,
                   rope=False),
+    # grouped K/V heads: GQA with RoPE and padding, MQA, non-causal GQA, ragged chunks
+    make_workload("gqa4x2_rope_pad", B=1, T=1024, T_valid=1021, H=4, H_kv=2, d=128, cp=2, rope=True),
+    make_workload("mqa_d64_cp3", B=2, T=768, H=3, H_kv=1, d=64, cp=3, rope=False),
+    make_workload("gqa6x3_noncausal", B=1, T=512, H=6, H_kv=3, d=128, cp=2, causal=False, rope=True),
+    make_workload("gqa8x2_ragged", B=1, T=1200, T_valid=1195, H=8, H_kv=2, d=64, cp=2, rope=True),
 ]
 
 
 @pytest.mark.parametrize("mode", ROPE_MODES)
-@pytest.mark.parametrize("w", SMALL_F32, ids=lambda w: w.name)
+@pytest.mark.parametrize("w", SMALL_F32 + SMALL_GQA_F32, ids=lambda w: w.name)
 def test_fp32_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
@@ -193,7 +203,8 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
 
 @pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
                                        ("long_16k", "shard"), ("window_32k", "shard"),
-                                       ("window_32k", "kernel"), ("padded_12289", "shard")])
+                                       ("window_32k", "kernel"), ("padded_12289", "shard"),
+                                       ("gqa_32k", "shard")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])
@@ -201,7 +212,7 @@ def test_workload_full_size_sampled(name, mode):
     for g in ("o", "lse", "dq", "dk", "dv"):
         assert torch.isfinite(got[g][:, :, : w.T_valid]).all(), g
     heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
-    _sampled_check(w, inp, got, heads, kv_head=(w.B - 1, w.H // 3))
+    _sampled_check(w, inp, got, heads, kv_head=(w.B - 1, w.kv_heads // 3))
     if w.T_valid < w.T:
         for g in ("dq", "dk", "dv"):
             assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
@@ -255,13 +266,14 @@ def test_long_schedule_sampled_rows():
         assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
 
 
-def test_long_schedule_padded_against_unpadded_oracle():
+@pytest.mark.parametrize("H,H_kv", [(1, 1), (2, 1)])
+def test_long_schedule_padded_against_unpadded_oracle(H, H_kv):
     """Only the first 3000 tokens are real; the real rows must equal the oracle
     on those 3000 tokens alone, for every output and gradient."""
-    w = make_workload("long_schedule_pad", T_valid=3000, **LONG_SCHEDULE)
+    w = make_workload("long_schedule_pad", T_valid=3000, **{**LONG_SCHEDULE, "H": H}, H_kv=H_kv)
     inp = make_inputs(w, seed=78)
     got = run_gpu(w, inp)
-    wu = make_workload("unpadded", B=1, T=w.T_valid, H=1, d=w.d, cp=1, rope=False)
+    wu = make_workload("unpadded", B=1, T=w.T_valid, H=H, H_kv=H_kv, d=w.d, cp=1, rope=False)
     want = _oracle_full(wu, {k: t[:, :, : w.T_valid] for k, t in inp.items()})
     _check_full(wu, {k: t[:, :, : w.T_valid] for k, t in got.items()}, want)
     for g in ("dq", "dk", "dv"):

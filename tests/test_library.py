@@ -90,3 +90,22 @@ def test_bwd_and_merge_validation(lib):
     assert st == cpattn.ERR_ALIGN
     st = lib.cpattn_shard(P[0], P[0] + 16, 1, 1, 8, 64, 2, cpattn.BF16, None)
     assert st == cpattn.ERR_ARG                    # overlapping src and dst
+
+
+@pytest.mark.parametrize("H,H_kv,status", [(8, 3, cpattn.ERR_SHAPE), (4, 0, cpattn.ERR_SHAPE),
+                                           (2, 4, cpattn.ERR_SHAPE)])
+def test_gqa_head_counts_are_validated(lib, H, H_kv, status):
+    st = lib.cpattn_fwd_gqa(*P[:5], 1, 1024, 1024, H, H_kv, 128, 2, 1, 1, cpattn.BF16, None)
+    assert st == status and "H_kv" in cpattn.cpattn_last_error()
+    st = lib.cpattn_bwd_gqa(*P, 1, 1024, 1024, H, H_kv, 128, 2, 1, 1, cpattn.BF16, None)
+    assert st == status
+
+
+def test_gqa_overlap_uses_kv_sizes(lib):
+    # k is [1,1,1024,128] bf16 (256 KiB): a dk starting inside it is rejected
+    kv_bytes = 1024 * 128 * 2
+    base = 0x40000000
+    q, k, v, o, lse, do, dq, dv, ws = (base + i * 0x1000000 for i in range(9))
+    st = lib.cpattn_bwd_gqa(q, k, v, o, lse, do, dq, k + kv_bytes // 2, dv, ws, 1, 1024, 1024, 4, 1,
+                            128, 2, 1, 1, cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG
