@@ -16,6 +16,9 @@ What the pages fix, and where:
   are padded at the tail to a multiple of 2*cp before sharding; pad tokens
   must not change the loss.
 
+* "Claude Logs", 2026-07-09, and "HANDOFF_H200_32K": YaRN-extended RoPE
+  (``RopeSpec``).
+
 Readings taken where the pages are silent (each is listed in the design
 notes): softmax scale 1/sqrt(d); LSE is the natural log of the sum of
 exponentials of the *scaled* scores; RoPE is the rotate-half pairing
@@ -29,6 +32,7 @@ forward result depends on that row alone, so rows may be evaluated in groups
 """
 from __future__ import annotations
 
+import dataclasses
 import math
 
 import numpy as np
@@ -48,30 +52,82 @@ def as_f64(x) -> np.ndarray:
 
 # ---------------------------------------------------------------- RoPE ----
 
-def rope_angles(positions: np.ndarray, d: int) -> np.ndarray:
-    """angle[p, i] = pos_p * theta_i, theta_i = base^(-2i/d), i in [0, d/2)."""
-    i = np.arange(d // 2, dtype=np.float64)
-    theta = ROPE_BASE ** (-2.0 * i / d)
-    return np.asarray(positions, dtype=np.float64)[:, None] * theta[None, :]
+@dataclasses.dataclass(frozen=True)
+class RopeSpec:
+    """Which rotary embedding: the standard one, or YaRN context extension.
+
+    "Claude Logs", 2026-07-09 (YaRN in the RoPE cache: an NTK-by-parts blend of
+    the frequencies over a dimension-index ramp set by the correction
+    dimensions, and an attention temperature m = 0.1 ln(s) + 1 multiplied into
+    cos and sin, so logits scale by m^2; scale 1 gives the standard RoPE), and
+    "HANDOFF_H200_32K" (the 32k run: scale 2 over an original 16384 positions).
+    The method is YaRN (Peng et al., 2023, sections 3.2 and 3.4).
+    """
+    base: float = ROPE_BASE
+    factor: float = 1.0                  # s: context-extension factor
+    original_max_position: int = 0       # L: length the weights were trained at
+    beta_fast: float = 32.0              # rotations over L above which a pair keeps theta
+    beta_slow: float = 1.0               # rotations over L below which a pair gets theta / s
+    attention_factor: float = 0.0        # m; <= 0 selects 0.1 ln(s) + 1 (1 when s <= 1)
+
+    def theta(self, d: int) -> np.ndarray:
+        """Per-pair angular frequency theta_i, i in [0, d/2)."""
+        i = np.arange(d // 2, dtype=np.float64)
+        plain = self.base ** (-2.0 * i / d)
+        if self.factor <= 1.0:
+            return plain
+        # Pair index at which a frequency makes n rotations over L:
+        # L * base^(-2i/d) = 2 pi n  =>  i = d ln(L / (2 pi n)) / (2 ln base).
+        def pair_index(n):
+            return d * math.log(self.original_max_position / (2.0 * math.pi * n)) / (2.0 * math.log(self.base))
+        lo = max(math.floor(pair_index(self.beta_fast)), 0)
+        hi = min(math.ceil(pair_index(self.beta_slow)), d - 1)
+        if hi == lo:
+            hi += 0.001                  # keeps the ramp a step instead of 0/0
+        ramp = np.clip((i - lo) / (hi - lo), 0.0, 1.0)   # 0: keep theta, 1: theta / s
+        return plain * (1.0 - ramp) + (plain / self.factor) * ramp
+
+    def mscale(self) -> float:
+        if self.attention_factor > 0.0:
+            return self.attention_factor
+        return 0.1 * math.log(self.factor) + 1.0 if self.factor > 1.0 else 1.0
 
 
-def rope(x: np.ndarray, positions: np.ndarray) -> np.ndarray:
-    """Rotate-half RoPE of x[..., T, d] at the given per-row positions.
+STANDARD_ROPE = RopeSpec()
 
-    x'_i = x_i cos - x_{i+d/2} sin ;  x'_{i+d/2} = x_{i+d/2} cos + x_i sin.
+
+def _spec(rope_on) -> RopeSpec | None:
+    """rope_on may be False / True (standard RoPE) or a RopeSpec."""
+    if isinstance(rope_on, RopeSpec):
+        return rope_on
+    return STANDARD_ROPE if rope_on else None
+
+
+def rope_angles(positions: np.ndarray, d: int, spec: RopeSpec = STANDARD_ROPE) -> np.ndarray:
+    """angle[p, i] = pos_p * theta_i; standard theta_i = base^(-2i/d), i in [0, d/2)."""
+    return np.asarray(positions, dtype=np.float64)[:, None] * spec.theta(d)[None, :]
+
+
+def rope(x: np.ndarray, positions: np.ndarray, spec: RopeSpec = STANDARD_ROPE) -> np.ndarray:
+    """Rotate-half RoPE of x[..., T, d] at the given per-row positions, times m.
+
+    x'_i = m (x_i cos - x_{i+d/2} sin) ;  x'_{i+d/2} = m (x_{i+d/2} cos + x_i sin),
+    with m = 1 for the standard rotation.
     """
     d = x.shape[-1]
-    ang = rope_angles(positions, d)
-    c, s = np.cos(ang), np.sin(ang)
+    ang = rope_angles(positions, d, spec)
+    m = spec.mscale()
+    c, s = m * np.cos(ang), m * np.sin(ang)
     x1, x2 = x[..., : d // 2], x[..., d // 2:]
     return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
 
 
-def rope_transpose(g: np.ndarray, positions: np.ndarray) -> np.ndarray:
-    """R(p)^T g: the adjoint of ``rope``, which carries a gradient back through it."""
+def rope_transpose(g: np.ndarray, positions: np.ndarray, spec: RopeSpec = STANDARD_ROPE) -> np.ndarray:
+    """(m R(p))^T g: the adjoint of ``rope``, which carries a gradient back through it."""
     d = g.shape[-1]
-    ang = rope_angles(positions, d)
-    c, s = np.cos(ang), np.sin(ang)
+    ang = rope_angles(positions, d, spec)
+    m = spec.mscale()
+    c, s = m * np.cos(ang), m * np.sin(ang)
     g1, g2 = g[..., : d // 2], g[..., d // 2:]
     return np.concatenate([g1 * c + g2 * s, g2 * c - g1 * s], axis=-1)
 
@@ -128,13 +184,14 @@ def kv_head(h: int, H: int, H_kv: int) -> int:
     return h // (H // H_kv)
 
 
-def _rotated(xh: np.ndarray, rope_on: bool) -> np.ndarray:
-    if not rope_on:
+def _rotated(xh: np.ndarray, rope_on) -> np.ndarray:
+    spec = _spec(rope_on)
+    if spec is None:
         return xh
-    return rope(xh, np.arange(xh.shape[0]))
+    return rope(xh, np.arange(xh.shape[0]), spec)
 
 
-def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool = False):
+def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool | RopeSpec = False):
     """Single-pass attention over natural-order inputs: q [B, H, T, d], k and v
     [B, H_kv, T, d] (H_kv divides H; see ``kv_head``).
 
@@ -160,14 +217,14 @@ def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: b
 
 
 def forward_rows(q, k, v, b: int, h: int, rows, causal: bool = True,
-                 T_valid: int | None = None, rope_on: bool = False):
+                 T_valid: int | None = None, rope_on: bool | RopeSpec = False):
     """O and LSE of selected natural rows of one head (each row is independent)."""
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head(h, q.shape[1], k.shape[1])
     qh, kh, vh = as_f64(q[b, h]), as_f64(k[b, hk]), as_f64(v[b, hk])
     T = kh.shape[0]
     T_valid = T if T_valid is None else T_valid
-    qr = rope(qh[rows], rows) if rope_on else qh[rows]
+    qr = rope(qh[rows], rows, _spec(rope_on)) if rope_on else qh[rows]
     kr = _rotated(kh, rope_on)
     return partial_attention(qr, kr, vh, rows, np.arange(T), causal, T_valid)
 
@@ -189,12 +246,12 @@ def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
     dQr = dS @ kr / math.sqrt(d)
     dKr = dS.T @ qr / math.sqrt(d)
     if rope_on:
-        return rope_transpose(dQr, pos), rope_transpose(dKr, pos), dV
+        return rope_transpose(dQr, pos, _spec(rope_on)), rope_transpose(dKr, pos, _spec(rope_on)), dV
     return dQr, dKr, dV
 
 
 def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = None,
-             rope_on: bool = False):
+             rope_on: bool | RopeSpec = False):
     """dq, dk, dv of the loss sum(dO * O), through RoPE if it is on.
 
     o and lse are the single-pass forward results (float64). With P = exp(S - LSE):
@@ -217,7 +274,7 @@ def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = Non
 
 
 def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
-                     T_valid: int | None = None, rope_on: bool = False):
+                     T_valid: int | None = None, rope_on: bool | RopeSpec = False):
     """dq of selected natural rows of one head; each needs only its own row of P."""
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head(h, q.shape[1], k.shape[1])
@@ -225,7 +282,7 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
     T, d = kh.shape
     T_valid = T if T_valid is None else T_valid
     o_r, lse_r = forward_rows(q, k, v, b, h, rows, causal, T_valid, rope_on)
-    qr = rope(as_f64(q[b, h])[rows], rows) if rope_on else as_f64(q[b, h])[rows]
+    qr = rope(as_f64(q[b, h])[rows], rows, _spec(rope_on)) if rope_on else as_f64(q[b, h])[rows]
     kr = _rotated(kh, rope_on)
     ok = allowed(rows, np.arange(T), causal, T_valid)
     S = (qr @ kr.T) / math.sqrt(d)
@@ -233,11 +290,11 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
     dP = doh[rows] @ vh.T
     D = np.sum(doh[rows] * o_r, axis=1)
     dQr = (P * (dP - D[:, None])) @ kr / math.sqrt(d)
-    return rope_transpose(dQr, rows) if rope_on else dQr
+    return rope_transpose(dQr, rows, _spec(rope_on)) if rope_on else dQr
 
 
 def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
-                       T_valid: int | None = None, rope_on: bool = False):
+                       T_valid: int | None = None, rope_on: bool | RopeSpec = False):
     """dk, dv of selected natural key rows of K/V head h.
 
     For each query head that reads K/V head h (one head without grouping, see
@@ -270,7 +327,7 @@ def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
         dP = doh @ vh[cols].T
         dS = P * (dP - D[:, None])
         dK += dS.T @ qr / math.sqrt(d)
-    return (rope_transpose(dK, cols) if rope_on else dK), dV
+    return (rope_transpose(dK, cols, _spec(rope_on)) if rope_on else dK), dV
 
 
 # ---------------------------------------------------------- LSE merge ----
@@ -308,7 +365,7 @@ def merge_many(o_parts, l_parts):
 # ---------------------------------------------------------------- ring ----
 
 def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = None,
-                 rope_on: bool = False):
+                 rope_on: bool | RopeSpec = False):
     """The ring schedule, stated step by step; returns natural-order O and LSE.
 
     Virtual rank r holds HeadTail chunks r and 2cp-1-r. At ring step s it

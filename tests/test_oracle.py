@@ -456,3 +456,126 @@ def test_gqa_ring_equals_single_pass():
     O, L = A.forward(q, k, v, True, Tv, True)
     Or, Lr = A.ring_forward(q, k, v, 3, True, Tv, True)
     assert np.abs(O - Or).max() < 1e-12 and np.abs(L - Lr).max() < 1e-12
+
+
+# ------------------------------------------------------------- YaRN RoPE ----
+
+# The 32k extension run: scale 2 over the 16384 positions the weights saw.
+YARN_32K = A.RopeSpec(factor=2.0, original_max_position=16384)
+
+
+def test_yarn_scale_one_is_standard_rope():
+    x = rnd(2, 40, 64)
+    pos = np.arange(40) * 37
+    plain = A.rope(x, pos)
+    same = A.rope(x, pos, A.RopeSpec(factor=1.0, original_max_position=4096))
+    assert np.array_equal(plain, same)
+    assert A.RopeSpec(factor=1.0).mscale() == 1.0
+
+
+def test_yarn_frequencies_closed_form_for_the_32k_run():
+    # d = 128, base 1e4, L = 16384: a frequency makes n rotations over L at pair
+    # index 128 ln(L / (2 pi n)) / (2 ln 1e4) = 30.58 for n = 32 and 54.66 for
+    # n = 1, so the ramp runs from pair 30 (floor) to pair 55 (ceil).
+    th = YARN_32K.theta(128)
+    plain = 1e4 ** (-np.arange(64) / 64.0)
+    assert np.array_equal(th[:31], plain[:31])               # pairs 0..30 keep theta
+    assert np.allclose(th[55:], plain[55:] / 2, rtol=1e-15)  # pairs 55..63 get theta / 2
+    for i in (31, 40, 54):                                    # linear in between
+        w = (i - 30) / 25.0
+        assert abs(th[i] - plain[i] * (1 - w / 2)) <= 1e-15 * plain[i]
+    assert abs(YARN_32K.mscale() - (0.1 * math.log(2.0) + 1.0)) < 1e-15
+    assert abs(YARN_32K.mscale() - 1.0693147180559945) < 1e-15
+
+
+def test_yarn_keeps_fast_pairs_and_scales_slow_ones():
+    """Stated in rotations over L (YaRN section 3.2): pairs that turn many times
+    over the trained length keep their frequency, pairs that turn less than
+    once are interpolated by the factor."""
+    for d, L, s in [(128, 16384, 2.0), (64, 4096, 8.0), (128, 2048, 4.0)]:
+        spec = A.RopeSpec(factor=s, original_max_position=L)
+        plain = 1e4 ** (-np.arange(d // 2) * 2.0 / d)
+        rot = L * plain / (2 * math.pi)
+        step = 1e4 ** (2.0 / d)                              # ratio of adjacent frequencies
+        fast, slow = rot >= 32 * step, rot <= 1 / step
+        assert fast.any() and slow.any()
+        assert np.array_equal(spec.theta(d)[fast], plain[fast])
+        assert np.allclose(spec.theta(d)[slow], plain[slow] / s, rtol=1e-15)
+        assert np.all(np.diff(spec.theta(d)) < 0)            # still strictly decreasing
+
+
+def test_yarn_rotation_properties():
+    x, y = rnd(3, 50, 128), rnd(3, 50, 128)
+    pos = np.arange(50) * 601
+    m = YARN_32K.mscale()
+    r = A.rope(x, pos, YARN_32K)
+    # each (i, i + d/2) pair is rotated and scaled by m
+    n_in = np.hypot(x[..., :64], x[..., 64:])
+    n_out = np.hypot(r[..., :64], r[..., 64:])
+    assert np.allclose(n_out, m * n_in, rtol=1e-13)
+    # the adjoint used by the backward
+    assert abs(np.sum(r * y) - np.sum(x * A.rope_transpose(y, pos, YARN_32K))) < 1e-9
+    # scores depend on the position difference only, and carry m^2
+    q, k = rnd(1, 128), rnd(1, 128)
+    s1 = A.rope(q, np.array([20000]), YARN_32K) @ A.rope(k, np.array([19000]), YARN_32K).T
+    s2 = A.rope(q, np.array([1500]), YARN_32K) @ A.rope(k, np.array([500]), YARN_32K).T
+    assert abs(s1 - s2).max() < 1e-10
+    s0 = A.rope(q, np.array([0]), YARN_32K) @ A.rope(k, np.array([0]), YARN_32K).T
+    assert abs(s0 - m * m * (q @ k.T)).max() < 1e-12
+
+
+# small trained length so that the ramp is not trivial at d = 8: pairs 0..3 get
+# weights 0, 1/2, 1, 1 towards theta / 4
+YARN_TINY = A.RopeSpec(factor=4.0, original_max_position=64)
+
+
+def test_yarn_tiny_spec_has_a_ramp():
+    th = YARN_TINY.theta(8)
+    plain = 1e4 ** (-np.arange(4) / 4.0)
+    assert np.allclose(th, plain * (1 - np.array([0, 0.5, 1, 1]) * 0.75), rtol=1e-15)
+
+
+def test_yarn_backward_against_finite_differences():
+    T, d, h = 6, 8, 1e-6
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 2, T, d)
+
+    def loss(q_, k_, v_):
+        return np.sum(do * A.forward(q_, k_, v_, True, T, YARN_TINY)[0])
+
+    O, L = A.forward(q, k, v, True, T, YARN_TINY)
+    grads = A.backward(q, k, v, O, L, do, True, T, YARN_TINY)
+    worst = 0.0
+    for which, g in enumerate(grads):
+        fd = np.zeros_like(g)
+        for idx in np.ndindex(g.shape):
+            args_p, args_m = [q.copy(), k.copy(), v.copy()], [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        worst = max(worst, np.abs(g - fd).max() / max(np.abs(fd).max(), 1e-3))
+    assert worst <= 1e-6
+
+
+def test_planted_yarn_mistakes_are_caught():
+    # beta_fast and beta_slow swapped: the ramp collapses and the closed form fails
+    swapped = A.RopeSpec(factor=2.0, original_max_position=16384, beta_fast=1.0, beta_slow=32.0)
+    plain = 1e4 ** (-np.arange(64) / 64.0)
+    assert not np.allclose(swapped.theta(128)[55:], plain[55:] / 2)
+    # temperature applied once instead of to both q and k: scores lose a factor m
+    q, k = rnd(1, 128), rnd(1, 128)
+    one_sided = A.rope(q, np.array([0]), YARN_32K) @ k.T
+    assert abs(one_sided - YARN_32K.mscale() ** 2 * (q @ k.T)).max() > 1e-3
+
+
+def test_yarn_ring_and_sampled_rows_match_full():
+    T, d = 48, 16
+    spec = A.RopeSpec(factor=4.0, original_max_position=12)
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, True, T, spec)
+    Or, Lr = A.ring_forward(q, k, v, 4, True, T, spec)
+    assert np.abs(O - Or).max() < 1e-12 and np.abs(L - Lr).max() < 1e-12
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, T, spec)
+    rows = [0, 7, 31, 47]
+    assert np.abs(A.backward_dq_rows(q, k, v, do, 0, 1, rows, True, T, spec) - dq[0, 1, rows]).max() < 1e-12
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 0, 0, rows, True, T, spec)
+    assert np.abs(dk_c - dk[0, 0, rows]).max() < 1e-12 and np.abs(dv_c - dv[0, 0, rows]).max() < 1e-12
