@@ -84,6 +84,8 @@ def workload_config(w):
                  % (input_bytes(w) // 2 ** 20)}
     if w.kv_heads != w.H:
         cfg["H_kv"] = w.kv_heads
+    if w.yarn:
+        cfg["yarn"] = {"factor": w.yarn_factor, "original_max_position": w.yarn_original}
     return cfg
 
 
@@ -196,6 +198,8 @@ def oracle_sample(w, seconds_target=12.0, max_heads=8):
     from oracle import attention as A
 
     T_s = min(w.T_valid, 4096)
+    rope = (A.RopeSpec(factor=w.yarn_factor, original_max_position=w.yarn_original)
+            if w.yarn else w.rope)
     inp = _workload_inputs(w)
     q, k, v, do = (inp[n][0:1, :, :T_s].double().numpy() for n in ("q", "k", "v", "do"))
     heads, t0 = 0, time.perf_counter()
@@ -203,8 +207,8 @@ def oracle_sample(w, seconds_target=12.0, max_heads=8):
         sl = slice(heads, heads + 1)
         hk = heads // (w.H // w.kv_heads)     # the K/V head this query head reads
         kl = slice(hk, hk + 1)
-        O, L = A.forward(q[:, sl], k[:, kl], v[:, kl], w.causal, T_s, w.rope)
-        A.backward(q[:, sl], k[:, kl], v[:, kl], O, L, do[:, sl], w.causal, T_s, w.rope)
+        O, L = A.forward(q[:, sl], k[:, kl], v[:, kl], w.causal, T_s, rope)
+        A.backward(q[:, sl], k[:, kl], v[:, kl], O, L, do[:, sl], w.causal, T_s, rope)
         heads += 1
         if time.perf_counter() - t0 >= seconds_target:
             break
@@ -306,13 +310,17 @@ def run_ours(args):
     # and dq, dk (default), or applied inside the attention kernels.
     fused = w.rope and not args.rope_in_kernel
     rope_flag = w.rope and not fused
+    if w.yarn and not fused:
+        raise SystemExit("YaRN RoPE runs in the shard / unshard passes; drop --rope-in-kernel")
+    rope_cfg = (cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original)
+                if w.yarn else None)
 
     def step(evs=None):
         for i, name in enumerate(("q", "k", "v", "do")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
             if fused and name in ("q", "k"):
-                cpattn.shard_rope(nat[name], sh[name], w.cp, stream)
+                cpattn.shard_rope(nat[name], sh[name], w.cp, stream, cfg=rope_cfg)
             else:
                 cpattn.shard(nat[name], sh[name], w.cp, stream)
         if evs:
@@ -326,7 +334,7 @@ def run_ours(args):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
             if fused and name in ("dq", "dk"):
-                cpattn.unshard_rope(outs[name], outs_nat[name], w.cp, stream)
+                cpattn.unshard_rope(outs[name], outs_nat[name], w.cp, stream, cfg=rope_cfg)
             else:
                 cpattn.unshard(outs[name], outs_nat[name], w.cp, stream)
         if evs:

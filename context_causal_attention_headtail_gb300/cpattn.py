@@ -23,7 +23,7 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_shard_index", "cpattn_fwd",
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
            "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
-           "cpattn_fwd_gqa", "cpattn_bwd_gqa")
+           "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg")
 
 
 class CpattnError(RuntimeError):
@@ -37,6 +37,17 @@ _c = ctypes
 _vp, _i, _sz = _c.c_void_p, _c.c_int, _c.c_size_t
 
 
+class RopeCfg(ctypes.Structure):
+    """cpattn_rope_cfg: RoPE base and the YaRN extension (factor 1 = standard)."""
+    _fields_ = [("base", ctypes.c_double), ("factor", ctypes.c_double),
+                ("original_max_position", ctypes.c_int), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("attention_factor", ctypes.c_double)]
+
+    def __init__(self, factor=1.0, original_max_position=0, base=10000.0, beta_fast=32.0,
+                 beta_slow=1.0, attention_factor=0.0):
+        super().__init__(base, factor, original_max_position, beta_fast, beta_slow, attention_factor)
+
+
 def _declare(lib):
     sig = {
         "cpattn_shard": [_vp, _vp, _i, _i, _i, _i, _i, _i, _vp],
@@ -48,6 +59,8 @@ def _declare(lib):
         "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
         "cpattn_bwd_noalloc": [_vp] * 9 + [_i] * 9 + [_vp],
         "cpattn_fwd_gqa": [_vp] * 5 + [_i] * 10 + [_vp],
+        "cpattn_shard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
+        "cpattn_unshard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
         "cpattn_bwd_gqa": [_vp] * 10 + [_i] * 10 + [_vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
@@ -98,6 +111,16 @@ def cpattn_shard_rope(src, dst, B, H, T, d, cp, dt, stream=None):
 
 def cpattn_unshard_rope(src, dst, B, H, T, d, cp, dt, stream=None):
     _check(lib().cpattn_unshard_rope(src, dst, B, H, T, d, cp, dt, stream))
+
+
+def cpattn_shard_rope_cfg(src, dst, B, H, T, d, cp, dt, cfg, stream=None):
+    _check(lib().cpattn_shard_rope_cfg(src, dst, B, H, T, d, cp, dt,
+                                       None if cfg is None else ctypes.byref(cfg), stream))
+
+
+def cpattn_unshard_rope_cfg(src, dst, B, H, T, d, cp, dt, cfg, stream=None):
+    _check(lib().cpattn_unshard_rope_cfg(src, dst, B, H, T, d, cp, dt,
+                                         None if cfg is None else ctypes.byref(cfg), stream))
 
 
 def cpattn_shard_index(T, cp):
@@ -196,14 +219,24 @@ def unshard(src, dst, cp, stream=None):
     cpattn_unshard(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
 
 
-def shard_rope(src, dst, cp, stream=None):
+def shard_rope(src, dst, cp, stream=None, cfg: RopeCfg | None = None):
+    """dst = HeadTail shard of m R(p) src; cfg selects YaRN (None: standard RoPE)."""
     B, H, T, d = src.shape
-    cpattn_shard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+    if cfg is None:
+        cpattn_shard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+    else:
+        cpattn_shard_rope_cfg(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), cfg,
+                              _stream(stream))
 
 
-def unshard_rope(src, dst, cp, stream=None):
+def unshard_rope(src, dst, cp, stream=None, cfg: RopeCfg | None = None):
+    """dst = unshard of (m R(p))^T src, the adjoint of shard_rope with the same cfg."""
     B, H, T, d = src.shape
-    cpattn_unshard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+    if cfg is None:
+        cpattn_unshard_rope(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), _stream(stream))
+    else:
+        cpattn_unshard_rope_cfg(_ptr(src), _ptr(dst), B, H, T, d, cp, _dtype_code(src), cfg,
+                                _stream(stream))
 
 
 def _kv_heads(q, *kv):

@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
+#include <cmath>
 #include <mutex>
 
 #include "internal.h"
@@ -50,13 +52,55 @@ int *device_err_flag() {
   return addr[dev];
 }
 
-void make_rope_theta(int d, RopeTheta *t) {
+void make_rope_theta(int d, RopeTheta *t, const cpattn_rope_cfg *cfg) {
+  const double base = cfg ? cfg->base : 10000.0;
+  const double s = cfg ? cfg->factor : 1.0;
+  // YaRN (NTK-by-parts): pair i keeps theta_i while it turns more than
+  // beta_fast times over the trained length L, gets theta_i / s below
+  // beta_slow turns, and a linear blend in between, the ramp running over the
+  // pair index between the floor and the ceiling of the two crossing indices
+  // (a frequency turns n times over L at pair d ln(L / (2 pi n)) / (2 ln base)).
+  double ramp_lo = 0.0, ramp_hi = 1.0;
+  if (s > 1.0) {
+    auto pair_index = [&](double n) {
+      return d * log(cfg->original_max_position / (2.0 * M_PI * n)) / (2.0 * log(base));
+    };
+    ramp_lo = std::max(floor(pair_index(cfg->beta_fast)), 0.0);
+    ramp_hi = std::min(ceil(pair_index(cfg->beta_slow)), (double)(d - 1));
+    if (ramp_hi == ramp_lo) ramp_hi += 0.001;
+  }
   for (int i = 0; i < 64; ++i) {
-    double th = (2 * i < d) ? pow(10000.0, -2.0 * i / d) : 0.0;
+    double th = (2 * i < d) ? pow(base, -2.0 * i / d) : 0.0;
+    if (s > 1.0) {
+      const double w = std::min(std::max((i - ramp_lo) / (ramp_hi - ramp_lo), 0.0), 1.0);
+      th = th * (1.0 - w) + (th / s) * w;
+    }
     float hi = (float)th;
     t->hi[i] = hi;
     t->lo[i] = (float)(th - (double)hi);
   }
+  double m = 1.0;
+  if (cfg && cfg->attention_factor > 0.0) m = cfg->attention_factor;
+  else if (s > 1.0) m = 0.1 * log(s) + 1.0;
+  t->mscale = (float)m;
+}
+
+cpattn_status check_rope_cfg(const cpattn_rope_cfg *cfg) {
+  if (!cfg) return fail(CPATTN_ERR_ARG, "RoPE configuration is NULL");
+  if (!std::isfinite(cfg->base) || cfg->base <= 1.0)
+    return fail(CPATTN_ERR_ARG, "RoPE base %g must be finite and > 1", cfg->base);
+  if (!std::isfinite(cfg->factor) || cfg->factor < 1.0)
+    return fail(CPATTN_ERR_ARG, "YaRN factor %g must be finite and >= 1", cfg->factor);
+  if (!std::isfinite(cfg->attention_factor))
+    return fail(CPATTN_ERR_ARG, "attention_factor must be finite");
+  if (cfg->factor > 1.0) {
+    if (cfg->original_max_position < 1)
+      return fail(CPATTN_ERR_ARG, "original_max_position=%d must be >= 1", cfg->original_max_position);
+    if (!(cfg->beta_slow > 0.0) || !(cfg->beta_fast > cfg->beta_slow) || !std::isfinite(cfg->beta_fast))
+      return fail(CPATTN_ERR_ARG, "need 0 < beta_slow (%g) < beta_fast (%g)", cfg->beta_slow,
+                  cfg->beta_fast);
+  }
+  return CPATTN_OK;
 }
 
 EncodeTiledFn encode_tiled_fn() {
@@ -172,9 +216,10 @@ cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host) {
 
 static cpattn_status shard_common(const void *src, void *dst, int B, int H, int T, int d, int cp,
                                   cpattn_dtype dt, cpattn_stream_t stream, bool inverse,
-                                  bool rope = false) {
+                                  bool rope = false, const cpattn_rope_cfg *cfg = nullptr) {
   g_msg[0] = 0;
   if (!src || !dst) return fail(CPATTN_ERR_ARG, "null pointer");
+  if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
   cpattn_status st = check_common(B, H, T, d, cp);
   if (st != CPATTN_OK) return st;
   if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
@@ -188,7 +233,7 @@ static cpattn_status shard_common(const void *src, void *dst, int B, int H, int 
   Geometry g = geometry(B, H, T, T, d, cp, 1, rope ? 1 : 0);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   trace_record(0, s);
-  st = rope ? launch_shard_rope(src, dst, g, dt, inverse, s) : launch_shard(src, dst, g, elt, inverse, s);
+  st = rope ? launch_shard_rope(src, dst, g, dt, inverse, cfg, s) : launch_shard(src, dst, g, elt, inverse, s);
   trace_record(1, s);
   return st;
 }
@@ -211,6 +256,22 @@ cpattn_status cpattn_shard_rope(const void *src, void *dst, int B, int H, int T,
 cpattn_status cpattn_unshard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
                                   cpattn_dtype dt, cpattn_stream_t stream) {
   return shard_common(src, dst, B, H, T, d, cp, dt, stream, true, true);
+}
+
+cpattn_status cpattn_shard_rope_cfg(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                    cpattn_dtype dt, const cpattn_rope_cfg *cfg,
+                                    cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!cfg) return fail(CPATTN_ERR_ARG, "RoPE configuration is NULL");
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, false, true, cfg);
+}
+
+cpattn_status cpattn_unshard_rope_cfg(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                      cpattn_dtype dt, const cpattn_rope_cfg *cfg,
+                                      cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!cfg) return fail(CPATTN_ERR_ARG, "RoPE configuration is NULL");
+  return shard_common(src, dst, B, H, T, d, cp, dt, stream, true, true, cfg);
 }
 
 cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -21,14 +21,20 @@ int *device_err_flag();
 // Device error codes written to the flag.
 enum : int { ERR_FLAG_TIMEOUT = 1 };
 
-// RoPE frequencies theta_i = 10000^(-2i/d), i < d/2, split into two floats
-// (hi + lo carries ~48 bits) so that pos * theta can be formed without
-// double arithmetic on the device.
+// RoPE frequencies theta_i, i < d/2 (standard: 10000^(-2i/d); YaRN: the
+// NTK-by-parts blend of theta_i and theta_i / s), split into two floats
+// (hi + lo carries ~48 bits) so that pos * theta can be formed without double
+// arithmetic on the device, and the factor m that multiplies cos and sin (1
+// for the standard rotation).
 struct RopeTheta {
   float hi[64];
   float lo[64];
+  float mscale;
 };
-void make_rope_theta(int d, RopeTheta *t);
+// cfg = nullptr: the standard rotation, base 10000.
+void make_rope_theta(int d, RopeTheta *t, const cpattn_rope_cfg *cfg = nullptr);
+// Host validation of a RoPE configuration.
+cpattn_status check_rope_cfg(const cpattn_rope_cfg *cfg);
 
 // HeadTail geometry of one [B,H,T,d] problem.
 struct Geometry {
@@ -41,7 +47,7 @@ struct Geometry {
 cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
                            bool inverse, cudaStream_t s);
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
-                                bool inverse, cudaStream_t s);
+                                bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
 cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,
                              float *lse, const Geometry &g, cudaStream_t s);
 cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,

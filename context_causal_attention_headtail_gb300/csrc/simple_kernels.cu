@@ -74,8 +74,9 @@ cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int el
 // HeadTail shard fused with RoPE, and its adjoint fused with unshard, so that
 // the rotation runs inside a pass that already reads and writes every element
 // of q and k. Natural row t of chunk kappa has position p = kappa*c + o.
-//   forward  (shard):   dst[sigma(t)] = R(p) src[t]
-//   adjoint  (unshard): dst[t] = R(p)^T src[sigma(t)]
+//   forward  (shard):   dst[sigma(t)] = m R(p) src[t]
+//   adjoint  (unshard): dst[t] = m R(p)^T src[sigma(t)]
+// (m = 1 and the standard frequencies unless a YaRN configuration is given).
 // A lane owns VEC consecutive frequencies f0..f0+VEC-1 (one 16-byte word from
 // each half of the row) and walks up to 256/RS rows of one chunk with stride
 // RS; its cos/sin are seeded with rope_sincos and advanced by an exact
@@ -155,8 +156,8 @@ __global__ void __launch_bounds__(256) shard_rope_kernel(const T *__restrict__ s
         const float s_ = INVERSE ? -sn[v] : sn[v];
         const float xr = fmaf(x[v], cs[v], -y[v] * s_);
         const float yr = fmaf(y[v], cs[v], x[v] * s_);
-        x[v] = xr;
-        y[v] = yr;
+        x[v] = xr * th.mscale;   // m = 1 (exact) for the standard rotation
+        y[v] = yr * th.mscale;
         const float nc = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
         const float ns = fmaf(sn[v], cd[v], cs[v] * sd[v]);
         cs[v] = nc;
@@ -184,9 +185,9 @@ static void launch_shard_rope_t(const void *src, void *dst, const Geometry &g, b
 }
 
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
-                                bool inverse, cudaStream_t s) {
+                                bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
   RopeTheta th;
-  make_rope_theta(g.d, &th);
+  make_rope_theta(g.d, &th, cfg);
   if (dt == CPATTN_BF16) {
     if (g.d == 128) launch_shard_rope_t<__nv_bfloat16, 128>(src, dst, g, inverse, th, s);
     else launch_shard_rope_t<__nv_bfloat16, 64>(src, dst, g, inverse, th, s);

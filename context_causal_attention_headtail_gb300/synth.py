@@ -33,10 +33,16 @@ class Workload:
     dtype: str      # "f32" or "bf16": storage and input dtype of q, k, v, dO
     qkv_std: float
     H_kv: int = 0   # K/V heads (grouped-query attention); 0 means H
+    yarn_factor: float = 1.0   # YaRN context-extension factor of the RoPE (1: standard)
+    yarn_original: int = 0     # length the weights were trained at (YaRN only)
 
     @property
     def kv_heads(self) -> int:
         return self.H_kv or self.H
+
+    @property
+    def yarn(self) -> bool:
+        return self.rope and self.yarn_factor != 1.0
 
     @property
     def chunk(self) -> int:
@@ -60,7 +66,7 @@ class Workload:
         return 3.5 * self.fwd_flops()
 
 
-# The five workloads of the benchmark description, then the grouped-K/V one.
+# The five workloads of the benchmark description, then grouped K/V and YaRN.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", B=1, T=512, T_valid=512, H=4, d=64, cp=2,
                           causal=True, rope=False, dtype="f32", qkv_std=1.0),
@@ -75,6 +81,10 @@ WORKLOADS = {
     # Grouped K/V heads at 32k: 32 query heads over 8 K/V heads of d=128.
     "gqa_32k": Workload("gqa_32k", B=1, T=32768, T_valid=32768, H=32, d=128, cp=2,
                         causal=True, rope=True, dtype="bf16", qkv_std=0.5, H_kv=8),
+    # The 32k context extension: YaRN factor 2 over the 16384 positions trained at.
+    "yarn_32k": Workload("yarn_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
+                         causal=True, rope=True, dtype="bf16", qkv_std=0.5,
+                         yarn_factor=2.0, yarn_original=16384),
 }
 
 # Seeds: 1234 + the workload's position in the list above (1-based).
@@ -83,9 +93,11 @@ SEEDS = {name: 1234 + i + 1 for i, name in enumerate(WORKLOADS)}
 
 def make_workload(name: str = "custom", *, B: int, T: int, H: int, d: int, cp: int,
                   T_valid: int | None = None, causal: bool = True, rope: bool = False,
-                  dtype: str = "bf16", qkv_std: float = 0.5, H_kv: int = 0) -> Workload:
+                  dtype: str = "bf16", qkv_std: float = 0.5, H_kv: int = 0,
+                  yarn_factor: float = 1.0, yarn_original: int = 0) -> Workload:
     return Workload(name, B=B, T=T, T_valid=T if T_valid is None else T_valid, H=H, d=d,
-                    cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std, H_kv=H_kv)
+                    cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std, H_kv=H_kv,
+                    yarn_factor=yarn_factor, yarn_original=yarn_original)
 
 
 def make_inputs(w: Workload, seed: int) -> dict[str, torch.Tensor]:

@@ -96,6 +96,39 @@ cpattn_status cpattn_shard_rope(const void *src, void *dst, int B, int H, int T,
 cpattn_status cpattn_unshard_rope(const void *src, void *dst, int B, int H, int T, int d, int cp,
                                   cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ---------------------------------------------------- YaRN-scaled RoPE ---
+ * cpattn_shard_rope / cpattn_unshard_rope with a RoPE configuration: the
+ * YaRN context extension (Claude Logs, 2026-07-09: NTK-by-parts frequency
+ * blend over a dimension-index ramp, and an attention temperature multiplied
+ * into cos and sin; HANDOFF_H200_32K: the 32k run uses factor 2 over an
+ * original 16384 positions). With s = factor and L = original_max_position,
+ * pair i of d/2 has theta_i = base^(-2i/d); pair i turns L theta_i / (2 pi)
+ * times over L, and the pair index where that count equals n is
+ * x(n) = d ln(L / (2 pi n)) / (2 ln base). With lo = max(floor(x(beta_fast)), 0),
+ * hi = min(ceil(x(beta_slow)), d - 1) and w_i = clamp((i - lo) / (hi - lo), 0, 1),
+ * the rotation uses theta'_i = (1 - w_i) theta_i + w_i theta_i / s and
+ * multiplies cos and sin by m (attention_factor, or 0.1 ln(s) + 1 when that
+ * is <= 0; 1 when s = 1). The forward stores m R(p) x, the adjoint m R(p)^T g.
+ * factor = 1 with base 10000 is exactly cpattn_shard_rope / cpattn_unshard_rope.
+ * cfg is read during the call only (host memory, caller-owned). Invalid
+ * values (NULL, base <= 1, factor < 1, non-finite fields; for factor > 1
+ * original_max_position < 1 or not 0 < beta_slow < beta_fast) give
+ * CPATTN_ERR_ARG. Arguments and layouts otherwise as cpattn_shard_rope. */
+typedef struct cpattn_rope_cfg {
+  double base;                /* 10000 for the standard rotation */
+  double factor;              /* YaRN s >= 1; 1 = no extension */
+  int original_max_position;  /* L: the length the weights were trained at */
+  double beta_fast;           /* usually 32 */
+  double beta_slow;           /* usually 1 */
+  double attention_factor;    /* m; <= 0 selects 0.1 ln(s) + 1 */
+} cpattn_rope_cfg;
+cpattn_status cpattn_shard_rope_cfg(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                    cpattn_dtype dt, const cpattn_rope_cfg *cfg,
+                                    cpattn_stream_t stream);
+cpattn_status cpattn_unshard_rope_cfg(const void *src, void *dst, int B, int H, int T, int d, int cp,
+                                      cpattn_dtype dt, const cpattn_rope_cfg *cfg,
+                                      cpattn_stream_t stream);
+
 /* Host-only: idx_host[t] = sigma(t) for t in [0, T) (int32, caller-owned,
  * T entries). Launches nothing. */
 cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host);

@@ -22,20 +22,37 @@ TOL = {
 }
 
 
+def oracle_rope(w: Workload):
+    """The oracle's rope argument for a workload: False, True or a YaRN RopeSpec."""
+    from oracle import attention as A
+    if w.yarn:
+        return A.RopeSpec(factor=w.yarn_factor, original_max_position=w.yarn_original)
+    return w.rope
+
+
+def gpu_rope_cfg(w: Workload):
+    """The library's RoPE configuration for a workload (None: standard RoPE)."""
+    return cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original) if w.yarn else None
+
+
 def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
             rope_mode: str = "kernel") -> dict:
     """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd;
-    "shard" rotates q, k in cpattn_shard_rope, runs the attention with rope=0
-    and takes dq, dk back through cpattn_unshard_rope."""
+    "shard" rotates q, k in cpattn_shard_rope (cpattn_shard_rope_cfg for YaRN),
+    runs the attention with rope=0 and takes dq, dk back through
+    cpattn_unshard_rope. YaRN exists only on the "shard" path."""
     dev = torch.device(device)
     stream = torch.cuda.current_stream(dev)
     fused = w.rope and rope_mode == "shard"
     rope_flag = w.rope and not fused
+    if w.yarn and not fused:
+        raise ValueError("YaRN RoPE runs in the shard / unshard passes only")
+    cfg = gpu_rope_cfg(w)
     nat = {k: v.to(dev).contiguous() for k, v in inp.items()}
     sh = {k: torch.empty_like(v) for k, v in nat.items()}
     for k in nat:
         if fused and k in ("q", "k"):
-            cpattn.shard_rope(nat[k], sh[k], w.cp, stream)
+            cpattn.shard_rope(nat[k], sh[k], w.cp, stream, cfg=cfg)
         else:
             cpattn.shard(nat[k], sh[k], w.cp, stream)
     o = torch.empty_like(sh["q"])
@@ -53,7 +70,7 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
         for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
             nt = torch.empty_like(t)
             if fused and name in ("dq", "dk"):
-                cpattn.unshard_rope(t, nt, w.cp, stream)
+                cpattn.unshard_rope(t, nt, w.cp, stream, cfg=cfg)
             else:
                 cpattn.unshard(t, nt, w.cp, stream)
             out[name] = nt

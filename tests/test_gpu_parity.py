@@ -19,15 +19,15 @@ from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make
 from oracle import attention as A
 from oracle import headtail as HT
 
-from harness import TOL, compare, run_gpu, sample_rows
+from harness import TOL, compare, gpu_rope_cfg, oracle_rope, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 
 
 def _oracle_full(w, inp):
     q, k, v, do = (inp[n].double().numpy() for n in ("q", "k", "v", "do"))
-    O, L = A.forward(q, k, v, w.causal, w.T_valid, w.rope)
-    dq, dk, dv = A.backward(q, k, v, O, L, do, w.causal, w.T_valid, w.rope)
+    O, L = A.forward(q, k, v, w.causal, w.T_valid, oracle_rope(w))
+    dq, dk, dv = A.backward(q, k, v, O, L, do, w.causal, w.T_valid, oracle_rope(w))
     return {"o": O, "lse": L, "dq": dq, "dk": dk, "dv": dv}
 
 
@@ -85,6 +85,52 @@ def test_shard_rope_against_oracle(dtype, B, H, T, d, cp):
     assert worst <= 1.0, f"round trip: worst error/bound {worst:.3f}, max err {err.max():.3e}"
 
 
+@pytest.mark.parametrize("dtype,B,H,T,d,cp,factor,L", [
+    (torch.bfloat16, 1, 2, 32768, 128, 2, 2.0, 16384),     # the 32k extension run
+    (torch.float32, 1, 1, 12296, 64, 4, 8.0, 2048),
+    (torch.bfloat16, 2, 1, 1200, 128, 2, 4.0, 300),
+])
+def test_shard_rope_yarn_against_oracle(dtype, B, H, T, d, cp, factor, L):
+    x = (torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(T + 7)) * 0.5).to(dtype)
+    xs = x.cuda()
+    ys, zs = torch.empty_like(xs), torch.empty_like(xs)
+    cfg = cpattn.RopeCfg(factor=factor, original_max_position=L)
+    cpattn.shard_rope(xs, ys, cp, cfg=cfg)
+    cpattn.unshard_rope(ys, zs, cp, cfg=cfg)
+    torch.cuda.synchronize()
+    spec = A.RopeSpec(factor=factor, original_max_position=L)
+    m = spec.mscale()
+    xd = x.double().numpy()
+    want = HT.shard(A.rope(xd, np.arange(T), spec), cp)
+    # as for the standard rotation, with every magnitude scaled by m (m^2 after
+    # the round trip); m is itself rounded to fp32 (relative 2^-24)
+    u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -24
+    pair = np.sqrt(xd[..., : d // 2] ** 2 + xd[..., d // 2:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    err = np.abs(ys.double().cpu().numpy() - want)
+    bound = u * np.abs(want) + 5e-6 * m * HT.shard(pair, cp) + 1e-7
+    worst = float((err / bound).max())
+    assert worst <= 1.0, f"shard_rope yarn: worst error/bound {worst:.3f}, max err {err.max():.3e}"
+    back = zs.double().cpu().numpy()
+    err = np.abs(back - m * m * xd)
+    worst = float((err / (3 * u * m * m * pair + 1e-5 * m * m * pair + 1e-7)).max())
+    assert worst <= 1.0, f"round trip: worst error/bound {worst:.3f}, max err {err.max():.3e}"
+
+
+def test_shard_rope_cfg_factor_one_is_plain_rope():
+    x = (torch.randn(1, 2, 4096, 128, generator=torch.Generator().manual_seed(3)) * 0.5).to(torch.bfloat16).cuda()
+    a, b = torch.empty_like(x), torch.empty_like(x)
+    cpattn.shard_rope(x, a, 2)
+    cpattn.shard_rope(x, b, 2, cfg=cpattn.RopeCfg(factor=1.0))
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    cpattn.unshard_rope(a, b, 2)
+    c = torch.empty_like(x)
+    cpattn.unshard_rope(a, c, 2, cfg=cpattn.RopeCfg(factor=1.0))
+    torch.cuda.synchronize()
+    assert torch.equal(b, c)
+
+
 def test_shard_index_matches_oracle():
     for T, cp in [(8, 2), (24, 3), (32768, 2), (12296, 4)]:
         assert cpattn.cpattn_shard_index(T, cp) == HT.shard_index(T, cp).tolist()
@@ -105,6 +151,8 @@ SMALL_F32 = [
 SMALL_GQA_F32 = [
     make_workload("f32_gqa_rope", B=1, T=256, T_valid=253, H=4, H_kv=2, d=64, cp=2, rope=True,
                   dtype="f32", qkv_std=1.0),
+    make_workload("f32_yarn", B=1, T=384, T_valid=381, H=2, d=128, cp=3, rope=True, dtype="f32",
+                  qkv_std=1.0, yarn_factor=4.0, yarn_original=96),
 ]
 
 SMALL_BF16 = [
@@ -121,6 +169,11 @@ SMALL_BF16 = [
     make_workload("mqa_d64_cp3", B=2, T=768, H=3, H_kv=1, d=64, cp=3, rope=False),
     make_workload("gqa6x3_noncausal", B=1, T=512, H=6, H_kv=3, d=128, cp=2, causal=False, rope=True),
     make_workload("gqa8x2_ragged", B=1, T=1200, T_valid=1195, H=8, H_kv=2, d=64, cp=2, rope=True),
+    # YaRN RoPE (trained length a quarter / half of T, so the extension is used)
+    make_workload("yarn4_pad", B=1, T=1024, T_valid=1019, H=2, d=128, cp=2, rope=True,
+                  yarn_factor=4.0, yarn_original=256),
+    make_workload("yarn2_gqa_d64", B=2, T=768, H=4, H_kv=2, d=64, cp=3, rope=True,
+                  yarn_factor=2.0, yarn_original=384),
 ]
 
 
@@ -129,6 +182,8 @@ SMALL_BF16 = [
 def test_fp32_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
+    if mode == "kernel" and w.yarn:
+        pytest.skip("YaRN runs in the shard / unshard passes only")
     inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
     _check_full(w, run_gpu(w, inp, rope_mode=mode), _oracle_full(w, inp))
 
@@ -138,6 +193,8 @@ def test_fp32_path_full(w, mode):
 def test_bf16_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
+    if mode == "kernel" and w.yarn:
+        pytest.skip("YaRN runs in the shard / unshard passes only")
     inp = make_inputs(w, seed=7 + w.T + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     want = _oracle_full(w, inp)
@@ -190,13 +247,13 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
     rows = sample_rows(w, n_random, seed=w.T)
     real = rows[rows < w.T_valid]
     for (b, h) in heads:
-        o_r, l_r = A.forward_rows(q, k, v, b, h, rows, w.causal, w.T_valid, w.rope)
+        o_r, l_r = A.forward_rows(q, k, v, b, h, rows, w.causal, w.T_valid, oracle_rope(w))
         compare(f"o[{b},{h}]", got["o"][b, h, rows], o_r, tol["o"], tol["cos"])
         compare(f"lse[{b},{h}]", got["lse"][b, h, rows], l_r, tol["lse"])
-        dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, w.rope)
+        dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, oracle_rope(w))
         compare(f"dq[{b},{h}]", got["dq"][b, h, real], dq_r, tol["grad"], tol["cos"])
     b, h = kv_head
-    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, w.rope)
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, oracle_rope(w))
     compare(f"dk[{b},{h}]", got["dk"][b, h, rows], dk_c, tol["grad"], tol["cos"])
     compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
 
@@ -204,7 +261,7 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
 @pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
                                        ("long_16k", "shard"), ("window_32k", "shard"),
                                        ("window_32k", "kernel"), ("padded_12289", "shard"),
-                                       ("gqa_32k", "shard")])
+                                       ("gqa_32k", "shard"), ("yarn_32k", "shard")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])

@@ -109,3 +109,23 @@ def test_gqa_overlap_uses_kv_sizes(lib):
     st = lib.cpattn_bwd_gqa(q, k, v, o, lse, do, dq, k + kv_bytes // 2, dv, ws, 1, 1024, 1024, 4, 1,
                             128, 2, 1, 1, cpattn.BF16, None)
     assert st == cpattn.ERR_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(base=1.0), dict(factor=0.5), dict(factor=2.0),
+                                dict(factor=2.0, original_max_position=4096, beta_fast=1.0,
+                                     beta_slow=32.0),
+                                dict(factor=float("nan"))])
+def test_rope_cfg_is_validated(lib, kw):
+    args = dict(factor=1.0, original_max_position=0)
+    args.update(kw)
+    cfg = cpattn.RopeCfg(**args)
+    for fn in (lib.cpattn_shard_rope_cfg, lib.cpattn_unshard_rope_cfg):
+        st = fn(P[0], P[1], 1, 1, 1024, 128, 2, cpattn.BF16, ctypes.byref(cfg), None)
+        assert st == cpattn.ERR_ARG
+    assert lib.cpattn_shard_rope_cfg(P[0], P[1], 1, 1, 1024, 128, 2, cpattn.BF16, None, None) == cpattn.ERR_ARG
+
+
+def test_rope_cfg_layout_matches_header():
+    # double, double, int (+4 bytes padding), double, double, double
+    assert ctypes.sizeof(cpattn.RopeCfg) == 48
+    assert cpattn.RopeCfg.beta_fast.offset == 24 and cpattn.RopeCfg.attention_factor.offset == 40
