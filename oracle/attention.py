@@ -134,16 +134,35 @@ def rope_transpose(g: np.ndarray, positions: np.ndarray, spec: RopeSpec = STANDA
 
 # ------------------------------------------------------- masked softmax ----
 
-def allowed(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool, T_valid: int) -> np.ndarray:
-    """allowed[a, b] = (not causal or k_pos[b] <= q_pos[a]) and k_pos[b] < T_valid."""
+def document_of(positions: np.ndarray, docs) -> np.ndarray:
+    """Index of the packed document holding each natural position, -1 for none.
+
+    ``docs`` is cu_seqlens: 0 = docs[0] < docs[1] < ... < docs[n]; document i
+    holds positions [docs[i], docs[i+1]); positions >= docs[n] are padding and
+    belong to no document.
+    """
+    docs = np.asarray(docs, dtype=np.int64)
+    idx = np.searchsorted(docs, np.asarray(positions), side="right") - 1
+    return np.where(np.asarray(positions) < docs[-1], idx, -1)
+
+
+def allowed(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool, T_valid: int,
+            docs=None) -> np.ndarray:
+    """allowed[a, b] = (not causal or k_pos[b] <= q_pos[a]) and k_pos[b] < T_valid
+    and, for packed documents (``docs`` = cu_seqlens), both positions lie in the
+    same document ("fix(cp): ... #2931": packed THD batches; "Claude Logs",
+    2026-07-16 training on length-bucketed documents)."""
     ok = np.broadcast_to(k_pos[None, :] < T_valid, (len(q_pos), len(k_pos))).copy()
     if causal:
         ok &= k_pos[None, :] <= q_pos[:, None]
+    if docs is not None:
+        dq, dk = document_of(q_pos, docs), document_of(k_pos, docs)
+        ok &= (dq[:, None] == dk[None, :]) & (dq[:, None] >= 0)
     return ok
 
 
 def partial_attention(qr: np.ndarray, kr: np.ndarray, vr: np.ndarray, q_pos: np.ndarray,
-                      k_pos: np.ndarray, causal: bool, T_valid: int):
+                      k_pos: np.ndarray, causal: bool, T_valid: int, docs=None):
     """Softmax attention of query rows over a key set, with the global mask.
 
     qr, kr are already rotated (if RoPE is on). Returns (O, LSE); a row with no
@@ -151,7 +170,7 @@ def partial_attention(qr: np.ndarray, kr: np.ndarray, vr: np.ndarray, q_pos: np.
     """
     d = qr.shape[-1]
     S = (qr @ kr.T) / math.sqrt(d)
-    ok = allowed(q_pos, k_pos, causal, T_valid)
+    ok = allowed(q_pos, k_pos, causal, T_valid, docs)
     S = np.where(ok, S, -np.inf)
     m = S.max(axis=1, initial=-np.inf)
     has = np.isfinite(m)
@@ -191,7 +210,7 @@ def _rotated(xh: np.ndarray, rope_on) -> np.ndarray:
     return rope(xh, np.arange(xh.shape[0]), spec)
 
 
-def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool | RopeSpec = False):
+def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: bool | RopeSpec = False, docs=None):
     """Single-pass attention over natural-order inputs: q [B, H, T, d], k and v
     [B, H_kv, T, d] (H_kv divides H; see ``kv_head``).
 
@@ -212,12 +231,12 @@ def forward(q, k, v, causal: bool = True, T_valid: int | None = None, rope_on: b
             for r0 in range(0, T, _ROW_BLOCK):
                 rows = pos[r0:r0 + _ROW_BLOCK]
                 O[b, h, rows], L[b, h, rows] = partial_attention(
-                    qh[rows], kh, v[b, hk], rows, pos, causal, T_valid)
+                    qh[rows], kh, v[b, hk], rows, pos, causal, T_valid, docs)
     return O, L
 
 
 def forward_rows(q, k, v, b: int, h: int, rows, causal: bool = True,
-                 T_valid: int | None = None, rope_on: bool | RopeSpec = False):
+                 T_valid: int | None = None, rope_on: bool | RopeSpec = False, docs=None):
     """O and LSE of selected natural rows of one head (each row is independent)."""
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head(h, q.shape[1], k.shape[1])
@@ -226,18 +245,18 @@ def forward_rows(q, k, v, b: int, h: int, rows, causal: bool = True,
     T_valid = T if T_valid is None else T_valid
     qr = rope(qh[rows], rows, _spec(rope_on)) if rope_on else qh[rows]
     kr = _rotated(kh, rope_on)
-    return partial_attention(qr, kr, vh, rows, np.arange(T), causal, T_valid)
+    return partial_attention(qr, kr, vh, rows, np.arange(T), causal, T_valid, docs)
 
 
 # ------------------------------------------------------------ backward ----
 
-def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
+def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on, docs=None):
     """Gradient of sum(dO * O) for one head, all rows (T x T matrices)."""
     T, d = qh.shape
     pos = np.arange(T)
     qr, kr = _rotated(qh, rope_on), _rotated(kh, rope_on)
     S = (qr @ kr.T) / math.sqrt(d)
-    ok = allowed(pos, pos, causal, T_valid)
+    ok = allowed(pos, pos, causal, T_valid, docs)
     P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lseh[:, None]), 0.0)
     dV = P.T @ doh
     dP = doh @ vh.T
@@ -251,7 +270,7 @@ def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
 
 
 def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = None,
-             rope_on: bool | RopeSpec = False):
+             rope_on: bool | RopeSpec = False, docs=None):
     """dq, dk, dv of the loss sum(dO * O), through RoPE if it is on.
 
     o and lse are the single-pass forward results (float64). With P = exp(S - LSE):
@@ -267,24 +286,25 @@ def backward(q, k, v, o, lse, do, causal: bool = True, T_valid: int | None = Non
         for h in range(H):
             hk = kv_head(h, H, k.shape[1])
             dq[b, h], dk_h, dv_h = _backward_head(
-                q[b, h], k[b, hk], v[b, hk], o[b, h], lse[b, h], do[b, h], causal, T_valid, rope_on)
+                q[b, h], k[b, hk], v[b, hk], o[b, h], lse[b, h], do[b, h], causal, T_valid, rope_on,
+                docs)
             dk[b, hk] += dk_h           # a shared K/V head gathers its group's gradients
             dv[b, hk] += dv_h
     return dq, dk, dv
 
 
 def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
-                     T_valid: int | None = None, rope_on: bool | RopeSpec = False):
+                     T_valid: int | None = None, rope_on: bool | RopeSpec = False, docs=None):
     """dq of selected natural rows of one head; each needs only its own row of P."""
     rows = np.asarray(rows, dtype=np.int64)
     hk = kv_head(h, q.shape[1], k.shape[1])
     kh, vh, doh = as_f64(k[b, hk]), as_f64(v[b, hk]), as_f64(do[b, h])
     T, d = kh.shape
     T_valid = T if T_valid is None else T_valid
-    o_r, lse_r = forward_rows(q, k, v, b, h, rows, causal, T_valid, rope_on)
+    o_r, lse_r = forward_rows(q, k, v, b, h, rows, causal, T_valid, rope_on, docs)
     qr = rope(as_f64(q[b, h])[rows], rows, _spec(rope_on)) if rope_on else as_f64(q[b, h])[rows]
     kr = _rotated(kh, rope_on)
-    ok = allowed(rows, np.arange(T), causal, T_valid)
+    ok = allowed(rows, np.arange(T), causal, T_valid, docs)
     S = (qr @ kr.T) / math.sqrt(d)
     P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lse_r[:, None]), 0.0)
     dP = doh[rows] @ vh.T
@@ -294,7 +314,7 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
 
 
 def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
-                       T_valid: int | None = None, rope_on: bool | RopeSpec = False):
+                       T_valid: int | None = None, rope_on: bool | RopeSpec = False, docs=None):
     """dk, dv of selected natural key rows of K/V head h.
 
     For each query head that reads K/V head h (one head without grouping, see
@@ -318,9 +338,9 @@ def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
         L = np.zeros(T)
         for r0 in range(0, T, _ROW_BLOCK):
             rows = pos[r0:r0 + _ROW_BLOCK]
-            O[rows], L[rows] = partial_attention(qr[rows], kr, vh, rows, pos, causal, T_valid)
+            O[rows], L[rows] = partial_attention(qr[rows], kr, vh, rows, pos, causal, T_valid, docs)
         D = np.sum(doh * O, axis=1)
-        ok = allowed(pos, cols, causal, T_valid)            # [T, n_cols]
+        ok = allowed(pos, cols, causal, T_valid, docs)      # [T, n_cols]
         S = (qr @ kr[cols].T) / math.sqrt(d)
         P = np.where(ok, np.exp(np.where(ok, S, 0.0) - L[:, None]), 0.0)
         dV += P.T @ doh
@@ -365,7 +385,7 @@ def merge_many(o_parts, l_parts):
 # ---------------------------------------------------------------- ring ----
 
 def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = None,
-                 rope_on: bool | RopeSpec = False):
+                 rope_on: bool | RopeSpec = False, docs=None):
     """The ring schedule, stated step by step; returns natural-order O and LSE.
 
     Virtual rank r holds HeadTail chunks r and 2cp-1-r. At ring step s it
@@ -391,7 +411,7 @@ def ring_forward(q, k, v, cp: int, causal: bool = True, T_valid: int | None = No
                     j = (r - s) % cp
                     keys = headtail.rank_tokens(T, cp, j)
                     o_s, l_s = partial_attention(qh[rows], kh[keys], v[b, hk][keys], rows, keys,
-                                                 causal, T_valid)
+                                                 causal, T_valid, docs)
                     o_run, l_run = merge(o_run, l_run, o_s, l_s)
                 O[b, h, rows], L[b, h, rows] = o_run, l_run
     return O, L

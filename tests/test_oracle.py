@@ -174,8 +174,8 @@ def test_forward_against_brute_force():
 def test_planted_forward_mistakes_are_caught(monkeypatch):
     real_allowed = A.allowed
 
-    def strict_causal(q_pos, k_pos, causal, T_valid):   # j < t instead of j <= t
-        ok = real_allowed(q_pos, k_pos, causal, T_valid)
+    def strict_causal(q_pos, k_pos, causal, T_valid, docs=None):   # j < t instead of j <= t
+        ok = real_allowed(q_pos, k_pos, causal, T_valid, docs)
         if causal:
             ok &= k_pos[None, :] != q_pos[:, None]
         return ok
@@ -184,16 +184,16 @@ def test_planted_forward_mistakes_are_caught(monkeypatch):
         assert not check_forward(A.forward) < 1e-6
     monkeypatch.setattr(A, "allowed", real_allowed)
 
-    def no_pad_mask(q_pos, k_pos, causal, T_valid):
-        return real_allowed(q_pos, k_pos, causal, 10 ** 9)
+    def no_pad_mask(q_pos, k_pos, causal, T_valid, docs=None):
+        return real_allowed(q_pos, k_pos, causal, 10 ** 9, docs)
     monkeypatch.setattr(A, "allowed", no_pad_mask)
     assert not check_forward(A.forward) < 1e-6
     monkeypatch.setattr(A, "allowed", real_allowed)
 
     real_pa = A.partial_attention
 
-    def transposed_v(qr, kr, vr, q_pos, k_pos, causal, T_valid):
-        return real_pa(qr, kr, vr[::-1], q_pos, k_pos, causal, T_valid)
+    def transposed_v(qr, kr, vr, q_pos, k_pos, causal, T_valid, docs=None):
+        return real_pa(qr, kr, vr[::-1], q_pos, k_pos, causal, T_valid, docs)
     monkeypatch.setattr(A, "partial_attention", transposed_v)
     assert not check_forward(A.forward) < 1e-6
 
@@ -307,13 +307,13 @@ def test_backward_against_finite_differences(causal, T_valid, rope_on):
 def test_planted_backward_mistakes_are_caught(monkeypatch):
     real = A._backward_head
 
-    def no_D(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):   # drops the D term
-        return real(qh, kh, vh, np.zeros_like(oh), lseh, doh, causal, T_valid, rope_on)
+    def no_D(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on, docs=None):   # drops the D term
+        return real(qh, kh, vh, np.zeros_like(oh), lseh, doh, causal, T_valid, rope_on, docs)
     monkeypatch.setattr(A, "_backward_head", no_D)
     assert check_gradients_fd(A.backward, True, 6, False) > 1e-3
 
-    def no_rope_adjoint(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on):
-        dq, dk, dv = real(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on)
+    def no_rope_adjoint(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on, docs=None):
+        dq, dk, dv = real(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on, docs)
         pos = np.arange(qh.shape[0])
         return A.rope(A.rope(dq, pos), pos), dk, dv                     # R instead of R^T
     monkeypatch.setattr(A, "_backward_head", no_rope_adjoint)
@@ -578,4 +578,103 @@ def test_yarn_ring_and_sampled_rows_match_full():
     rows = [0, 7, 31, 47]
     assert np.abs(A.backward_dq_rows(q, k, v, do, 0, 1, rows, True, T, spec) - dq[0, 1, rows]).max() < 1e-12
     dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 0, 0, rows, True, T, spec)
+    assert np.abs(dk_c - dk[0, 0, rows]).max() < 1e-12 and np.abs(dv_c - dv[0, 0, rows]).max() < 1e-12
+
+
+# ------------------------------------------------ packed documents (varlen) ----
+
+# 64 positions: documents of 5, 1, 17, 17 and 21 tokens, then 3 pad positions.
+DOCS = np.array([0, 5, 6, 23, 40, 61])
+
+
+def test_document_of():
+    pos = np.arange(64)
+    want = [0] * 5 + [1] + [2] * 17 + [3] * 17 + [4] * 21 + [-1] * 3
+    assert A.document_of(pos, DOCS).tolist() == want
+
+
+def _varlen_vs_documents(causal, rope_on, H=4, H_kv=2):
+    """Max difference between packed attention and each document run alone,
+    with its positions restarting at 0 (RoPE scores depend on position
+    differences only, so the packed run may keep global positions)."""
+    T, d, Tv = 64, 8, int(DOCS[-1])
+    q, do = rnd(2, H, T, d), rnd(2, H, T, d)
+    k, v = rnd(2, H_kv, T, d), rnd(2, H_kv, T, d)
+    O, L = A.forward(q, k, v, causal, Tv, rope_on, docs=DOCS)
+    dq, dk, dv = A.backward(q, k, v, O, L, do, causal, Tv, rope_on, docs=DOCS)
+    err = 0.0
+    for a, b in zip(DOCS[:-1], DOCS[1:]):
+        sl = slice(a, b)
+        Od, Ld = A.forward(q[:, :, sl], k[:, :, sl], v[:, :, sl], causal, b - a, rope_on)
+        g = A.backward(q[:, :, sl], k[:, :, sl], v[:, :, sl], Od, Ld, do[:, :, sl], causal, b - a, rope_on)
+        err = max(err, np.abs(O[:, :, sl] - Od).max(), np.abs(L[:, :, sl] - Ld).max(),
+                  *(np.abs(x[:, :, sl] - y).max() for x, y in zip((dq, dk, dv), g)))
+    # pad rows attend nothing and receive nothing
+    assert np.all(O[:, :, Tv:] == 0) and np.all(L[:, :, Tv:] == -np.inf)
+    for x in (dq, dk, dv):
+        assert np.all(x[:, :, Tv:] == 0)
+    return err
+
+
+@pytest.mark.parametrize("causal,rope_on", [(True, False), (True, True), (False, True),
+                                            (True, A.RopeSpec(factor=4.0, original_max_position=8))])
+def test_varlen_equals_documents_run_alone(causal, rope_on):
+    assert _varlen_vs_documents(causal, rope_on) < 1e-12
+
+
+def test_planted_document_boundary_is_caught(monkeypatch):
+    real = A.document_of
+
+    def off_by_one(positions, docs):      # first token of each document put in the previous one
+        docs = np.asarray(docs)
+        idx = np.searchsorted(docs, np.asarray(positions), side="left") - 1
+        return np.where(np.asarray(positions) < docs[-1], np.maximum(idx, 0), -1)
+    monkeypatch.setattr(A, "document_of", off_by_one)
+    assert _varlen_vs_documents(True, False) > 1e-3
+    monkeypatch.setattr(A, "document_of", real)
+
+
+def test_single_document_is_plain_causal():
+    T, d = 40, 8
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, True, 37, True)
+    Od, Ld = A.forward(q, k, v, True, 37, True, docs=np.array([0, 37]))
+    assert np.array_equal(O[:, :, :37], Od[:, :, :37]) and np.array_equal(L[:, :, :37], Ld[:, :, :37])
+
+
+def test_varlen_backward_against_finite_differences():
+    T, d, h = 7, 4, 1e-6
+    docs = np.array([0, 3, 4, 7])
+    q, k, v, do = rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d)
+
+    def loss(q_, k_, v_):
+        return np.sum(do * A.forward(q_, k_, v_, True, T, True, docs=docs)[0])
+
+    O, L = A.forward(q, k, v, True, T, True, docs=docs)
+    grads = A.backward(q, k, v, O, L, do, True, T, True, docs=docs)
+    worst = 0.0
+    for which, g in enumerate(grads):
+        fd = np.zeros_like(g)
+        for idx in np.ndindex(g.shape):
+            args_p, args_m = [q.copy(), k.copy(), v.copy()], [q.copy(), k.copy(), v.copy()]
+            args_p[which][idx] += h
+            args_m[which][idx] -= h
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * h)
+        worst = max(worst, np.abs(g - fd).max() / max(np.abs(fd).max(), 1e-3))
+    assert worst <= 1e-6
+
+
+def test_varlen_ring_and_sampled_match_full():
+    T, d = 64, 8
+    q, k, v, do = rnd(1, 2, T, d), rnd(1, 1, T, d), rnd(1, 1, T, d), rnd(1, 2, T, d)
+    O, L = A.forward(q, k, v, True, 61, True, docs=DOCS)
+    Or, Lr = A.ring_forward(q, k, v, 4, True, 61, True, docs=DOCS)
+    assert np.abs(O - Or).max() < 1e-12 and np.array_equal(np.isinf(L), np.isinf(Lr))
+    fin = np.isfinite(L)
+    assert np.abs(L[fin] - Lr[fin]).max() < 1e-12
+    dq, dk, dv = A.backward(q, k, v, O, L, do, True, 61, True, docs=DOCS)
+    rows = [0, 4, 5, 6, 22, 23, 60, 62]
+    assert np.abs(A.backward_dq_rows(q, k, v, do, 0, 1, rows, True, 61, True, docs=DOCS)
+                  - dq[0, 1, rows]).max() < 1e-12
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 0, 0, rows, True, 61, True, docs=DOCS)
     assert np.abs(dk_c - dk[0, 0, rows]).max() < 1e-12 and np.abs(dv_c - dv[0, 0, rows]).max() < 1e-12
