@@ -29,6 +29,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -86,6 +88,10 @@ def workload_config(w):
         cfg["H_kv"] = w.kv_heads
     if w.yarn:
         cfg["yarn"] = {"factor": w.yarn_factor, "original_max_position": w.yarn_original}
+    if w.packed:
+        cu = w.cu_seqlens()
+        cfg["documents"] = {"n": len(cu) - 1, "length_range": list(w.doc_len),
+                            "lengths": [int(x) for x in np.diff(cu)]}
     return cfg
 
 
@@ -193,13 +199,20 @@ def oracle_sample(w, seconds_target=12.0, max_heads=8):
     first T_s tokens of the workload's own inputs. For causal attention the
     first T_s output rows of a head are exactly that prefix's attention, so
     this is a slice of the same problem; its algorithmic work is
-    7 * T_s^2 * d flops per head (3.5 x the causal forward 2 * T_s^2 * d).
+    7 * T_s^2 * d flops per head (3.5 x the causal forward 2 * T_s^2 * d), or
+    the same count over the prefix's documents for packed workloads.
     """
     from oracle import attention as A
 
     T_s = min(w.T_valid, 4096)
     rope = (A.RopeSpec(factor=w.yarn_factor, original_max_position=w.yarn_original)
             if w.yarn else w.rope)
+    docs, pairs = None, T_s * T_s * (0.5 if w.causal else 1.0)
+    if w.packed:          # the documents of the prefix, the last one cut at T_s
+        cu = w.cu_seqlens()
+        docs = np.append(cu[cu < T_s], T_s)
+        lens = np.diff(docs).astype(np.float64)
+        pairs = float(np.sum(lens * lens)) * (0.5 if w.causal else 1.0)
     inp = _workload_inputs(w)
     q, k, v, do = (inp[n][0:1, :, :T_s].double().numpy() for n in ("q", "k", "v", "do"))
     heads, t0 = 0, time.perf_counter()
@@ -207,13 +220,13 @@ def oracle_sample(w, seconds_target=12.0, max_heads=8):
         sl = slice(heads, heads + 1)
         hk = heads // (w.H // w.kv_heads)     # the K/V head this query head reads
         kl = slice(hk, hk + 1)
-        O, L = A.forward(q[:, sl], k[:, kl], v[:, kl], w.causal, T_s, rope)
-        A.backward(q[:, sl], k[:, kl], v[:, kl], O, L, do[:, sl], w.causal, T_s, rope)
+        O, L = A.forward(q[:, sl], k[:, kl], v[:, kl], w.causal, T_s, rope, docs=docs)
+        A.backward(q[:, sl], k[:, kl], v[:, kl], O, L, do[:, sl], w.causal, T_s, rope, docs=docs)
         heads += 1
         if time.perf_counter() - t0 >= seconds_target:
             break
     dt = time.perf_counter() - t0
-    flops = heads * 7.0 * T_s * T_s * w.d * (0.5 if w.causal else 1.0) * 2.0
+    flops = heads * 3.5 * 4.0 * pairs * w.d          # 3.5 x the forward's 4 d flops per live pair
     return {"seconds": dt, "flops": flops, "tokens": heads * T_s, "T_s": T_s, "heads": heads,
             "cores": os.cpu_count(),
             "blas_threads": os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
@@ -293,7 +306,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     kernels = ["shard", "fwd", "bwd_D", "bwd_dkdv", "bwd_dq", "unshard"]
-    launches_per_step = 4 + 1 + 3 + 4
+    launches_per_step = 4 + 1 + 3 + 4 + (1 if w.packed else 0)
 
     def new_events():
         evs = {"shard": [], "unshard": []}
@@ -314,6 +327,11 @@ def run_ours(args):
         raise SystemExit("YaRN RoPE runs in the shard / unshard passes; drop --rope-in-kernel")
     rope_cfg = (cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original)
                 if w.yarn else None)
+    docs = cu_dev = cu_host = None
+    if w.packed:          # cu_seqlens -> per-position document bounds, every step
+        cu_host = torch.from_numpy(w.cu_seqlens()).pin_memory()
+        cu_dev = cu_host.to(dev)
+        docs = (torch.empty(w.T, dtype=torch.int32, device=dev), torch.empty(w.T, dtype=torch.int32, device=dev))
 
     def step(evs=None):
         for i, name in enumerate(("q", "k", "v", "do")):
@@ -323,13 +341,16 @@ def run_ours(args):
                 cpattn.shard_rope(nat[name], sh[name], w.cp, stream, cfg=rope_cfg)
             else:
                 cpattn.shard(nat[name], sh[name], w.cp, stream)
+        if docs is not None:
+            cpattn.doc_bounds(cu_dev, w.T, docs[0], docs[1], stream)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["fwd"]])
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream)
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
+                   docs=docs)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["bwd"]])
         cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
-                   w.causal, rope_flag, stream)
+                   w.causal, rope_flag, stream, docs=docs)
         for i, name in enumerate(("o", "dq", "dk", "dv")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
@@ -393,6 +414,8 @@ def run_ours(args):
         for _ in range(args.steps):
             for k_ in nat:
                 nat[k_].copy_(host_in[k_], non_blocking=True)
+            if cu_dev is not None:
+                cu_dev.copy_(cu_host, non_blocking=True)
             step()
             for k_ in outs_nat:
                 host_out[k_].copy_(outs_nat[k_], non_blocking=True)
@@ -402,6 +425,8 @@ def run_ours(args):
         barrier()
         e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        if cu_host is not None:
+            h2d += cu_host.numel() * 4
         d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
         e2e = {"value": weak_scaling_value(world, w.fwdbwd_flops(), e2e_ms), "unit": UNIT,
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -23,7 +23,8 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_shard_index", "cpattn_fwd",
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
            "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
-           "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg")
+           "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
+           "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen")
 
 
 class CpattnError(RuntimeError):
@@ -59,6 +60,9 @@ def _declare(lib):
         "cpattn_bwd": [_vp] * 10 + [_i] * 9 + [_vp],
         "cpattn_bwd_noalloc": [_vp] * 9 + [_i] * 9 + [_vp],
         "cpattn_fwd_gqa": [_vp] * 5 + [_i] * 10 + [_vp],
+        "cpattn_doc_bounds": [_vp, _i, _i, _vp, _vp, _vp],
+        "cpattn_fwd_varlen": [_vp] * 5 + [_i] * 8 + [_vp, _vp, _i, _vp],
+        "cpattn_bwd_varlen": [_vp] * 10 + [_i] * 8 + [_vp, _vp, _i, _vp],
         "cpattn_shard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
         "cpattn_unshard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
         "cpattn_bwd_gqa": [_vp] * 10 + [_i] * 10 + [_vp],
@@ -138,6 +142,16 @@ def cpattn_fwd_gqa(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, rope,
                                 stream))
 
 
+def cpattn_fwd_varlen(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, doc_lo, doc_hi, dt,
+                      stream=None):
+    _check(lib().cpattn_fwd_varlen(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, doc_lo,
+                                   doc_hi, dt, stream))
+
+
+def cpattn_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, stream=None):
+    _check(lib().cpattn_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, stream))
+
+
 def cpattn_bwd_workspace_bytes(B, T, H, d):
     return int(lib().cpattn_bwd_workspace_bytes(B, T, H, d))
 
@@ -152,6 +166,12 @@ def cpattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H,
                    rope, dt, stream=None):
     _check(lib().cpattn_bwd_gqa(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d,
                                 cp, causal, rope, dt, stream))
+
+
+def cpattn_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp,
+                      causal, doc_lo, doc_hi, dt, stream=None):
+    _check(lib().cpattn_bwd_varlen(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv,
+                                   d, cp, causal, doc_lo, doc_hi, dt, stream))
 
 
 def cpattn_bwd_noalloc(q, k, v, o, lse, dO, dq, dk, dv, B, T, T_valid, H, d, cp, causal, rope, dt,
@@ -250,11 +270,32 @@ def _kv_heads(q, *kv):
     return H_kv
 
 
-def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None):
-    """o, lse = attention(q, k, v); k, v may have fewer heads than q (grouped K/V)."""
+def doc_bounds(cu_seqlens, T, doc_lo, doc_hi, stream=None):
+    """doc_lo, doc_hi [T] int32 (device) from cu_seqlens [n_docs + 1] int32 (device)."""
+    for t in (cu_seqlens, doc_lo, doc_hi):
+        if t.dtype != _torch().int32:
+            raise CpattnError(ERR_DTYPE, "cu_seqlens, doc_lo and doc_hi must be int32")
+    cpattn_doc_bounds(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, _ptr(doc_lo), _ptr(doc_hi),
+                      _stream(stream))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None, docs=None):
+    """o, lse = attention(q, k, v); k, v may have fewer heads than q (grouped K/V);
+    docs = (doc_lo, doc_hi) from doc_bounds restricts attention to documents."""
     B, H, T, d = q.shape
     H_kv = _kv_heads(q, k, v)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, T if T_valid is None else T_valid)
+    if docs is not None:
+        if rope:
+            raise CpattnError(ERR_ARG, "packed documents take RoPE from shard_rope (rope=False)")
+        cpattn_fwd_varlen(*args, H, H_kv, d, cp, int(causal), _ptr(docs[0]), _ptr(docs[1]),
+                          _dtype_code(q), _stream(stream))
+        return
     tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
     if H_kv == H:
         cpattn_fwd(*args, H, *tail)
@@ -263,12 +304,19 @@ def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None)
 
 
 def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=True, rope=False,
-        stream=None):
-    """dq, dk, dv of sum(dO * o); k, v, dk, dv may have fewer heads than q."""
+        stream=None, docs=None):
+    """dq, dk, dv of sum(dO * o); k, v, dk, dv may have fewer heads than q;
+    docs as for fwd."""
     B, H, T, d = q.shape
     H_kv = _kv_heads(q, k, v, dk, dv)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
             _ptr(workspace), B, T, T if T_valid is None else T_valid)
+    if docs is not None:
+        if rope:
+            raise CpattnError(ERR_ARG, "packed documents take RoPE from shard_rope (rope=False)")
+        cpattn_bwd_varlen(*args, H, H_kv, d, cp, int(causal), _ptr(docs[0]), _ptr(docs[1]),
+                          _dtype_code(q), _stream(stream))
+        return
     tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
     if H_kv == H:
         cpattn_bwd(*args, H, *tail)

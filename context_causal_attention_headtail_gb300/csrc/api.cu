@@ -196,6 +196,8 @@ cpattn_status cpattn_sync_status(cpattn_stream_t stream) {
     cudaMemcpy(flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (v & ERR_FLAG_TIMEOUT)
       return fail(CPATTN_ERR_TIMEOUT, "a kernel's bounded wait expired (flag=%d)", v);
+    if (v & ERR_FLAG_BAD_DOCS)
+      return fail(CPATTN_ERR_ARG, "cu_seqlens is not a document list (0 = cu[0] <= ... <= cu[n] <= T)");
     return fail(CPATTN_ERR_CUDA, "device error flag=%d", v);
   }
   return CPATTN_OK;
@@ -280,9 +282,31 @@ cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, f
   return cpattn_fwd_gqa(q, k, v, o, lse, B, T, T_valid, H, H, d, cp, causal, rope, dt, stream);
 }
 
+static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                              int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
+                              cpattn_stream_t stream);
+
 cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
                              int rope, cpattn_dtype dt, cpattn_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, rope, nullptr, nullptr, dt,
+                  stream);
+}
+
+cpattn_status cpattn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                                const int32_t *doc_lo, const int32_t *doc_hi, cpattn_dtype dt,
+                                cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!doc_lo || !doc_hi) return fail(CPATTN_ERR_ARG, "document bounds are NULL");
+  return fwd_impl(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, 0, doc_lo, doc_hi, dt, stream);
+}
+
+static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                              int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
+                              cpattn_stream_t stream) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
@@ -297,6 +321,8 @@ cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *
       overlaps(lse, (size_t)B * H * T * 4, o, tb))
     return fail(CPATTN_ERR_ARG, "outputs overlap inputs");
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
+  g.doc_lo = doc_lo;
+  g.doc_hi = doc_hi;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   trace_record(0, s);
   if (dt == CPATTN_F32)
@@ -323,10 +349,50 @@ cpattn_status cpattn_bwd(const void *q, const void *k, const void *v, const void
                         causal, rope, dt, stream);
 }
 
+static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                              void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                              int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
+                              cpattn_dtype dt, cpattn_stream_t stream);
+
 cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
                              void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                              int cp, int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream) {
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal,
+                  rope, nullptr, nullptr, dt, stream);
+}
+
+cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                                const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                                int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
+                                cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!doc_lo || !doc_hi) return fail(CPATTN_ERR_ARG, "document bounds are NULL");
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal, 0,
+                  doc_lo, doc_hi, dt, stream);
+}
+
+cpattn_status cpattn_doc_bounds(const int32_t *cu_seqlens, int n_docs, int T, int32_t *doc_lo,
+                                int32_t *doc_hi, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!cu_seqlens || !doc_lo || !doc_hi) return fail(CPATTN_ERR_ARG, "null pointer");
+  if (n_docs < 1 || T < 1) return fail(CPATTN_ERR_SHAPE, "n_docs=%d and T=%d must be >= 1", n_docs, T);
+  if (!aligned16(doc_lo) || !aligned16(doc_hi) || (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u))
+    return fail(CPATTN_ERR_ALIGN, "doc_lo, doc_hi must be 16-byte aligned, cu_seqlens 4-byte aligned");
+  const size_t tb = (size_t)T * 4;
+  if (overlaps(doc_lo, tb, doc_hi, tb) || overlaps(cu_seqlens, (size_t)(n_docs + 1) * 4, doc_lo, tb) ||
+      overlaps(cu_seqlens, (size_t)(n_docs + 1) * 4, doc_hi, tb))
+    return fail(CPATTN_ERR_ARG, "cu_seqlens, doc_lo and doc_hi must not overlap");
+  return launch_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, reinterpret_cast<cudaStream_t>(stream));
+}
+
+static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
+                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                              void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                              int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
+                              cpattn_dtype dt, cpattn_stream_t stream) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(CPATTN_ERR_ARG, "null pointer");
@@ -354,6 +420,8 @@ cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const 
     if (overlaps(outs[i], out_b[i], workspace, wb)) return fail(CPATTN_ERR_ARG, "workspace overlaps outputs");
   }
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
+  g.doc_lo = doc_lo;
+  g.doc_hi = doc_hi;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
   trace_record(0, s);

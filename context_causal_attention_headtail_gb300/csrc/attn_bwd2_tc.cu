@@ -27,6 +27,7 @@ struct Bwd2Params {
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
   int group;   // query heads per K/V head
+  const int *doc_lo, *doc_hi;   // packed documents: [T] bounds per natural position, or nullptr
   float scale, scale_log2;
 };
 
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(320, 1)
     tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
     tc::tmem_relinquish();
     {
-      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, lane);
+      const KvBounds kb = kv_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, q_pos0, q_pos0 + q_rows - 1);
+      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, kb, lane);
       if (lane == 0) *ntiles_slot = nt;
     }
   }
@@ -233,6 +235,8 @@ __global__ void __launch_bounds__(320, 1)
       tc::mbar_arrive(bar_qdo);
     }
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this row's document [dlo, dhi)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(q_pos, p.T - 1), p.T, dlo, dhi);
     int n = 0;
     bool ok = true;
     while (n < ntiles && (decode_tile(tab[n], t), true)) {
@@ -247,12 +251,15 @@ __global__ void __launch_bounds__(320, 1)
         tc::tmem_ld_wait();
         tc::tc_fence_before();
         tc::mbar_arrive(bar_s_free);                 // S may now be overwritten by S(n+1)
-        int lim = kTile;
+        // keep key columns lo <= j < lim (see the forward kernel)
+        int lim = kTile, lo = 0;
         if (t.need_mask) {
-          lim = min(t.nvalid, p.T_valid - t.pos0);
+          lim = min(min(t.nvalid, p.T_valid - t.pos0), dhi - t.pos0);
           if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
+          lo = dlo - t.pos0;
         }
         lim -= 64 * h;
+        lo -= 64 * h;
         const uint64_t sl2x2 = tc::f2(sl2, sl2), nl2 = tc::f2(-lse2, -lse2);
 #pragma unroll
         for (int j = 0; j < 64; j += 2) {
@@ -262,10 +269,11 @@ __global__ void __launch_bounds__(320, 1)
           pr[j] = tc::ex2(x0);
           pr[j + 1] = tc::ex2(x1);
         }
-        if (__any_sync(0xffffffffu, lim < 64)) {
+        if (__any_sync(0xffffffffu, lim < 64 || lo > 0)) {
+          const unsigned width = (unsigned)max(lim - lo, 0);
 #pragma unroll
           for (int j = 0; j < 64; ++j)
-            if (j >= lim) pr[j] = 0.f;
+            if ((unsigned)(j - lo) >= width) pr[j] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_full, n & 1, wc));
@@ -302,6 +310,10 @@ __global__ void __launch_bounds__(320, 1)
         tc::tc_fence_after();
         store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
       }
+    } else if (ok && valid) {   // no key tile at all (rows outside every document)
+      uint4 *d4 = reinterpret_cast<uint4 *>(p.dq + grow * D + h * (D / 2));
+#pragma unroll 1
+      for (int v = 0; v < D / 16; ++v) d4[v] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
 
@@ -393,7 +405,8 @@ __global__ void __launch_bounds__(320, 1)
     tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
     tc::tmem_relinquish();
     {
-      const int nt = build_q_table(tab, cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1, k_rows < kTile, lane);
+      const QBounds qb = q_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, k_pos0, k_pos0 + k_rows - 1);
+      const int nt = build_q_table(tab, cp, c, rk, p.causal, p.T_valid, qb, k_rows < kTile, lane);
       if (lane == 0) *ntiles_slot = nt;
     }
   }
@@ -529,6 +542,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const long long grow = (long long)bkv * p.T + (long long)(2 * c * rk + hk * c + kt * kTile + row);
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this key row's document [dlo, dhi)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(k_pos, p.T - 1), p.T, dlo, dhi);
     int n = 0, ent = 0;
     bool ok = true;
     while (n < ntot) {
@@ -538,14 +553,20 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc::tc_fence_after();
       const uint32_t sl = tc::smem_u32(ld_lse(st)) + 4u * (64 * h), sd = tc::smem_u32(ld_D(st)) + 4u * (64 * h);
-      // Queries kept: column q with q >= lo (causal) and none for padding keys;
-      // ragged query columns carry LSE = +inf, so their P is 0 already.
-      int lo = 0;
+      // Queries kept: columns lo <= q < hi: q >= k (causal), dlo <= pos0 + q <
+      // dhi (packed documents), none for padding keys; ragged query columns
+      // carry LSE = +inf, so their P is 0 already.
+      int lo = 0, hi = kTile;
       if (t.need_mask) {
-        if (k_pos >= p.T_valid) lo = kTile;
-        else if (p.causal) lo = max(0, k_pos - t.pos0);
+        if (k_pos >= p.T_valid) {
+          lo = kTile;
+        } else {
+          lo = max(p.causal ? k_pos - t.pos0 : 0, dlo - t.pos0);
+          hi = dhi - t.pos0;
+        }
       }
       lo -= 64 * h;
+      hi -= 64 * h;
       float pr[64];
       {
         uint32_t r[2][32];
@@ -569,10 +590,11 @@ __global__ void __launch_bounds__(320, 1)
           pr[q + 2] = tc::ex2(x2);
           pr[q + 3] = tc::ex2(x3);
         }
-        if (__any_sync(0xffffffffu, lo > 0)) {
+        if (__any_sync(0xffffffffu, lo > 0 || hi < 64)) {
+          const unsigned width = (unsigned)max(hi - lo, 0);
 #pragma unroll
           for (int q = 0; q < 64; ++q)
-            if (q < lo) pr[q] = 0.f;
+            if ((unsigned)(q - lo) >= width) pr[q] = 0.f;
         }
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_read, n & 1, wc));
@@ -693,6 +715,8 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   bp.err = device_err_flag();
   bp.BH = (int)BH;
   bp.group = g.H / g.Hkv;
+  bp.doc_lo = g.doc_lo;
+  bp.doc_hi = g.doc_hi;
   bp.T = g.T;
   bp.T_valid = g.T_valid;
   bp.c = g.c;

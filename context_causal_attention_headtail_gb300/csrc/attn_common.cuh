@@ -160,69 +160,135 @@ __device__ __forceinline__ int warp_offset(int cnt, int lane, int &base) {
   return off;
 }
 
-// K/V tiles seen by a query tile of rank r with positions [qmin, qmax]
-// (the KvSchedule order). All 32 lanes call it; returns the tile count.
+// Tiles [t0, t1] of a chunk that starts at natural position cpos (c rows,
+// tpc tiles) and meet the positions [lo, hi]; t1 < t0 when none do.
+__device__ __forceinline__ void chunk_tiles(int cpos, int c, int tpc, int lo, int hi, int &t0, int &t1) {
+  if (hi < lo || hi < cpos || lo > cpos + c - 1) { t0 = 0; t1 = -1; return; }
+  const int x = lo - cpos - (kTile - 1);            // first tile whose last row reaches lo
+  t0 = x <= 0 ? 0 : (x + kTile - 1) / kTile;
+  t1 = min(tpc - 1, (hi - cpos) / kTile);           // last tile whose first row is <= hi
+}
+
+// What a stationary query tile (rows at positions qmin..qmax) may attend to:
+// keys in [key_lo, key_hi]. A key tile [p0, p0 + nv) needs an element mask if
+// it is ragged, reaches padding, crosses the causal diagonal (p0 + nv - 1 >
+// qmin), starts before doc_lo_max (the document start of the last query) or
+// ends after doc_hi_min (the document end of the first query). Without packed
+// documents doc_lo_max = 0 and doc_hi_min = T.
+struct KvBounds {
+  int key_lo, key_hi, qmin, doc_lo_max, doc_hi_min;
+};
+
+// K/V tiles seen by a query tile of rank r (the KvSchedule order: ring steps,
+// head chunk then tail chunk). All 32 lanes call it; returns the tile count.
 __device__ inline int build_kv_table(TileEntry *tab, int cp, int c, int r, int causal, int T_valid,
-                                     int qmin, int qmax, int lane) {
+                                     const KvBounds &kb, int lane) {
   const int tpc = (c + kTile - 1) / kTile;
   int base = 0;
   for (int g0 = 0; g0 < 2 * cp; g0 += 32) {
     const int g = g0 + lane;
-    int cnt = 0, cpos = 0, slot = 0;
+    int cnt = 0, cpos = 0, slot = 0, t0 = 0;
     if (g < 2 * cp) {
       const int s = g >> 1, half = g & 1;
       const int j = (r - s + cp) % cp;
       cpos = chunk_of(j, half, cp) * c;
       slot = 2 * j + half;
-      // tile kt is live iff cpos + 128 kt < T_valid and (not causal or cpos + 128 kt <= qmax)
-      const int lim = causal ? min(T_valid - 1, qmax) : T_valid - 1;
-      cnt = lim < cpos ? 0 : min(tpc - 1, (lim - cpos) / kTile) + 1;
+      int t1;
+      chunk_tiles(cpos, c, tpc, kb.key_lo, kb.key_hi, t0, t1);
+      cnt = t1 - t0 + 1;
     }
     const int off = warp_offset(cnt, lane, base);
-    for (int kt = 0; kt < cnt; ++kt) {
+    for (int i = 0; i < cnt; ++i) {
+      const int kt = t0 + i;
       const int pos0 = cpos + kt * kTile;
       const int nv = min(kTile, c - kt * kTile);
-      const int nm = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > qmin);
-      tab[off + kt] = encode_tile(pos0, kt, slot, nv, nm);
+      const int nm = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > kb.qmin) ||
+                     (pos0 < kb.doc_lo_max) || (pos0 + nv > kb.doc_hi_min);
+      tab[off + i] = encode_tile(pos0, kt, slot, nv, nm);
     }
   }
   return base;
 }
 
-// Query tiles that see a key tile of rank j with positions [kmin, kmax]
-// (the QSchedule order: at step s the key tile sits on rank (j + s) mod cp).
+// What a stationary key tile (rows at positions kmin..kmax) is seen by:
+// queries in [q_lo, q_hi]. A query tile [p0, p0 + nv) needs an element mask
+// if it or the key tile is ragged, some key is padding, it crosses the causal
+// diagonal (kmax > p0), it starts before doc_lo_max (the document start of
+// the last key) or ends after doc_hi_min (the document end of the first key).
+struct QBounds {
+  int q_lo, q_hi, kmax, doc_lo_max, doc_hi_min;
+};
+
+// Query tiles that see a key tile of rank j (the QSchedule order: at step s
+// the key tile sits on rank (j + s) mod cp).
 __device__ inline int build_q_table(TileEntry *tab, int cp, int c, int j, int causal, int T_valid,
-                                    int kmin, int kmax, int k_ragged, int lane) {
+                                    const QBounds &qb, int k_ragged, int lane) {
   const int tpc = (c + kTile - 1) / kTile;
   int base = 0;
   for (int g0 = 0; g0 < 2 * cp; g0 += 32) {
     const int g = g0 + lane;
-    int cnt = 0, cpos = 0, slot = 0, qt_lo = 0;
-    if (g < 2 * cp && kmin < T_valid) {
+    int cnt = 0, cpos = 0, slot = 0, t0 = 0;
+    if (g < 2 * cp) {
       const int s = g >> 1, half = g & 1;
       const int r = (j + s) % cp;
       cpos = chunk_of(r, half, cp) * c;
       slot = 2 * r + half;
-      if (!causal) {
-        qt_lo = 0;
-      } else if (cpos + c - 1 < kmin) {   // every query of the chunk precedes every key
-        qt_lo = tpc;
-      } else {                             // first tile whose last row reaches kmin
-        const int x = kmin - cpos - (kTile - 1);
-        qt_lo = x <= 0 ? 0 : (x + kTile - 1) / kTile;
-      }
-      cnt = tpc - qt_lo;
+      int t1;
+      chunk_tiles(cpos, c, tpc, qb.q_lo, qb.q_hi, t0, t1);
+      cnt = t1 - t0 + 1;
     }
     const int off = warp_offset(cnt, lane, base);
     for (int i = 0; i < cnt; ++i) {
-      const int qt = qt_lo + i;
+      const int qt = t0 + i;
       const int pos0 = cpos + qt * kTile;
       const int nv = min(kTile, c - qt * kTile);
-      const int nm = (nv < kTile) || k_ragged || (kmax >= T_valid) || (causal && kmax > pos0);
+      const int nm = (nv < kTile) || k_ragged || (qb.kmax >= T_valid) || (causal && qb.kmax > pos0) ||
+                     (pos0 < qb.doc_lo_max) || (pos0 + nv > qb.doc_hi_min);
       tab[off + i] = encode_tile(pos0, qt, slot, nv, nm);
     }
   }
   return base;
+}
+
+// Document bounds [lo, hi) of natural position pos from per-position arrays
+// (nullptr: one document covering everything); values are clamped to [0, T]
+// so that a malformed array cannot send an index out of range.
+__device__ __forceinline__ void doc_bounds_at(const int *doc_lo, const int *doc_hi, int pos, int T,
+                                              int &lo, int &hi) {
+  if (!doc_lo) { lo = 0; hi = T; return; }
+  lo = min(max(__ldg(doc_lo + pos), 0), T);
+  hi = min(max(__ldg(doc_hi + pos), 0), T);
+}
+
+// The KvBounds of a query tile with rows qmin..qmax.
+__device__ __forceinline__ KvBounds kv_bounds(const int *doc_lo, const int *doc_hi, int T, int T_valid,
+                                              int causal, int qmin, int qmax) {
+  int lo_min, hi_min, lo_max, hi_max;
+  doc_bounds_at(doc_lo, doc_hi, qmin, T, lo_min, hi_min);
+  doc_bounds_at(doc_lo, doc_hi, qmax, T, lo_max, hi_max);
+  KvBounds kb;
+  kb.key_lo = lo_min;
+  kb.key_hi = min(T_valid - 1, causal ? qmax : hi_max - 1);
+  if (causal && doc_lo) kb.key_hi = min(kb.key_hi, hi_max - 1);
+  kb.qmin = qmin;
+  kb.doc_lo_max = lo_max;
+  kb.doc_hi_min = hi_min;
+  return kb;
+}
+
+// The QBounds of a key tile with rows kmin..kmax (no query when every key is padding).
+__device__ __forceinline__ QBounds q_bounds(const int *doc_lo, const int *doc_hi, int T, int T_valid,
+                                            int causal, int kmin, int kmax) {
+  int lo_min, hi_min, lo_max, hi_max;
+  doc_bounds_at(doc_lo, doc_hi, kmin, T, lo_min, hi_min);
+  doc_bounds_at(doc_lo, doc_hi, kmax, T, lo_max, hi_max);
+  QBounds qb;
+  qb.q_lo = causal ? kmin : lo_min;
+  qb.q_hi = kmin >= T_valid ? -1 : hi_max - 1;
+  qb.kmax = kmax;
+  qb.doc_lo_max = lo_max;
+  qb.doc_hi_min = hi_min;
+  return qb;
 }
 
 }  // namespace cpattn

@@ -32,6 +32,7 @@ struct FwdParams {
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
   int group;   // query heads per K/V head
+  const int *doc_lo, *doc_hi;   // packed documents: [T] bounds per natural position, or nullptr
   float scale_log2;  // log2(e) / sqrt(d)
   RopeTheta theta;
 };
@@ -398,7 +399,8 @@ __global__ void __launch_bounds__(320, 1)
     tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
     {
-      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, lane);
+      const KvBounds kb = kv_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, q_pos0, q_pos0 + q_rows - 1);
+      const int nt = build_kv_table(tab, cp, c, rq, p.causal, p.T_valid, kb, lane);
       if (lane == 0) *ntiles_slot = nt;
     }
   }
@@ -512,6 +514,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_s = t_row + wg * 128;
     const uint32_t t_o = t_row + colO0 + wg * D;
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this row's document [dlo, dhi) (everything without packed documents)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(q_pos, p.T - 1), p.T, dlo, dhi);
     float m_run = -INFINITY, l = 0.f;
     int n = 0;
     bool ok = true;
@@ -519,15 +523,18 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_full(wg), n & 1, wc));
       if (!ok) break;
       tc::tc_fence_after();
-      // Every mask of a row is an upper bound on the key column j inside the
-      // tile: j < nvalid (ragged tile), pos0 + j < T_valid (padding) and
-      // pos0 + j <= q_pos (causal). Keep j < lim.
-      int lim = kTile;
+      // The masks of a row keep one interval of key columns j of the tile:
+      // j < nvalid (ragged tile), pos0 + j < T_valid (padding), pos0 + j <=
+      // q_pos (causal) and dlo <= pos0 + j < dhi (packed documents). Keep
+      // lo <= j < lim, tested as one unsigned compare of j - lo with width.
+      int lim = kTile, lo = 0;
       if (t.need_mask) {
-        lim = min(t.nvalid, p.T_valid - t.pos0);
+        lim = min(min(t.nvalid, p.T_valid - t.pos0), dhi - t.pos0);
         if (p.causal) lim = min(lim, q_pos - t.pos0 + 1);
+        lo = dlo - t.pos0;
       }
-      const bool masked = __any_sync(0xffffffffu, lim < kTile);
+      const bool masked = __any_sync(0xffffffffu, lim < kTile || lo > 0);
+      const unsigned width = (unsigned)max(lim - lo, 0);
       // pass 1: row max over the kept columns (three-input max).
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(320, 1)
         if (masked) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (cb * 32 + e >= lim) r[e] = 0xff800000u;   // -inf
+            if ((unsigned)(cb * 32 + e - lo) >= width) r[e] = 0xff800000u;   // -inf
         }
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
@@ -587,7 +594,7 @@ __global__ void __launch_bounds__(320, 1)
         if (masked) {
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (cb * 32 + e >= lim) r[e] = 0xff800000u;
+            if ((unsigned)(cb * 32 + e - lo) >= width) r[e] = 0xff800000u;
         }
         uint32_t pk[16];
 #pragma unroll
@@ -634,6 +641,12 @@ __global__ void __launch_bounds__(320, 1)
         }
         if (valid) p.lse[grow] = l > 0.f ? (m_run + log2f(l)) * 0.693147180559945309f : -INFINITY;
       }
+    } else if (ok && prow < q_rows) {   // no key tile at all (rows outside every document)
+      const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y0 + prow);
+      uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
+#pragma unroll 1
+      for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[grow] = -INFINITY;
     }
   }
 
@@ -701,6 +714,8 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   fp.err = device_err_flag();
   fp.BH = (int)BH;
   fp.group = g.H / g.Hkv;
+  fp.doc_lo = g.doc_lo;
+  fp.doc_hi = g.doc_hi;
   fp.T = g.T;
   fp.T_valid = g.T_valid;
   fp.c = g.c;
@@ -717,6 +732,9 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
     return g.d == 128 ? launch_fwd2_t<128>(mq, mk, mv, fp, (unsigned)grid2, s)
                       : launch_fwd2_t<64>(mq, mk, mv, fp, (unsigned)grid2, s);
   }
+  if (g.doc_lo)
+    return fail(CPATTN_ERR_UNSUPPORTED, "packed documents need 2*cp*ceil(c/128) <= %d tiles per chunk "
+                "schedule and RoPE in the shard pass (rope=0)", kMaxTiles);
   const long long grid = BH * 2 * g.cp * fp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
   if (g.d == 128)

@@ -19,7 +19,7 @@ cpattn_status check_launch(const char *what);
 int *device_err_flag();
 
 // Device error codes written to the flag.
-enum : int { ERR_FLAG_TIMEOUT = 1 };
+enum : int { ERR_FLAG_TIMEOUT = 1, ERR_FLAG_BAD_DOCS = 2 };
 
 // RoPE frequencies theta_i, i < d/2 (standard: 10000^(-2i/d); YaRN: the
 // NTK-by-parts blend of theta_i and theta_i / s), split into two floats
@@ -41,11 +41,18 @@ struct Geometry {
   int B, H, T, T_valid, d, cp, c;  // c = T / (2 cp)
   int causal, rope;
   int Hkv;                         // K/V heads; query head h reads K/V head h / (H / Hkv)
+  // Packed documents: per natural position, its document's [doc_lo, doc_hi)
+  // (device int32 [T]); nullptr when the sequence is one document.
+  const int *doc_lo = nullptr, *doc_hi = nullptr;
 };
 
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------
 cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
                            bool inverse, cudaStream_t s);
+// doc_lo[p], doc_hi[p] for p < T from cu_seqlens[0..n_docs]; raises
+// ERR_FLAG_BAD_DOCS on the device flag if cu_seqlens is not a document list.
+cpattn_status launch_doc_bounds(const int *cu_seqlens, int n_docs, int T, int *doc_lo, int *doc_hi,
+                                cudaStream_t s);
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
                                 bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
 cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,

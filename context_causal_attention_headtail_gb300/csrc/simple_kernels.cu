@@ -198,6 +198,47 @@ cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, c
   return check_launch(inverse ? "unshard+RoPE kernel" : "shard+RoPE kernel");
 }
 
+// -------------------------------------------------- document bounds ---
+// Packed documents: document i holds natural positions [cu[i], cu[i+1]);
+// positions >= cu[n] hold padding and get the empty range [cu[n], cu[n]).
+// Thread p finds the last i with cu[i] <= p by binary search. Threads
+// i < n also check the list (cu[0] = 0, non-decreasing, cu[n] <= T); a bad
+// list raises ERR_FLAG_BAD_DOCS and every index stays clamped to [0, T].
+__global__ void __launch_bounds__(256) doc_bounds_kernel(const int *__restrict__ cu, int n, int T,
+                                                         int *__restrict__ doc_lo,
+                                                         int *__restrict__ doc_hi, int *err) {
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p <= n && err) {
+    const int x = __ldg(cu + p);
+    const bool bad = (p == 0 && x != 0) || (p == n && x > T) || (p < n && x > __ldg(cu + p + 1)) || x < 0;
+    if (bad) atomicOr(err, ERR_FLAG_BAD_DOCS);
+  }
+  if (p >= T) return;
+  const int end = min(max(__ldg(cu + n), 0), T);
+  int lo = end, hi = end;
+  if (p < end) {
+    int a = 0, b = n - 1;                      // invariant: the answer is in [a, b]
+    while (a < b) {
+      const int m = (a + b + 1) >> 1;
+      if (__ldg(cu + m) <= p) a = m;
+      else b = m - 1;
+    }
+    lo = min(max(__ldg(cu + a), 0), T);
+    hi = min(max(__ldg(cu + a + 1), 0), T);
+  }
+  doc_lo[p] = lo;
+  doc_hi[p] = hi;
+}
+
+cpattn_status launch_doc_bounds(const int *cu_seqlens, int n_docs, int T, int *doc_lo, int *doc_hi,
+                                cudaStream_t s) {
+  const int threads = 256;
+  const long long need = (long long)(T > n_docs + 1 ? T : n_docs + 1);
+  doc_bounds_kernel<<<(unsigned)((need + threads - 1) / threads), threads, 0, s>>>(
+      cu_seqlens, n_docs, T, doc_lo, doc_hi, device_err_flag());
+  return check_launch("document bounds kernel");
+}
+
 // ------------------------------------------------------------- D = dO.O ---
 template <typename T>
 __device__ __forceinline__ float ld_f(const T *p);
@@ -354,7 +395,11 @@ __device__ __forceinline__ float warp_dot(const float (&a)[D / 32], const float 
 }
 
 __device__ __forceinline__ bool pair_allowed(int qp, int kp, const Geometry &g) {
-  return (!g.causal || kp <= qp) && kp < g.T_valid;
+  if (!((!g.causal || kp <= qp) && kp < g.T_valid)) return false;
+  if (!g.doc_lo) return true;
+  // packed documents: the key must lie in the query's document [lo, hi)
+  const int lo = min(max(__ldg(g.doc_lo + qp), 0), g.T), hi = min(max(__ldg(g.doc_hi + qp), 0), g.T);
+  return kp >= lo && kp < hi;
 }
 
 // Forward: one warp per sharded query row. For ring step s the row's rank r

@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import dataclasses
 
+import numpy as np
 import torch
 
 
@@ -35,6 +36,8 @@ class Workload:
     H_kv: int = 0   # K/V heads (grouped-query attention); 0 means H
     yarn_factor: float = 1.0   # YaRN context-extension factor of the RoPE (1: standard)
     yarn_original: int = 0     # length the weights were trained at (YaRN only)
+    doc_len: tuple = (0, 0)    # packed documents: lengths uniform in [lo, hi]; (0, 0): one sequence
+    doc_seed: int = 0
 
     @property
     def kv_heads(self) -> int:
@@ -43,6 +46,25 @@ class Workload:
     @property
     def yarn(self) -> bool:
         return self.rope and self.yarn_factor != 1.0
+
+    @property
+    def packed(self) -> bool:
+        return self.doc_len[1] > 0
+
+    def cu_seqlens(self):
+        """Document boundaries of a packed workload (int32 numpy [n_docs + 1]), or None.
+
+        Lengths are drawn uniformly from doc_len with a generator seeded by
+        doc_seed, documents are laid end to end from position 0, and the last
+        one is cut at T_valid; positions T_valid..T-1 are padding.
+        """
+        if not self.packed:
+            return None
+        rng = np.random.default_rng(4321 + self.doc_seed)
+        cu = [0]
+        while cu[-1] < self.T_valid:
+            cu.append(min(self.T_valid, cu[-1] + int(rng.integers(self.doc_len[0], self.doc_len[1] + 1))))
+        return np.asarray(cu, dtype=np.int32)
 
     @property
     def chunk(self) -> int:
@@ -56,9 +78,14 @@ class Workload:
         """Algorithmic forward flops: QK^T and PV over the live score pairs.
 
         Causal counts half of the dense T_valid x T_valid square
-        (2 GEMMs x 2 flops x d per pair); non-causal counts all of it.
+        (2 GEMMs x 2 flops x d per pair); non-causal counts all of it. Packed
+        documents count each document's own square.
         """
-        pairs = self.T_valid * self.T_valid * (0.5 if self.causal else 1.0)
+        if self.packed:     # live pairs lie inside the documents only
+            lens = np.diff(self.cu_seqlens()).astype(np.float64)
+            pairs = float(np.sum(lens * lens)) * (0.5 if self.causal else 1.0)
+        else:
+            pairs = self.T_valid * self.T_valid * (0.5 if self.causal else 1.0)
         return 4.0 * self.B * self.H * pairs * self.d
 
     def fwdbwd_flops(self) -> float:
@@ -66,7 +93,7 @@ class Workload:
         return 3.5 * self.fwd_flops()
 
 
-# The five workloads of the benchmark description, then grouped K/V and YaRN.
+# The five workloads of the benchmark description, then grouped K/V, YaRN and packed documents.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", B=1, T=512, T_valid=512, H=4, d=64, cp=2,
                           causal=True, rope=False, dtype="f32", qkv_std=1.0),
@@ -85,6 +112,9 @@ WORKLOADS = {
     "yarn_32k": Workload("yarn_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
                          causal=True, rope=True, dtype="bf16", qkv_std=0.5,
                          yarn_factor=2.0, yarn_original=16384),
+    # Packed documents in the 32k window: lengths uniform in 1k-8k tokens.
+    "varlen_32k": Workload("varlen_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
+                           causal=True, rope=True, dtype="bf16", qkv_std=0.5, doc_len=(1024, 8192)),
 }
 
 # Seeds: 1234 + the workload's position in the list above (1-based).
@@ -94,10 +124,12 @@ SEEDS = {name: 1234 + i + 1 for i, name in enumerate(WORKLOADS)}
 def make_workload(name: str = "custom", *, B: int, T: int, H: int, d: int, cp: int,
                   T_valid: int | None = None, causal: bool = True, rope: bool = False,
                   dtype: str = "bf16", qkv_std: float = 0.5, H_kv: int = 0,
-                  yarn_factor: float = 1.0, yarn_original: int = 0) -> Workload:
+                  yarn_factor: float = 1.0, yarn_original: int = 0, doc_len: tuple = (0, 0),
+                  doc_seed: int = 0) -> Workload:
     return Workload(name, B=B, T=T, T_valid=T if T_valid is None else T_valid, H=H, d=d,
                     cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std, H_kv=H_kv,
-                    yarn_factor=yarn_factor, yarn_original=yarn_original)
+                    yarn_factor=yarn_factor, yarn_original=yarn_original, doc_len=tuple(doc_len),
+                    doc_seed=doc_seed)
 
 
 def make_inputs(w: Workload, seed: int) -> dict[str, torch.Tensor]:

@@ -185,6 +185,42 @@ cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const 
                              void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                              int cp, int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ------------------------------------------ packed documents (varlen) ---
+ * Several documents packed along T (the THD layout of "fix(cp): preserve
+ * gradients when sharding VLM inputs - #2931"; Claude Logs, 2026-07-16:
+ * training on length-bucketed documents, HANDOFF_H200_32K: 16k-32k
+ * documents in a 32k window). A query attends only to keys of its own
+ * document, causally when causal = 1; positions past the last document are
+ * padding and attend to nothing (O = 0, LSE = -inf, zero gradients).
+ *
+ * cpattn_doc_bounds turns cu_seqlens (device int32 [n_docs + 1],
+ * 0 = cu[0] <= cu[1] <= ... <= cu[n_docs] <= T; document i holds natural
+ * positions [cu[i], cu[i+1])) into per-position bounds: doc_lo[p], doc_hi[p]
+ * (device int32 [T] each, natural order, caller-owned, 16-byte aligned) are
+ * the start and end of p's document, and both equal cu[n_docs] for padding.
+ * The list is checked on the device: a bad one makes the next
+ * cpattn_sync_status return CPATTN_ERR_ARG (the bounds then stay inside
+ * [0, T] but mean nothing). One layout serves every batch row and head.
+ *
+ * cpattn_fwd_varlen / cpattn_bwd_varlen are cpattn_fwd_gqa / cpattn_bwd_gqa
+ * with that same-document condition, rope = 0 (rotate q, k with
+ * cpattn_shard_rope: scores inside one document depend only on position
+ * differences, so global positions give the per-document result), and
+ * T_valid = cu[n_docs] (any T_valid >= it gives the same result). bf16
+ * needs 2*cp*ceil(T/(2*cp*128)) <= 1024, else CPATTN_ERR_UNSUPPORTED; fp32
+ * has no limit. doc_lo / doc_hi are read during the kernels only. */
+cpattn_status cpattn_doc_bounds(const int32_t *cu_seqlens, int n_docs, int T, int32_t *doc_lo,
+                                int32_t *doc_hi, cpattn_stream_t stream);
+cpattn_status cpattn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                                int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                                const int32_t *doc_lo, const int32_t *doc_hi, cpattn_dtype dt,
+                                cpattn_stream_t stream);
+cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                                const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                                int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
+                                cpattn_dtype dt, cpattn_stream_t stream);
+
 /* --------------------------------------------- allocation-free backward ---
  * Not from the pages: an addition of this library for callers that cannot
  * allocate device memory when they call it -- for example a plugin inside a

@@ -30,6 +30,11 @@ def oracle_rope(w: Workload):
     return w.rope
 
 
+def oracle_docs(w: Workload):
+    """cu_seqlens of a packed workload for the oracle, or None."""
+    return w.cu_seqlens()
+
+
 def gpu_rope_cfg(w: Workload):
     """The library's RoPE configuration for a workload (None: standard RoPE)."""
     return cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original) if w.yarn else None
@@ -45,9 +50,14 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     stream = torch.cuda.current_stream(dev)
     fused = w.rope and rope_mode == "shard"
     rope_flag = w.rope and not fused
-    if w.yarn and not fused:
-        raise ValueError("YaRN RoPE runs in the shard / unshard passes only")
+    if (w.yarn or w.packed) and w.rope and not fused:
+        raise ValueError("YaRN and packed documents take RoPE from the shard / unshard passes")
     cfg = gpu_rope_cfg(w)
+    docs = None
+    if w.packed:
+        cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+        docs = (torch.empty(w.T, dtype=torch.int32, device=dev), torch.empty(w.T, dtype=torch.int32, device=dev))
+        cpattn.doc_bounds(cu, w.T, docs[0], docs[1], stream)
     nat = {k: v.to(dev).contiguous() for k, v in inp.items()}
     sh = {k: torch.empty_like(v) for k, v in nat.items()}
     for k in nat:
@@ -59,14 +69,15 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
     out = {}
     for _ in range(repeat):
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream)
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
+                   docs=docs)
     if with_bwd:
         dq, dk, dv = torch.empty_like(sh["q"]), torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
         ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
                          device=dev)
         for _ in range(repeat):
             cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
-                       w.causal, rope_flag, stream)
+                       w.causal, rope_flag, stream, docs=docs)
         for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
             nt = torch.empty_like(t)
             if fused and name in ("dq", "dk"):

@@ -19,15 +19,15 @@ from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make
 from oracle import attention as A
 from oracle import headtail as HT
 
-from harness import TOL, compare, gpu_rope_cfg, oracle_rope, run_gpu, sample_rows
+from harness import TOL, compare, gpu_rope_cfg, oracle_docs, oracle_rope, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
 
 
 def _oracle_full(w, inp):
     q, k, v, do = (inp[n].double().numpy() for n in ("q", "k", "v", "do"))
-    O, L = A.forward(q, k, v, w.causal, w.T_valid, oracle_rope(w))
-    dq, dk, dv = A.backward(q, k, v, O, L, do, w.causal, w.T_valid, oracle_rope(w))
+    O, L = A.forward(q, k, v, w.causal, w.T_valid, oracle_rope(w), docs=oracle_docs(w))
+    dq, dk, dv = A.backward(q, k, v, O, L, do, w.causal, w.T_valid, oracle_rope(w), docs=oracle_docs(w))
     return {"o": O, "lse": L, "dq": dq, "dk": dk, "dv": dv}
 
 
@@ -131,6 +131,42 @@ def test_shard_rope_cfg_factor_one_is_plain_rope():
     assert torch.equal(b, c)
 
 
+@pytest.mark.parametrize("cu,T", [([0, 5, 6, 23, 40, 61], 64), ([0, 64], 64), ([0, 0, 3, 3, 10], 16),
+                                  ([0, 1000, 1000, 4097, 8000, 12289], 12296)])
+def test_doc_bounds_against_oracle(cu, T):
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    lo = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    hi = torch.full((T,), -7, dtype=torch.int32, device="cuda")
+    cpattn.doc_bounds(cu_d, T, lo, hi)
+    cpattn.cpattn_sync_status(None)
+    doc = A.document_of(np.arange(T), np.array(cu))
+    cu_np = np.array(cu)
+    want_lo = np.where(doc >= 0, cu_np[np.maximum(doc, 0)], cu[-1])
+    want_hi = np.where(doc >= 0, cu_np[np.maximum(doc, 0) + 1], cu[-1])
+    assert np.array_equal(lo.cpu().numpy(), want_lo)
+    assert np.array_equal(hi.cpu().numpy(), want_hi)
+
+
+def test_doc_bounds_rejects_a_bad_list():
+    cu_d = torch.tensor([0, 9, 4, 16], dtype=torch.int32, device="cuda")    # not non-decreasing
+    lo = torch.empty(16, dtype=torch.int32, device="cuda")
+    hi = torch.empty(16, dtype=torch.int32, device="cuda")
+    cpattn.doc_bounds(cu_d, 16, lo, hi)
+    with pytest.raises(cpattn.CpattnError) as e:
+        cpattn.cpattn_sync_status(None)
+    assert e.value.status == cpattn.ERR_ARG
+    cpattn.cpattn_sync_status(None)     # the flag is cleared once reported
+    assert int(lo.min()) >= 0 and int(hi.max()) <= 16
+
+
+def test_varlen_long_schedule_is_refused():
+    w = make_workload("long_varlen", B=1, T=2 * 128 * 513, H=1, d=64, cp=128, doc_len=(100, 5000))
+    inp = make_inputs(w, seed=1)
+    with pytest.raises(cpattn.CpattnError) as e:
+        run_gpu(w, inp)
+    assert e.value.status == cpattn.ERR_UNSUPPORTED
+
+
 def test_shard_index_matches_oracle():
     for T, cp in [(8, 2), (24, 3), (32768, 2), (12296, 4)]:
         assert cpattn.cpattn_shard_index(T, cp) == HT.shard_index(T, cp).tolist()
@@ -153,6 +189,8 @@ SMALL_GQA_F32 = [
                   dtype="f32", qkv_std=1.0),
     make_workload("f32_yarn", B=1, T=384, T_valid=381, H=2, d=128, cp=3, rope=True, dtype="f32",
                   qkv_std=1.0, yarn_factor=4.0, yarn_original=96),
+    make_workload("f32_varlen", B=1, T=384, T_valid=379, H=2, H_kv=1, d=64, cp=2, rope=True,
+                  dtype="f32", qkv_std=1.0, doc_len=(1, 120), doc_seed=1),
 ]
 
 SMALL_BF16 = [
@@ -174,6 +212,16 @@ SMALL_BF16 = [
                   yarn_factor=4.0, yarn_original=256),
     make_workload("yarn2_gqa_d64", B=2, T=768, H=4, H_kv=2, d=64, cp=3, rope=True,
                   yarn_factor=2.0, yarn_original=384),
+    # packed documents: short and long ones, boundaries inside tiles and chunks,
+    # one-token documents, padding, GQA, non-causal, ragged chunks
+    make_workload("varlen_short_docs", B=1, T=1024, T_valid=1019, H=2, d=128, cp=2, rope=True,
+                  doc_len=(1, 90), doc_seed=2),
+    make_workload("varlen_long_docs_gqa", B=2, T=2048, H=4, H_kv=2, d=128, cp=2, rope=True,
+                  doc_len=(200, 900), doc_seed=3),
+    make_workload("varlen_noncausal_d64", B=1, T=768, T_valid=760, H=2, d=64, cp=3, causal=False,
+                  rope=False, doc_len=(30, 300), doc_seed=4),
+    make_workload("varlen_ragged_c300", B=1, T=1200, T_valid=1195, H=2, d=128, cp=2, rope=True,
+                  doc_len=(100, 500), doc_seed=5),
 ]
 
 
@@ -182,8 +230,8 @@ SMALL_BF16 = [
 def test_fp32_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
-    if mode == "kernel" and w.yarn:
-        pytest.skip("YaRN runs in the shard / unshard passes only")
+    if mode == "kernel" and (w.yarn or (w.packed and w.rope)):
+        pytest.skip("YaRN and packed documents take RoPE from the shard / unshard passes")
     inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
     _check_full(w, run_gpu(w, inp, rope_mode=mode), _oracle_full(w, inp))
 
@@ -193,8 +241,8 @@ def test_fp32_path_full(w, mode):
 def test_bf16_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
-    if mode == "kernel" and w.yarn:
-        pytest.skip("YaRN runs in the shard / unshard passes only")
+    if mode == "kernel" and (w.yarn or (w.packed and w.rope)):
+        pytest.skip("YaRN and packed documents take RoPE from the shard / unshard passes")
     inp = make_inputs(w, seed=7 + w.T + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     want = _oracle_full(w, inp)
@@ -247,13 +295,16 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
     rows = sample_rows(w, n_random, seed=w.T)
     real = rows[rows < w.T_valid]
     for (b, h) in heads:
-        o_r, l_r = A.forward_rows(q, k, v, b, h, rows, w.causal, w.T_valid, oracle_rope(w))
+        o_r, l_r = A.forward_rows(q, k, v, b, h, rows, w.causal, w.T_valid, oracle_rope(w),
+                                  docs=oracle_docs(w))
         compare(f"o[{b},{h}]", got["o"][b, h, rows], o_r, tol["o"], tol["cos"])
         compare(f"lse[{b},{h}]", got["lse"][b, h, rows], l_r, tol["lse"])
-        dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, oracle_rope(w))
+        dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, oracle_rope(w),
+                                  docs=oracle_docs(w))
         compare(f"dq[{b},{h}]", got["dq"][b, h, real], dq_r, tol["grad"], tol["cos"])
     b, h = kv_head
-    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, oracle_rope(w))
+    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, oracle_rope(w),
+                                      docs=oracle_docs(w))
     compare(f"dk[{b},{h}]", got["dk"][b, h, rows], dk_c, tol["grad"], tol["cos"])
     compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
 
@@ -261,7 +312,8 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
 @pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
                                        ("long_16k", "shard"), ("window_32k", "shard"),
                                        ("window_32k", "kernel"), ("padded_12289", "shard"),
-                                       ("gqa_32k", "shard"), ("yarn_32k", "shard")])
+                                       ("gqa_32k", "shard"), ("yarn_32k", "shard"),
+                                       ("varlen_32k", "shard")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])

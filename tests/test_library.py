@@ -129,3 +129,16 @@ def test_rope_cfg_layout_matches_header():
     # double, double, int (+4 bytes padding), double, double, double
     assert ctypes.sizeof(cpattn.RopeCfg) == 48
     assert cpattn.RopeCfg.beta_fast.offset == 24 and cpattn.RopeCfg.attention_factor.offset == 40
+
+
+def test_varlen_and_doc_bounds_validation(lib):
+    assert lib.cpattn_doc_bounds(None, 4, 64, P[1], P[2], None) == cpattn.ERR_ARG
+    assert lib.cpattn_doc_bounds(P[0], 0, 64, P[1], P[2], None) == cpattn.ERR_SHAPE
+    assert lib.cpattn_doc_bounds(P[0], 4, 64, P[1] + 4, P[2], None) == cpattn.ERR_ALIGN
+    assert lib.cpattn_doc_bounds(P[0], 4, 64, P[1], P[1] + 128, None) == cpattn.ERR_ARG   # lo, hi overlap
+    st = lib.cpattn_fwd_varlen(*P[:5], 1, 1024, 1024, 2, 2, 128, 2, 1, None, P[6], cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG
+    st = lib.cpattn_bwd_varlen(*P, 1, 1024, 1024, 2, 2, 128, 2, 1, P[0], None, cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG
+    st = lib.cpattn_fwd_varlen(*P[:5], 1, 1000, 1000, 2, 2, 128, 3, 1, P[5], P[6], cpattn.BF16, None)
+    assert st == cpattn.ERR_SHAPE
