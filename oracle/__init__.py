@@ -11,10 +11,12 @@ from the pages it follows and sharing no code with the CUDA path:
 * ``attention`` -- RoPE at global positions, single-pass masked softmax
   attention (forward O and LSE) and its analytic gradients, the log-sum-exp
   merge (SDPAMerger), and the ring variant that merges per-step partials.
+* ``ulysses``   -- the Ulysses all-to-all between sequence and head shards,
+  and the attention run rank by rank on head shards.
 
 Every function is pinned by ``tests/test_oracle.py`` against facts that do not
 come from the oracle itself: the pages' worked HeadTail example, brute-force
 softmax, closed forms, the ring == single-pass invariant, merge algebra,
 complex-number RoPE, and central finite differences.
 """
-from . import attention, headtail  # noqa: F401
+from . import attention, headtail, ulysses  # noqa: F401

@@ -678,3 +678,40 @@ def test_varlen_ring_and_sampled_match_full():
                   - dq[0, 1, rows]).max() < 1e-12
     dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, 0, 0, rows, True, 61, True, docs=DOCS)
     assert np.abs(dk_c - dk[0, 0, rows]).max() < 1e-12 and np.abs(dv_c - dv[0, 0, rows]).max() < 1e-12
+
+
+# ---------------------------------------------------------------- Ulysses ----
+
+from oracle import ulysses as U  # noqa: E402
+
+
+@pytest.mark.parametrize("B,H,T,P", [(1, 4, 8, 2), (2, 6, 12, 3), (1, 8, 16, 4), (2, 3, 9, 1)])
+def test_ulysses_all_to_all_gives_head_blocks(B, H, T, P):
+    x = rnd(B, H, T, 5)
+    xs = U.seq_shards(x, P)
+    Tl, Hl = T // P, H // P
+    for r in range(P):                                    # rank r holds its token block
+        assert np.array_equal(xs[r], x[:, :, r * Tl:(r + 1) * Tl])
+    xh = U.all_to_all(xs)
+    for s in range(P):                                    # rank s holds its heads, all tokens
+        assert np.array_equal(xh[s], x[:, s * Hl:(s + 1) * Hl])
+    assert np.array_equal(U.all_to_all_inverse(xh), xs)
+
+
+def test_ulysses_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        U.seq_shards(rnd(1, 4, 10, 2), 3)
+    with pytest.raises(ValueError):
+        U.all_to_all(rnd(2, 1, 3, 5, 2))
+
+
+@pytest.mark.parametrize("P,H_kv,rope_on,docs", [(2, 4, False, None), (4, 4, True, None),
+                                                 (2, 2, True, None), (2, 4, True, np.array([0, 9, 30, 47]))])
+def test_ulysses_equals_single_pass(P, H_kv, rope_on, docs):
+    T, d = 48, 8
+    q, k, v = rnd(2, 4, T, d), rnd(2, H_kv, T, d), rnd(2, H_kv, T, d)
+    O, L = A.forward(q, k, v, True, 47, rope_on, docs=docs)
+    Ou, Lu = U.ulysses_forward(q, k, v, P, True, 47, rope_on, docs=docs)
+    assert np.abs(O - Ou).max() < 1e-13
+    fin = np.isfinite(L)
+    assert np.array_equal(fin, np.isfinite(Lu)) and np.abs(L[fin] - Lu[fin]).max() < 1e-13
