@@ -88,6 +88,8 @@ def workload_config(w):
         cfg["H_kv"] = w.kv_heads
     if w.yarn:
         cfg["yarn"] = {"factor": w.yarn_factor, "original_max_position": w.yarn_original}
+    if w.ulysses:
+        cfg["ulysses_ranks"] = w.ulysses
     if w.packed:
         cu = w.cu_seqlens()
         cfg["documents"] = {"n": len(cu) - 1, "length_range": list(w.doc_len),
@@ -292,15 +294,30 @@ def run_ours(args):
     inp = make_inputs(w, rank_seed(w, rank))
     if rank == 0:
         _INPUT_CACHE[w.name] = inp
+    P = w.ulysses
+    if P:
+        # Ulysses: the caller holds P sequence shards (contiguous token blocks,
+        # stacked rank-major as [P*B, H, T/P, d]); the attention runs on the
+        # head shards [P*B, H/P, T, d] at cp = 1.
+        Tl = w.T // P
+        inp = {k: torch.cat([v[:, :, r * Tl:(r + 1) * Tl] for r in range(P)], dim=0).contiguous()
+               for k, v in inp.items()}
     host_in = {k: v.pin_memory() for k, v in inp.items()}
     nat = {k: v.to(dev) for k, v in inp.items()}
-    sh = {k: torch.empty_like(v) for k, v in nat.items()}
+    if P:
+        sh = {k: torch.empty((v.shape[0], v.shape[1] // P, w.T, w.d), dtype=v.dtype, device=dev)
+              for k, v in nat.items()}
+    else:
+        sh = {k: torch.empty_like(v) for k, v in nat.items()}
     o, dq = torch.empty_like(sh["q"]), torch.empty_like(sh["q"])
     dk, dv = torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
-    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
-    ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8, device=dev)
+    Bx, Hx = sh["q"].shape[0], sh["q"].shape[1]       # batch and heads the attention sees
+    cp_attn = 1 if P else w.cp
+    lse = torch.empty((Bx, Hx, w.T), dtype=torch.float32, device=dev)
+    ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(Bx, w.T, Hx, w.d), dtype=torch.uint8, device=dev)
     outs = {"o": o, "dq": dq, "dk": dk, "dv": dv}
-    outs_nat = {k: torch.empty_like(v) for k, v in outs.items()}
+    out_like = {"o": "q", "dq": "q", "dk": "k", "dv": "v"}
+    outs_nat = {k: torch.empty_like(nat[out_like[k]]) for k in outs}
     host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
     host_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     stream = torch.cuda.current_stream(dev)
@@ -337,7 +354,10 @@ def run_ours(args):
         for i, name in enumerate(("q", "k", "v", "do")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
-            if fused and name in ("q", "k"):
+            if P:
+                cpattn.ulysses_a2a(nat[name], sh[name], P, rope=fused and name in ("q", "k"), cfg=rope_cfg,
+                                   stream=stream)
+            elif fused and name in ("q", "k"):
                 cpattn.shard_rope(nat[name], sh[name], w.cp, stream, cfg=rope_cfg)
             else:
                 cpattn.shard(nat[name], sh[name], w.cp, stream)
@@ -345,16 +365,19 @@ def run_ours(args):
             cpattn.doc_bounds(cu_dev, w.T, docs[0], docs[1], stream)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["fwd"]])
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
+        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, cp_attn, w.T_valid, w.causal, rope_flag, stream,
                    docs=docs)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["bwd"]])
-        cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
+        cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
                    w.causal, rope_flag, stream, docs=docs)
         for i, name in enumerate(("o", "dq", "dk", "dv")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
-            if fused and name in ("dq", "dk"):
+            if P:
+                cpattn.ulysses_a2a(outs[name], outs_nat[name], P, inverse=True,
+                                   rope=fused and name in ("dq", "dk"), cfg=rope_cfg, stream=stream)
+            elif fused and name in ("dq", "dk"):
                 cpattn.unshard_rope(outs[name], outs_nat[name], w.cp, stream, cfg=rope_cfg)
             else:
                 cpattn.unshard(outs[name], outs_nat[name], w.cp, stream)

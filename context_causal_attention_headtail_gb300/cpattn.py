@@ -24,7 +24,8 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_bwd_workspace_bytes", "cpattn_bwd", "cpattn_merge", "cpattn_last_error",
            "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
            "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
-           "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen")
+           "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen", "cpattn_ulysses_a2a",
+           "cpattn_ulysses_a2a_rope")
 
 
 class CpattnError(RuntimeError):
@@ -61,6 +62,8 @@ def _declare(lib):
         "cpattn_bwd_noalloc": [_vp] * 9 + [_i] * 9 + [_vp],
         "cpattn_fwd_gqa": [_vp] * 5 + [_i] * 10 + [_vp],
         "cpattn_doc_bounds": [_vp, _i, _i, _vp, _vp, _vp],
+        "cpattn_ulysses_a2a": [_vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp],
+        "cpattn_ulysses_a2a_rope": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _i, _vp],
         "cpattn_fwd_varlen": [_vp] * 5 + [_i] * 8 + [_vp, _vp, _i, _vp],
         "cpattn_bwd_varlen": [_vp] * 10 + [_i] * 8 + [_vp, _vp, _i, _vp],
         "cpattn_shard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
@@ -125,6 +128,15 @@ def cpattn_shard_rope_cfg(src, dst, B, H, T, d, cp, dt, cfg, stream=None):
 def cpattn_unshard_rope_cfg(src, dst, B, H, T, d, cp, dt, cfg, stream=None):
     _check(lib().cpattn_unshard_rope_cfg(src, dst, B, H, T, d, cp, dt,
                                          None if cfg is None else ctypes.byref(cfg), stream))
+
+
+def cpattn_ulysses_a2a(src, dst, B, H, T, d, P, inverse, dt, stream=None):
+    _check(lib().cpattn_ulysses_a2a(src, dst, B, H, T, d, P, inverse, dt, stream))
+
+
+def cpattn_ulysses_a2a_rope(src, dst, B, H, T, d, P, inverse, cfg, dt, stream=None):
+    _check(lib().cpattn_ulysses_a2a_rope(src, dst, B, H, T, d, P, inverse,
+                                         None if cfg is None else ctypes.byref(cfg), dt, stream))
 
 
 def cpattn_shard_index(T, cp):
@@ -268,6 +280,26 @@ def _kv_heads(q, *kv):
             raise CpattnError(ERR_SHAPE, f"K/V-side tensor of shape {tuple(t.shape)} does not match "
                                          f"q {tuple(q.shape)} with {H_kv} K/V heads")
     return H_kv
+
+
+def ulysses_a2a(src, dst, P, inverse=False, rope=False, cfg: RopeCfg | None = None, stream=None):
+    """Sequence shards [P*B, H, T/P, d] <-> head shards [P*B, H/P, T, d] (both
+    rank-major); rope=True also rotates rows at their natural positions, with
+    cfg (YaRN) when given. cfg is not used when rope is False."""
+    if not inverse:
+        PB, H, Tl, d = src.shape
+        B, T = PB // P, Tl * P
+    else:
+        PB, Hl, T, d = src.shape
+        B, H = PB // P, Hl * P
+    if dst.numel() != src.numel():
+        raise CpattnError(ERR_SHAPE, "dst must have as many elements as src")
+    if rope:
+        cpattn_ulysses_a2a_rope(_ptr(src), _ptr(dst), B, H, T, d, P, int(inverse), cfg, _dtype_code(src),
+                                _stream(stream))
+    else:
+        cpattn_ulysses_a2a(_ptr(src), _ptr(dst), B, H, T, d, P, int(inverse), _dtype_code(src),
+                           _stream(stream))
 
 
 def doc_bounds(cu_seqlens, T, doc_lo, doc_hi, stream=None):

@@ -276,6 +276,46 @@ cpattn_status cpattn_unshard_rope_cfg(const void *src, void *dst, int B, int H, 
   return shard_common(src, dst, B, H, T, d, cp, dt, stream, true, true, cfg);
 }
 
+static cpattn_status ulysses_common(const void *src, void *dst, int B, int H, int T, int d, int P,
+                                    int inverse, bool rope, const cpattn_rope_cfg *cfg,
+                                    cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!src || !dst) return fail(CPATTN_ERR_ARG, "null pointer");
+  if (B < 1 || H < 1 || T < 1 || d < 1 || P < 1)
+    return fail(CPATTN_ERR_SHAPE, "sizes must be >= 1 (B=%d H=%d T=%d d=%d P=%d)", B, H, T, d, P);
+  if (T % P != 0 || H % P != 0)
+    return fail(CPATTN_ERR_SHAPE, "P=%d must divide T=%d and H=%d", P, T, H);
+  if ((long long)B * H * T > (1LL << 31) - 1) return fail(CPATTN_ERR_SHAPE, "B*H*T too large");
+  if (inverse != 0 && inverse != 1) return fail(CPATTN_ERR_ARG, "inverse must be 0 or 1");
+  if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
+  const int elt = dt == CPATTN_F32 ? 4 : 2;
+  if ((d * elt) % 16 != 0) return fail(CPATTN_ERR_ALIGN, "row of d*elt=%d bytes is not a multiple of 16", d * elt);
+  if (!aligned16(src) || !aligned16(dst)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t bytes = (size_t)B * H * T * d * elt;
+  if (overlaps(src, bytes, dst, bytes)) return fail(CPATTN_ERR_ARG, "src and dst overlap");
+  if (rope && d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: RoPE needs d in {64, 128}", d);
+  if (rope && T > (1 << 24)) return fail(CPATTN_ERR_SHAPE, "T=%d exceeds 2^24", T);
+  Geometry g = geometry(B, H, T, T, d, 1, 1, rope ? 1 : 0);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  trace_record(0, s);
+  cpattn_status st = rope ? launch_ulysses_rope(src, dst, g, P, dt, inverse != 0, cfg, s)
+                          : launch_ulysses(src, dst, g, P, elt, inverse != 0, s);
+  trace_record(1, s);
+  return st;
+}
+
+cpattn_status cpattn_ulysses_a2a(const void *src, void *dst, int B, int H, int T, int d, int P,
+                                 int inverse, cpattn_dtype dt, cpattn_stream_t stream) {
+  return ulysses_common(src, dst, B, H, T, d, P, inverse, false, nullptr, dt, stream);
+}
+
+cpattn_status cpattn_ulysses_a2a_rope(const void *src, void *dst, int B, int H, int T, int d, int P,
+                                      int inverse, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                      cpattn_stream_t stream) {
+  return ulysses_common(src, dst, B, H, T, d, P, inverse, true, cfg, dt, stream);
+}
+
 cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                          int B, int T, int T_valid, int H, int d, int cp, int causal, int rope,
                          cpattn_dtype dt, cpattn_stream_t stream) {

@@ -55,6 +55,13 @@ cpattn_status launch_doc_bounds(const int *cu_seqlens, int n_docs, int T, int *d
                                 cudaStream_t s);
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
                                 bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
+// Ulysses all-to-all of P virtual ranks between the stacked sequence shards
+// [P][B][H][T/P][d] and the stacked head shards [P][B][H/P][T][d] (inverse:
+// back), optionally fused with RoPE (cfg = nullptr and rope = false: none).
+cpattn_status launch_ulysses(const void *src, void *dst, const Geometry &g, int P, int elt_bytes,
+                             bool inverse, cudaStream_t s);
+cpattn_status launch_ulysses_rope(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
+                                  bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
 cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,
                              float *lse, const Geometry &g, cudaStream_t s);
 cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,

@@ -22,24 +22,62 @@ static int sm_count() {
   return n;
 }
 
-// ------------------------------------------------------------------ shard ---
-// One natural chunk kappa of one (b,h) is c contiguous rows; it lands as c
-// contiguous rows at slot 2r+half of the sharded tensor. Each grid row (y)
-// takes whole chunks, each x-block a strided slice of 16-byte words.
-template <bool INVERSE>
-__global__ void __launch_bounds__(256) shard_kernel(const uint4 *__restrict__ src,
-                                                    uint4 *__restrict__ dst, int cp,
-                                                    long long n_chunks, long long chunk_u4) {
-  const int two_cp = 2 * cp;
-  for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
+// ---------------------------------------------------- row permutations ---
+// Both layouts that the path permutes between are made of chunks of
+// contiguous rows: a chunk of the "natural" tensor lands as a chunk of the
+// permuted one. A map gives, for chunk ch, its first row on either side and
+// the natural (global) position of its first row, used by RoPE.
+//
+// HeadTail: chunk (bh, kappa) of c rows; natural row (bh*2cp + kappa)*c, the
+// sharded copy at slot 2r+half of that (b,h), position kappa*c.
+struct HeadTailMap {
+  int cp, c;
+  __device__ __forceinline__ int rows() const { return c; }
+  __device__ __forceinline__ void at(long long ch, long long &nat, long long &perm, int &pos0) const {
+    const int two_cp = 2 * cp;
     const long long bh = ch / two_cp;
     const int kappa = (int)(ch % two_cp);
     int r, half;
     owner_of(kappa, cp, r, half);
-    const long long nat = (bh * two_cp + kappa) * chunk_u4;
-    const long long shd = (bh * two_cp + 2 * r + half) * chunk_u4;
-    const uint4 *s = src + (INVERSE ? shd : nat);
-    uint4 *d = dst + (INVERSE ? nat : shd);
+    nat = (bh * two_cp + kappa) * (long long)c;
+    perm = (bh * two_cp + 2 * r + half) * (long long)c;
+    pos0 = kappa * c;
+  }
+};
+
+// Ulysses all-to-all over P virtual ranks (Tl = T/P tokens, Hl = H/P heads
+// per rank): chunk (r, b, h) is rank r's Tl tokens of head h. Its "natural"
+// side is the stacked sequence shards [P][B][H][Tl] (row ch*Tl); it lands in
+// the stacked head shards [P][B][Hl][T] at rank s = h / Hl, local head
+// h % Hl, rows r*Tl..; position r*Tl.
+struct UlyssesMap {
+  int P, B, H, Tl;
+  __device__ __forceinline__ int rows() const { return Tl; }
+  __device__ __forceinline__ void at(long long ch, long long &nat, long long &perm, int &pos0) const {
+    const int Hl = H / P;
+    const long long bh_all = (long long)B * H;
+    const int r = (int)(ch / bh_all);
+    const long long rem = ch % bh_all;
+    const int b = (int)(rem / H), h = (int)(rem % H);
+    nat = ch * (long long)Tl;
+    perm = (((long long)(h / Hl) * B + b) * Hl + h % Hl) * (long long)Tl * P + (long long)r * Tl;
+    pos0 = r * Tl;
+  }
+};
+
+// Each grid row (y) takes whole chunks, each x-block a strided slice of the
+// chunk's 16-byte words.
+template <class Map, bool INVERSE>
+__global__ void __launch_bounds__(256) permute_kernel(const uint4 *__restrict__ src,
+                                                      uint4 *__restrict__ dst, Map map,
+                                                      long long n_chunks, int row_u4) {
+  const long long chunk_u4 = (long long)map.rows() * row_u4;
+  for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
+    long long nat, perm;
+    int pos0;
+    map.at(ch, nat, perm, pos0);
+    const uint4 *s = src + (INVERSE ? perm : nat) * row_u4;
+    uint4 *d = dst + (INVERSE ? nat : perm) * row_u4;
     const long long stride = (long long)gridDim.x * blockDim.x;
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     for (; i + 3 * stride < chunk_u4; i += 4 * stride) {
@@ -50,10 +88,10 @@ __global__ void __launch_bounds__(256) shard_kernel(const uint4 *__restrict__ sr
   }
 }
 
-cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
-                           bool inverse, cudaStream_t s) {
-  const long long n_chunks = (long long)g.B * g.H * 2 * g.cp;
-  const long long chunk_u4 = (long long)g.c * g.d * elt_bytes / 16;
+template <class Map>
+static cpattn_status launch_permute_t(const void *src, void *dst, const Map &map, int rows,
+                                      long long n_chunks, int row_u4, bool inverse, cudaStream_t s) {
+  const long long chunk_u4 = (long long)rows * row_u4;
   const long long want_blocks = (long long)sm_count() * 8;
   long long bx = (chunk_u4 + 1023) / 1024;
   long long per_chunk = (want_blocks + n_chunks - 1) / n_chunks;
@@ -62,18 +100,33 @@ cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int el
   long long gy = n_chunks < 65535 ? n_chunks : 65535;
   dim3 grid((unsigned)bx, (unsigned)gy);
   if (inverse)
-    shard_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
-                                            g.cp, n_chunks, chunk_u4);
+    permute_kernel<Map, true><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                                   map, n_chunks, row_u4);
   else
-    shard_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
-                                             g.cp, n_chunks, chunk_u4);
-  return check_launch(inverse ? "unshard kernel" : "shard kernel");
+    permute_kernel<Map, false><<<grid, 256, 0, s>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst),
+                                                    map, n_chunks, row_u4);
+  return check_launch(inverse ? "inverse row permutation kernel" : "row permutation kernel");
+}
+
+cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int elt_bytes,
+                           bool inverse, cudaStream_t s) {
+  const HeadTailMap map{g.cp, g.c};
+  return launch_permute_t(src, dst, map, g.c, (long long)g.B * g.H * 2 * g.cp, g.d * elt_bytes / 16,
+                          inverse, s);
+}
+
+cpattn_status launch_ulysses(const void *src, void *dst, const Geometry &g, int P, int elt_bytes,
+                             bool inverse, cudaStream_t s) {
+  const UlyssesMap map{P, g.B, g.H, g.T / P};
+  return launch_permute_t(src, dst, map, g.T / P, (long long)P * g.B * g.H, g.d * elt_bytes / 16,
+                          inverse, s);
 }
 
 // ------------------------------------------------------- shard + RoPE ---
-// HeadTail shard fused with RoPE, and its adjoint fused with unshard, so that
-// the rotation runs inside a pass that already reads and writes every element
-// of q and k. Natural row t of chunk kappa has position p = kappa*c + o.
+// A row permutation (HeadTail shard, Ulysses all-to-all) fused with RoPE, and
+// its adjoint fused with the inverse permutation, so that the rotation runs
+// inside a pass that already reads and writes every element of q and k. Row
+// o of a chunk has position p = pos0 + o.
 //   forward  (shard):   dst[sigma(t)] = m R(p) src[t]
 //   adjoint  (unshard): dst[t] = m R(p)^T src[sigma(t)]
 // (m = 1 and the standard frequencies unless a YaRN configuration is given).
@@ -116,31 +169,28 @@ __device__ __forceinline__ uint4 pack16<float>(const float *x) {
 
 constexpr int kRopeRowsPerBlock = 256;
 
-// grid: x = row blocks of 256 rows within a chunk, y = (b,h,kappa) chunks.
+// grid: x = row blocks of 256 rows within a chunk, y = chunks of the map.
 // block: 256 threads = (D/2)/VEC frequency groups x the rest as row lanes.
-template <typename T, int D, bool INVERSE>
+template <typename T, int D, class Map, bool INVERSE>
 __global__ void __launch_bounds__(256) shard_rope_kernel(const T *__restrict__ src, T *__restrict__ dst,
-                                                         int cp, int c, long long n_chunks, RopeTheta th) {
+                                                         Map map, long long n_chunks, RopeTheta th) {
   constexpr int VEC = VecOf<T>::N;
   constexpr int GROUPS = (D / 2) / VEC;       // frequency groups per row
   constexpr int RS = 256 / GROUPS;            // rows advanced per step
   const int grp = threadIdx.x % GROUPS, lrow = threadIdx.x / GROUPS;
   const int f0 = grp * VEC;
-  const int two_cp = 2 * cp;
+  const int c = map.rows();
   for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
-    const long long bh = ch / two_cp;
-    const int kappa = (int)(ch % two_cp);
-    int r, half;
-    owner_of(kappa, cp, r, half);
-    const long long nat0 = (bh * two_cp + kappa) * (long long)c;       // first natural row of the chunk
-    const long long shd0 = (bh * two_cp + 2 * r + half) * (long long)c;
+    long long nat0, shd0;                      // first row of the chunk on either side
+    int pos0;
+    map.at(ch, nat0, shd0, pos0);
     const int row_begin = blockIdx.x * kRopeRowsPerBlock + lrow;
     const int row_end = min(c, (int)(blockIdx.x + 1) * kRopeRowsPerBlock);
     if (row_begin >= row_end) continue;
     float cs[VEC], sn[VEC], cd[VEC], sd[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
-      rope_sincos(kappa * c + row_begin, th.hi[f0 + v], th.lo[f0 + v], sn[v], cs[v]);
+      rope_sincos(pos0 + row_begin, th.hi[f0 + v], th.lo[f0 + v], sn[v], cs[v]);
       rope_sincos(RS, th.hi[f0 + v], th.lo[f0 + v], sd[v], cd[v]);
     }
     for (int o = row_begin; o < row_end; o += RS) {
@@ -169,33 +219,46 @@ __global__ void __launch_bounds__(256) shard_rope_kernel(const T *__restrict__ s
   }
 }
 
-template <typename T, int D>
-static void launch_shard_rope_t(const void *src, void *dst, const Geometry &g, bool inverse,
-                                const RopeTheta &th, cudaStream_t s) {
-  const long long n_chunks = (long long)g.B * g.H * 2 * g.cp;
-  const unsigned gx = (unsigned)((g.c + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock);
+template <typename T, int D, class Map>
+static void launch_rope_t(const void *src, void *dst, const Map &map, int rows, long long n_chunks,
+                          bool inverse, const RopeTheta &th, cudaStream_t s) {
+  const unsigned gx = (unsigned)((rows + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock);
   const unsigned gy = (unsigned)(n_chunks < 65535 ? n_chunks : 65535);
   dim3 grid(gx, gy);
   if (inverse)
-    shard_rope_kernel<T, D, true><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
-                                                       g.cp, g.c, n_chunks, th);
+    shard_rope_kernel<T, D, Map, true><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
+                                                            map, n_chunks, th);
   else
-    shard_rope_kernel<T, D, false><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
-                                                        g.cp, g.c, n_chunks, th);
+    shard_rope_kernel<T, D, Map, false><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst),
+                                                             map, n_chunks, th);
+}
+
+template <class Map>
+static cpattn_status launch_rope_map(const void *src, void *dst, const Map &map, int rows,
+                                     long long n_chunks, int d, cpattn_dtype dt, bool inverse,
+                                     const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  RopeTheta th;
+  make_rope_theta(d, &th, cfg);
+  if (dt == CPATTN_BF16) {
+    if (d == 128) launch_rope_t<__nv_bfloat16, 128>(src, dst, map, rows, n_chunks, inverse, th, s);
+    else launch_rope_t<__nv_bfloat16, 64>(src, dst, map, rows, n_chunks, inverse, th, s);
+  } else {
+    if (d == 128) launch_rope_t<float, 128>(src, dst, map, rows, n_chunks, inverse, th, s);
+    else launch_rope_t<float, 64>(src, dst, map, rows, n_chunks, inverse, th, s);
+  }
+  return check_launch(inverse ? "inverse permutation + RoPE kernel" : "permutation + RoPE kernel");
 }
 
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
                                 bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
-  RopeTheta th;
-  make_rope_theta(g.d, &th, cfg);
-  if (dt == CPATTN_BF16) {
-    if (g.d == 128) launch_shard_rope_t<__nv_bfloat16, 128>(src, dst, g, inverse, th, s);
-    else launch_shard_rope_t<__nv_bfloat16, 64>(src, dst, g, inverse, th, s);
-  } else {
-    if (g.d == 128) launch_shard_rope_t<float, 128>(src, dst, g, inverse, th, s);
-    else launch_shard_rope_t<float, 64>(src, dst, g, inverse, th, s);
-  }
-  return check_launch(inverse ? "unshard+RoPE kernel" : "shard+RoPE kernel");
+  const HeadTailMap map{g.cp, g.c};
+  return launch_rope_map(src, dst, map, g.c, (long long)g.B * g.H * 2 * g.cp, g.d, dt, inverse, cfg, s);
+}
+
+cpattn_status launch_ulysses_rope(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
+                                  bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  const UlyssesMap map{P, g.B, g.H, g.T / P};
+  return launch_rope_map(src, dst, map, g.T / P, (long long)P * g.B * g.H, g.d, dt, inverse, cfg, s);
 }
 
 // -------------------------------------------------- document bounds ---

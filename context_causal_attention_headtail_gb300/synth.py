@@ -38,6 +38,7 @@ class Workload:
     yarn_original: int = 0     # length the weights were trained at (YaRN only)
     doc_len: tuple = (0, 0)    # packed documents: lengths uniform in [lo, hi]; (0, 0): one sequence
     doc_seed: int = 0
+    ulysses: int = 0           # Ulysses ranks P (sequence -> head shards, attention at cp = 1); 0: ring
 
     @property
     def kv_heads(self) -> int:
@@ -93,7 +94,8 @@ class Workload:
         return 3.5 * self.fwd_flops()
 
 
-# The five workloads of the benchmark description, then grouped K/V, YaRN and packed documents.
+# The five workloads of the benchmark description, then grouped K/V, YaRN, Ulysses and
+# packed documents.
 WORKLOADS = {
     "tiny_fp32": Workload("tiny_fp32", B=1, T=512, T_valid=512, H=4, d=64, cp=2,
                           causal=True, rope=False, dtype="f32", qkv_std=1.0),
@@ -112,6 +114,9 @@ WORKLOADS = {
     "yarn_32k": Workload("yarn_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
                          causal=True, rope=True, dtype="bf16", qkv_std=0.5,
                          yarn_factor=2.0, yarn_original=16384),
+    # Ulysses over 2 virtual ranks at 32k: all-to-all to head shards, attention at cp = 1.
+    "ulysses_32k": Workload("ulysses_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=1,
+                            causal=True, rope=True, dtype="bf16", qkv_std=0.5, ulysses=2),
     # Packed documents in the 32k window: lengths uniform in 1k-8k tokens.
     "varlen_32k": Workload("varlen_32k", B=1, T=32768, T_valid=32768, H=16, d=128, cp=2,
                            causal=True, rope=True, dtype="bf16", qkv_std=0.5, doc_len=(1024, 8192)),
@@ -125,11 +130,11 @@ def make_workload(name: str = "custom", *, B: int, T: int, H: int, d: int, cp: i
                   T_valid: int | None = None, causal: bool = True, rope: bool = False,
                   dtype: str = "bf16", qkv_std: float = 0.5, H_kv: int = 0,
                   yarn_factor: float = 1.0, yarn_original: int = 0, doc_len: tuple = (0, 0),
-                  doc_seed: int = 0) -> Workload:
+                  doc_seed: int = 0, ulysses: int = 0) -> Workload:
     return Workload(name, B=B, T=T, T_valid=T if T_valid is None else T_valid, H=H, d=d,
                     cp=cp, causal=causal, rope=rope, dtype=dtype, qkv_std=qkv_std, H_kv=H_kv,
                     yarn_factor=yarn_factor, yarn_original=yarn_original, doc_len=tuple(doc_len),
-                    doc_seed=doc_seed)
+                    doc_seed=doc_seed, ulysses=ulysses)
 
 
 def make_inputs(w: Workload, seed: int) -> dict[str, torch.Tensor]:

@@ -221,6 +221,29 @@ cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, con
                                 int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
                                 cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ----------------------------------------------- Ulysses all-to-all ---
+ * The Ulysses (DeepSpeed) variant of sequence parallelism on P virtual
+ * ranks (Claude Logs, 2026-06-30: all-to-all layout swaps [B,H,Tl,D] <->
+ * [B,Hl,T,D], contiguous shards, one full attention per rank; 2026-07-01:
+ * the K/V all-to-all moves only K/V heads). With Tl = T/P and Hl = H/P:
+ *   sequence shards  [P][B][H][Tl][d] -- rank r: tokens [r*Tl, (r+1)*Tl) of every head
+ *   head shards      [P][B][Hl][T][d] -- rank s: heads [s*Hl, (s+1)*Hl), all T tokens
+ * inverse = 0 maps sequence shards to head shards (rank s receives head
+ * block s of every rank's tokens, laid out in rank order); inverse = 1 maps
+ * back. The head shards are an ordinary [P*B, Hl, T, d] tensor: run
+ * cpattn_fwd / cpattn_bwd (or the _gqa forms, with the K/V all-to-all over
+ * H_kv heads) on it with B' = P*B, H' = Hl and cp = 1. cpattn_ulysses_a2a_rope
+ * also rotates each row at its natural position r*Tl + t (m R(p) forward,
+ * (m R(p))^T with inverse = 1), cfg as for cpattn_shard_rope_cfg (NULL:
+ * standard RoPE). P must divide T and H, else CPATTN_ERR_SHAPE; otherwise
+ * as cpattn_shard / cpattn_shard_rope (out of place, 16-byte aligned,
+ * d*elt a multiple of 16). */
+cpattn_status cpattn_ulysses_a2a(const void *src, void *dst, int B, int H, int T, int d, int P,
+                                 int inverse, cpattn_dtype dt, cpattn_stream_t stream);
+cpattn_status cpattn_ulysses_a2a_rope(const void *src, void *dst, int B, int H, int T, int d, int P,
+                                      int inverse, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                      cpattn_stream_t stream);
+
 /* --------------------------------------------- allocation-free backward ---
  * Not from the pages: an addition of this library for callers that cannot
  * allocate device memory when they call it -- for example a plugin inside a

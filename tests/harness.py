@@ -40,6 +40,58 @@ def gpu_rope_cfg(w: Workload):
     return cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original) if w.yarn else None
 
 
+def to_seq_shards(x: torch.Tensor, P: int) -> torch.Tensor:
+    """Natural [B, H, T, d] -> the P ranks' sequence shards stacked as [P*B, H, T/P, d]
+    (plain slicing: this is how P ranks would hold the input)."""
+    B, H, T, d = x.shape
+    return torch.cat([x[:, :, r * (T // P):(r + 1) * (T // P)] for r in range(P)], dim=0).contiguous()
+
+
+def from_seq_shards(x: torch.Tensor, P: int) -> torch.Tensor:
+    """Inverse of to_seq_shards."""
+    PB, H, Tl, d = x.shape
+    B = PB // P
+    return torch.cat([x[r * B:(r + 1) * B] for r in range(P)], dim=2).contiguous()
+
+
+def run_gpu_ulysses(w: Workload, inp: dict, device="cuda:0") -> dict:
+    """The Ulysses path: sequence shards -> cpattn_ulysses_a2a(_rope) -> head
+    shards -> cpattn_fwd / cpattn_bwd at cp = 1 over P*B batches of H/P heads
+    -> inverse all-to-all (RoPE adjoint for dq, dk) -> natural order on the CPU."""
+    P = w.ulysses
+    dev = torch.device(device)
+    stream = torch.cuda.current_stream(dev)
+    cfg = gpu_rope_cfg(w)
+    seq = {k: to_seq_shards(v, P).to(dev) for k, v in inp.items()}
+    head = {}
+    for k, v in seq.items():
+        PB, Hx, Tl, d = v.shape
+        head[k] = torch.empty((PB, Hx // P, Tl * P, d), dtype=v.dtype, device=dev)
+        cpattn.ulysses_a2a(v, head[k], P, rope=w.rope and k in ("q", "k"), cfg=cfg, stream=stream)
+    Bp, Hl, T = w.B * P, w.H // P, w.T
+    o = torch.empty_like(head["q"])
+    lse = torch.empty((Bp, Hl, T), dtype=torch.float32, device=dev)
+    cpattn.fwd(head["q"], head["k"], head["v"], o, lse, 1, w.T_valid, w.causal, False, stream)
+    dq, dk, dv = torch.empty_like(head["q"]), torch.empty_like(head["k"]), torch.empty_like(head["v"])
+    ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(Bp, T, Hl, w.d), dtype=torch.uint8, device=dev)
+    cpattn.bwd(head["q"], head["k"], head["v"], o, lse, head["do"], dq, dk, dv, ws, 1, w.T_valid,
+               w.causal, False, stream)
+    out = {}
+    for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+        PB, Hx, Tt, d = t.shape
+        back = torch.empty((PB, Hx * P, Tt // P, d), dtype=t.dtype, device=dev)
+        cpattn.ulysses_a2a(t, back, P, inverse=True, rope=w.rope and name in ("dq", "dk"), cfg=cfg,
+                           stream=stream)
+        out[name] = from_seq_shards(back.float().cpu(), P)
+    lse4 = torch.zeros((Bp, Hl, T, 4), dtype=torch.float32, device=dev)   # 16-byte rows
+    lse4[..., 0] = lse
+    back = torch.empty((Bp, Hl * P, T // P, 4), dtype=torch.float32, device=dev)
+    cpattn.ulysses_a2a(lse4, back, P, inverse=True, stream=stream)
+    out["lse"] = from_seq_shards(back.cpu(), P)[..., 0].contiguous()
+    cpattn.cpattn_sync_status(stream.cuda_stream)
+    return out
+
+
 def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
             rope_mode: str = "kernel") -> dict:
     """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd;

@@ -19,7 +19,9 @@ from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make
 from oracle import attention as A
 from oracle import headtail as HT
 
-from harness import TOL, compare, gpu_rope_cfg, oracle_docs, oracle_rope, run_gpu, sample_rows
+from harness import (TOL, compare, gpu_rope_cfg, oracle_docs, oracle_rope, run_gpu, run_gpu_ulysses,
+                     sample_rows, to_seq_shards)
+from oracle import ulysses as U
 
 pytestmark = pytest.mark.gpu
 
@@ -165,6 +167,76 @@ def test_varlen_long_schedule_is_refused():
     with pytest.raises(cpattn.CpattnError) as e:
         run_gpu(w, inp)
     assert e.value.status == cpattn.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("B,H,T,d,P", [(1, 4, 8, 64, 2), (2, 6, 24, 128, 3), (1, 16, 32768, 128, 2),
+                                       (2, 8, 4096, 64, 4), (1, 3, 300, 128, 1)])
+def test_ulysses_a2a_bit_exact(dtype, B, H, T, d, P):
+    x = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(T + P)).to(dtype)
+    xs = to_seq_shards(x, P).cuda()
+    head = torch.empty((B * P, H // P, T, d), dtype=dtype, device="cuda")
+    back = torch.empty_like(xs)
+    cpattn.ulysses_a2a(xs, head, P)
+    cpattn.ulysses_a2a(head, back, P, inverse=True)
+    torch.cuda.synchronize()
+    want = U.all_to_all(U.seq_shards(x.float().numpy(), P))       # [P, B, Hl, T, d]
+    assert torch.equal(head.cpu(), torch.from_numpy(want.reshape(B * P, H // P, T, d)).to(dtype))
+    assert torch.equal(back.cpu(), xs.cpu())
+
+
+@pytest.mark.parametrize("dtype,B,H,T,d,P,yarn", [(torch.bfloat16, 1, 4, 32768, 128, 2, False),
+                                                  (torch.float32, 2, 6, 1200, 64, 3, True)])
+def test_ulysses_a2a_rope_against_oracle(dtype, B, H, T, d, P, yarn):
+    x = (torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(T)) * 0.5).to(dtype)
+    spec = A.RopeSpec(factor=4.0, original_max_position=T // 4) if yarn else A.STANDARD_ROPE
+    cfg = cpattn.RopeCfg(factor=4.0, original_max_position=T // 4) if yarn else None
+    xs = to_seq_shards(x, P).cuda()
+    head = torch.empty((B * P, H // P, T, d), dtype=dtype, device="cuda")
+    back = torch.empty_like(xs)
+    cpattn.ulysses_a2a(xs, head, P, rope=True, cfg=cfg)
+    cpattn.ulysses_a2a(head, back, P, inverse=True, rope=True, cfg=cfg)
+    torch.cuda.synchronize()
+    xd = x.double().numpy()
+    m = spec.mscale()
+    want = U.all_to_all(U.seq_shards(A.rope(xd, np.arange(T), spec), P)).reshape(B * P, H // P, T, d)
+    pair = np.sqrt(xd[..., : d // 2] ** 2 + xd[..., d // 2:] ** 2)
+    pair = np.concatenate([pair, pair], axis=-1)
+    u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -24
+    pair_h = U.all_to_all(U.seq_shards(pair, P)).reshape(want.shape)
+    err = np.abs(head.double().cpu().numpy() - want)
+    worst = float((err / (u * np.abs(want) + 5e-6 * m * pair_h + 1e-7)).max())
+    assert worst <= 1.0, f"a2a+rope: worst error/bound {worst:.3f}"
+    err = np.abs(back.double().cpu().numpy() - m * m * to_seq_shards(x.double(), P).numpy())
+    pair_s = to_seq_shards(torch.from_numpy(pair), P).numpy()
+    worst = float((err / (3 * u * m * m * pair_s + 1e-5 * m * m * pair_s + 1e-7)).max())
+    assert worst <= 1.0, f"round trip: worst error/bound {worst:.3f}"
+
+
+ULYSSES_SMALL = [
+    make_workload("ulysses2_rope", B=1, T=1024, T_valid=1021, H=4, d=128, cp=1, rope=True, ulysses=2),
+    make_workload("ulysses4_gqa_d64", B=2, T=768, H=8, H_kv=4, d=64, cp=1, rope=True, ulysses=4),
+    make_workload("ulysses2_f32", B=1, T=256, H=2, d=64, cp=1, rope=True, dtype="f32", qkv_std=1.0,
+                  ulysses=2),
+    make_workload("ulysses2_yarn_noncausal", B=1, T=640, H=4, d=128, cp=1, causal=False, rope=True,
+                  yarn_factor=2.0, yarn_original=320, ulysses=2),
+]
+
+
+@pytest.mark.parametrize("w", ULYSSES_SMALL, ids=lambda w: w.name)
+def test_ulysses_path_full(w):
+    inp = make_inputs(w, seed=11 + w.T)
+    got = run_gpu_ulysses(w, inp)
+    _check_full(w, got, _oracle_full(w, inp))
+
+
+def test_ulysses_32k_sampled():
+    w = WORKLOADS["ulysses_32k"]
+    inp = make_inputs(w, SEEDS["ulysses_32k"])
+    got = run_gpu_ulysses(w, inp)
+    for g in ("o", "lse", "dq", "dk", "dv"):
+        assert torch.isfinite(got[g]).all(), g
+    _sampled_check(w, inp, got, [(0, 0), (0, 7), (0, 15)], kv_head=(0, 9))
 
 
 def test_shard_index_matches_oracle():

@@ -26,7 +26,7 @@ def declared_symbols():
     with open(os.path.join(ROOT, "include", "cpattn.h")) as f:
         text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(cpattn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(cpattn_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_exports_every_declared_symbol(lib):
@@ -142,3 +142,21 @@ def test_varlen_and_doc_bounds_validation(lib):
     assert st == cpattn.ERR_ARG
     st = lib.cpattn_fwd_varlen(*P[:5], 1, 1000, 1000, 2, 2, 128, 3, 1, P[5], P[6], cpattn.BF16, None)
     assert st == cpattn.ERR_SHAPE
+
+
+def test_ulysses_binding_rotates_only_when_asked(monkeypatch):
+    """The wrapper picks the rotating entry point from rope alone; a YaRN cfg
+    handed along for V / dO must not rotate them."""
+    import torch
+    calls = []
+    monkeypatch.setattr(cpattn, "_ptr", lambda t: 16)
+    monkeypatch.setattr(cpattn, "_stream", lambda s: None)
+    monkeypatch.setattr(cpattn, "cpattn_ulysses_a2a", lambda *a, **k: calls.append("plain"))
+    monkeypatch.setattr(cpattn, "cpattn_ulysses_a2a_rope", lambda *a, **k: calls.append("rope"))
+    x = torch.zeros(2, 4, 8, 64, dtype=torch.bfloat16)
+    y = torch.zeros(2, 2, 16, 64, dtype=torch.bfloat16)
+    cfg = cpattn.RopeCfg(factor=2.0, original_max_position=8)
+    cpattn.ulysses_a2a(x, y, 2, rope=False, cfg=cfg)
+    cpattn.ulysses_a2a(x, y, 2, rope=True, cfg=cfg)
+    cpattn.ulysses_a2a(y, x, 2, inverse=True, rope=False, cfg=cfg)
+    assert calls == ["plain", "rope", "plain"]
