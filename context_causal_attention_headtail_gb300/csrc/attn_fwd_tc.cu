@@ -535,72 +535,58 @@ __global__ void __launch_bounds__(320, 1)
       }
       const bool masked = __any_sync(0xffffffffu, lim < kTile || lo > 0);
       const unsigned width = (unsigned)max(lim - lo, 0);
-      // pass 1: row max over the kept columns (three-input max).
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_s + cb * 32, r);
-        tc::tmem_ld_wait();
-        if (masked) {
+      // The whole row of S comes out of TMEM in one batch of four loads and
+      // one wait; the max and the exponentials then run from registers.
+      uint32_t r[4][32];
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld32(t_s + cb * 32, r[cb]);
+      tc::tmem_ld_wait();
+      if (masked) {
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if ((unsigned)(cb * 32 + e - lo) >= width) r[e] = 0xff800000u;   // -inf
-        }
+            if ((unsigned)(cb * 32 + e - lo) >= width) r[cb][e] = 0xff800000u;   // -inf
+      }
+      // row max over the kept columns (three-input max)
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb)
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
-          mx[0] = tc::fmax3(mx[0], __uint_as_float(r[e]), __uint_as_float(r[e + 1]));
-          mx[1] = tc::fmax3(mx[1], __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]));
-          mx[2] = tc::fmax3(mx[2], __uint_as_float(r[e + 4]), __uint_as_float(r[e + 5]));
-          mx[3] = tc::fmax3(mx[3], __uint_as_float(r[e + 6]), __uint_as_float(r[e + 7]));
+          mx[0] = tc::fmax3(mx[0], __uint_as_float(r[cb][e]), __uint_as_float(r[cb][e + 1]));
+          mx[1] = tc::fmax3(mx[1], __uint_as_float(r[cb][e + 2]), __uint_as_float(r[cb][e + 3]));
+          mx[2] = tc::fmax3(mx[2], __uint_as_float(r[cb][e + 4]), __uint_as_float(r[cb][e + 5]));
+          mx[3] = tc::fmax3(mx[3], __uint_as_float(r[cb][e + 6]), __uint_as_float(r[cb][e + 7]));
         }
-      }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_new = fmaxf(m_run, mt * sl2);
+      // The running max moves only when it grows by more than 2^8 (the stale
+      // max keeps every P <= 2^8, and l uses the same max, so this is exact).
       bool need = m_new > m_run + 8.f;
+      float alpha = 1.f;
       if (n == 0) {
         m_run = m_new;
         need = false;
-      } else if (__any_sync(0xffffffffu, need)) {
-        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done(wg), (n - 1) & 1, wc));
-        if (!ok) break;
-        tc::tc_fence_after();
-        const float alpha = need ? tc::ex2(m_run - m_new) : 1.f;
-#pragma unroll 1
-        for (int cb = 0; cb < D / 32; ++cb) {
-          uint32_t r[32];
-          tc::tmem_ld32(t_o + cb * 32, r);
-          tc::tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-          tc::tmem_st32(t_o + cb * 32, r);
-        }
-        tc::tmem_st_wait();
-        if (need) {
-          l *= alpha;
-          m_run = m_new;
-        }
+      } else if (need) {
+        alpha = tc::ex2(m_run - m_new);
+        l *= alpha;
+        m_run = m_new;
       }
+      const bool rescale = n > 0 && __any_sync(0xffffffffu, need);
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = 2^(S*scale*log2e - m), rounded to bf16 and written over S;
-      // the argument and the row sum use packed fp32 pairs.
+      // P = 2^(S*scale*log2e - m), rounded to bf16 and written over S; the
+      // argument and the row sum use packed fp32 pairs.
       const uint64_t sl2x2 = tc::f2(sl2, sl2), negm2 = tc::f2(-m_use, -m_use);
       uint64_t ls2[2] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
-#pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t r[32];
-        tc::tmem_ld32(t_s + cb * 32, r);
-        tc::tmem_ld_wait();
-        if (masked) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if ((unsigned)(cb * 32 + e - lo) >= width) r[e] = 0xff800000u;
-        }
+      for (int cb = 0; cb < 4; ++cb) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           float x0, x1;
-          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), sl2x2, negm2), x0, x1);
+          tc::unf2(tc::ffma2(tc::f2(__uint_as_float(r[cb][2 * e]), __uint_as_float(r[cb][2 * e + 1])), sl2x2, negm2),
+                   x0, x1);
           const uint64_t p01 = tc::f2(tc::ex2(x0), tc::ex2(x1));
           ls2[e & 1] = tc::fadd2(ls2[e & 1], p01);
           pk[e] = tc::pack_bf16x2_2(p01);
@@ -611,6 +597,22 @@ __global__ void __launch_bounds__(320, 1)
       tc::unf2(ls2[0], ls[0], ls[1]);
       tc::unf2(ls2[1], ls[2], ls[3]);
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // O *= alpha once PV(n-1) has landed, before PV(n) is issued
+      if (rescale) {
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_o_done(wg), (n - 1) & 1, wc));
+        if (!ok) break;
+        tc::tc_fence_after();
+        uint32_t ro[D / 32][32];
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) tc::tmem_ld32(t_o + cb * 32, ro[cb]);
+        tc::tmem_ld_wait();
+#pragma unroll
+        for (int cb = 0; cb < D / 32; ++cb) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ro[cb][e] = __float_as_uint(__uint_as_float(ro[cb][e]) * alpha);
+          tc::tmem_st32(t_o + cb * 32, ro[cb]);
+        }
+      }
       tc::tmem_st_wait();
       tc::tc_fence_before();
       tc::mbar_arrive(bar_p_full(wg));
