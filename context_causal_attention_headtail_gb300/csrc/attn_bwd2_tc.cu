@@ -53,11 +53,13 @@ __device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchu
 }
 
 // ================================================================== dQ
-// Query-stationary. TMEM: Q (bf16 A operand) 0, dO 64, S 128, dP 256 (dS is
-// written over its first 64 columns), dQ 384. Per key tile n the MMA issuer
-// runs S(n+1) as soon as both softmax warpgroups have read S(n), then dQ(n)
-// once dS(n) is in TMEM, then dP(n+1) once dQ(n) has consumed dS(n).
-// Warpgroup h owns key columns [64h, 64h+64) of each tile.
+// Query-stationary. TMEM: Q (bf16 A operand) 0, dO 64, S 128, dP 256, dQ 384.
+// Warpgroup h owns key columns [64h, 64h+64) of each tile and writes its
+// half of dS (bf16 pairs, 32 columns) over the start of its own half of dP,
+// at 256 + 64h, so neither warpgroup waits for the other; the dQ MMA reads
+// its A operand from columns 256..287 then 320..351. Per key tile n the MMA
+// issuer runs S(n+1) as soon as both softmax warpgroups have read S(n), then
+// dQ(n) once dS(n) is in TMEM, then dP(n+1) once dQ(n) has consumed dS(n).
 template <int D>
 struct Dq3Cfg {
   static constexpr int NS = (D == 128) ? 3 : 4;  // K/V stages
@@ -65,7 +67,7 @@ struct Dq3Cfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NS * TILE;
   static constexpr int OFF_BAR = 2 * NS * TILE;
-  // qdo_ready, fin, s_full, dp_full, s_free, dp_read, ds_ready, dq_done, kv_full[NS], kv_empty[NS]
+  // qdo_ready, fin, s_full, dp_full, s_free, (spare), ds_ready, dq_done, kv_full[NS], kv_empty[NS]
   static constexpr int NBAR = 8 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(320, 1)
   auto sV = [&](int st) { return sbase + C::OFF_V + st * C::TILE; };
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_qdo = bar0, bar_fin = bar0 + 8, bar_s_full = bar0 + 16, bar_dp_full = bar0 + 24,
-                 bar_s_free = bar0 + 32, bar_dp_read = bar0 + 40, bar_ds_ready = bar0 + 48, bar_dq_done = bar0 + 56;
+                 bar_s_free = bar0 + 32, bar_ds_ready = bar0 + 48, bar_dq_done = bar0 + 56;
   auto bar_kv_full = [&](int st) { return bar0 + 64 + 8 * st; };
   auto bar_kv_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -109,7 +111,7 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
-      const bool by_threads = b == bar_qdo || b == bar_s_free || b == bar_dp_read || b == bar_ds_ready;
+      const bool by_threads = b == bar_qdo || b == bar_s_free || b == bar_ds_ready;
       tc::mbar_init(b, by_threads ? 256 : 1);
     }
     abort_flag[0] = 0;
@@ -194,8 +196,9 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t bk = tc::mndesc0(sK(st), kTile);
             const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts(tmem + C::colDQ, tmem + C::colDP + kk * 8, bk + tc::mnoff(kk), idQ, kk > 0 ? 1u : acc0);
+            for (int kk = 0; kk < kTile / 16; ++kk)   // dS of keys 0..63 at +0, of keys 64..127 at +64
+              tc::mma_ts(tmem + C::colDQ, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bk + tc::mnoff(kk), idQ,
+                         kk > 0 ? 1u : acc0);
             tc::mma_commit(bar_dq_done);
             tc::mma_commit(bar_kv_empty(st));
           }
@@ -283,10 +286,6 @@ __global__ void __launch_bounds__(320, 1)
       tc::tmem_ld32(t_row + C::colDP + 64 * h, rd[0]);
       tc::tmem_ld32(t_row + C::colDP + 64 * h + 32, rd[1]);
       tc::tmem_ld_wait();
-      // Both warpgroups must have read dP before either writes dS over it.
-      tc::mbar_arrive(bar_dp_read);
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));
-      if (!ok) break;
       const uint64_t nD2 = tc::f2(-Drow, -Drow);
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
@@ -297,7 +296,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint64_t dp = tc::fadd2(tc::f2(__uint_as_float(rd[cb][2 * e]), __uint_as_float(rd[cb][2 * e + 1])), nD2);
           pk[e] = tc::pack_bf16x2_2(tc::fmul2(tc::f2(pr[j], pr[j + 1]), dp));
         }
-        tc::tmem_st16(t_row + C::colDP + 32 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colDP + 64 * h + cb * 16, pk);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -326,11 +325,14 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ============================================================== dK / dV
-// Key-stationary. TMEM: S^T 0 (P^T written over its first 64 columns),
-// dP^T 128 (dS^T over its first 64), dV 256, dK 256 + D. Per query tile n:
+// Key-stationary. TMEM: S^T 0, dP^T 128, dV 256, dK 256 + D. Warpgroup h owns
+// query columns [64h, 64h+64) and writes its half of P^T (bf16 pairs, 32
+// columns) at 64h and of dS^T at 128 + 64h, over the start of its own
+// halves, so neither warpgroup waits for the other; the dV and dK MMAs read
+// their A operands from the two 32-column pieces. Per query tile n:
 //   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | dK(n) once dS^T(n)
 //   is | S^T(n+1) once dV(n) has consumed P^T | dP^T(n+1) once dK(n) has
-// consumed dS^T; warpgroup h owns query columns [64h, 64h+64).
+// consumed dS^T.
 template <int D>
 struct Dkdv3Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;  // Q/dO stages
@@ -341,7 +343,7 @@ struct Dkdv3Cfg {
   static constexpr int OFF_DO = OFF_Q + NS * TILE;
   static constexpr int OFF_LD = OFF_DO + NS * TILE;  // per stage: lse*log2e [128], D [128]
   static constexpr int OFF_BAR = OFF_LD + NS * 1024;
-  // kv_full, fin, s_full, dp_full, s_read, dp_read, p_ready, ds_ready, dv_done, dk_done, qd_full[NS], qd_empty[NS]
+  // kv_full, fin, s_full, dp_full, (spare), (spare), p_ready, ds_ready, dv_done, dk_done, qd_full[NS], qd_empty[NS]
   static constexpr int NBAR = 10 + 2 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
@@ -366,7 +368,7 @@ __global__ void __launch_bounds__(320, 1)
   auto ld_D = [&](int st) { return reinterpret_cast<float *>(smem + C::OFF_LD + st * 1024 + 512); };
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_kv_full = bar0, bar_fin = bar0 + 8, bar_s_full = bar0 + 16, bar_dp_full = bar0 + 24,
-                 bar_s_read = bar0 + 32, bar_dp_read = bar0 + 40, bar_p_ready = bar0 + 48,
+                 bar_p_ready = bar0 + 48,
                  bar_ds_ready = bar0 + 56, bar_dv_done = bar0 + 64, bar_dk_done = bar0 + 72;
   auto bar_qd_full = [&](int st) { return bar0 + 80 + 8 * st; };
   auto bar_qd_empty = [&](int st) { return bar0 + 80 + 8 * NS + 8 * st; };
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
       uint32_t cnt = 1;
-      if (b == bar_s_read || b == bar_dp_read || b == bar_p_ready || b == bar_ds_ready) cnt = 256;
+      if (b == bar_p_ready || b == bar_ds_ready) cnt = 256;
       for (int st = 0; st < NS; ++st)
         if (b == bar_qd_full(st)) cnt = 33;   // expect_tx arrive + 32 producer lanes
       tc::mbar_init(b, cnt);
@@ -507,7 +509,8 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t bo = tc::mndesc0(sDO(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts(tmem + C::colDV, tmem + C::colS + kk * 8, bo + tc::mnoff(kk), idA, kk > 0 ? 1u : acc0);
+              tc::mma_ts(tmem + C::colDV, tmem + C::colS + kk * 8 + (kk >= 4 ? 32 : 0), bo + tc::mnoff(kk), idA,
+                         kk > 0 ? 1u : acc0);
             tc::mma_commit(bar_dv_done);
           }
           if (!(ok = tc::mbar_wait(bar_ds_ready, n & 1, wc))) break;
@@ -516,7 +519,8 @@ __global__ void __launch_bounds__(320, 1)
             const uint64_t bq = tc::mndesc0(sQ(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts(tmem + C::colDK, tmem + C::colDP + kk * 8, bq + tc::mnoff(kk), idA, kk > 0 ? 1u : acc0);
+              tc::mma_ts(tmem + C::colDK, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bq + tc::mnoff(kk), idA,
+                         kk > 0 ? 1u : acc0);
             tc::mma_commit(bar_dk_done);
             tc::mma_commit(bar_qd_empty(st));
           }
@@ -573,8 +577,6 @@ __global__ void __launch_bounds__(320, 1)
         tc::tmem_ld32(t_row + C::colS + 64 * h, r[0]);
         tc::tmem_ld32(t_row + C::colS + 64 * h + 32, r[1]);
         tc::tmem_ld_wait();
-        // Both warpgroups must have read S^T before either writes P^T over it.
-        tc::mbar_arrive(bar_s_read);
         const uint64_t sl2x2 = tc::f2(sl2, sl2);
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
@@ -597,14 +599,12 @@ __global__ void __launch_bounds__(320, 1)
             if ((unsigned)(q - lo) >= width) pr[q] = 0.f;
         }
       }
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_s_read, n & 1, wc));
-      if (!ok) break;
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
-        tc::tmem_st16(t_row + C::colS + 32 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -617,7 +617,6 @@ __global__ void __launch_bounds__(320, 1)
         tc::tmem_ld32(t_row + C::colDP + 64 * h, rd[0]);
         tc::tmem_ld32(t_row + C::colDP + 64 * h + 32, rd[1]);
         tc::tmem_ld_wait();
-        tc::mbar_arrive(bar_dp_read);
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
           const float4 d4 = tc::lds_f4(sd + 16u * q4);
@@ -632,14 +631,12 @@ __global__ void __launch_bounds__(320, 1)
           tc::unf2(b, pr[q + 2], pr[q + 3]);
         }
       }
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_read, n & 1, wc));
-      if (!ok) break;
 #pragma unroll
       for (int cb = 0; cb < 2; ++cb) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
-        tc::tmem_st16(t_row + C::colDP + 32 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colDP + 64 * h + cb * 16, pk);
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
