@@ -156,26 +156,29 @@ __global__ void __launch_bounds__(320, 1)
       for (int m = (n > NS ? n - NS : 0); m < n; ++m) tc::mbar_wait(bar_kv_full(m % NS), (m / NS) & 1, drain);
     }
   } else if (warp == 9) {
-    if (lane == 0) {
+    {   // the whole warp runs the issue loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idQ = tc::idesc_bf16(128, D, false, true);
       auto issue_s = [&](int st) {
         const uint64_t bk = tc::kdesc0(sK(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ts(tmem + C::colS, tmem + C::colQ + kk * 8, bk + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
-        tc::mma_commit(bar_s_full);
+          tc::mma_ts_w(tmem + C::colS, tmem + C::colQ + kk * 8, bk + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit_w(bar_s_full);
       };
       auto issue_dp = [&](int st) {
         const uint64_t bv = tc::kdesc0(sV(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ts(tmem + C::colDP, tmem + C::colDO + kk * 8, bv + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
-        tc::mma_commit(bar_dp_full);
+          tc::mma_ts_w(tmem + C::colDP, tmem + C::colDO + kk * 8, bv + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit_w(bar_dp_full);
       };
-      bool ok = tc::mbar_wait(bar_qdo, 0, wc);
+      auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
+        return __all_sync(0xffffffffu, tc::mbar_wait(bar, par, w));
+      };
+      bool ok = wait_all(bar_qdo, 0, wc);
       if (ok && ntiles > 0) {
-        ok = tc::mbar_wait(bar_kv_full(0), 0, wc);
+        ok = wait_all(bar_kv_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0);
@@ -185,31 +188,31 @@ __global__ void __launch_bounds__(320, 1)
           const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           if (more) {   // S(n+1) once S(n) has been read
-            if (!(ok = tc::mbar_wait(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
-            if (!(ok = tc::mbar_wait(bar_s_free, n & 1, wc))) break;
+            if (!(ok = wait_all(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_s_free, n & 1, wc))) break;
             tc::tc_fence_after();
             issue_s(st1);
           }
-          if (!(ok = tc::mbar_wait(bar_ds_ready, n & 1, wc))) break;
+          if (!(ok = wait_all(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
           {   // dQ += dS(n) K(n); dS is 128 keys = 64 packed columns
             const uint64_t bk = tc::mndesc0(sK(st), kTile);
             const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)   // dS of keys 0..63 at +0, of keys 64..127 at +64
-              tc::mma_ts(tmem + C::colDQ, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bk + tc::mnoff(kk), idQ,
+              tc::mma_ts_w(tmem + C::colDQ, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bk + tc::mnoff(kk), idQ,
                          kk > 0 ? 1u : acc0);
-            tc::mma_commit(bar_dq_done);
-            tc::mma_commit(bar_kv_empty(st));
+            tc::mma_commit_w(bar_dq_done);
+            tc::mma_commit_w(bar_kv_empty(st));
           }
           if (!more) break;
-          if (!(ok = tc::mbar_wait(bar_dq_done, n & 1, wc))) break;   // dP(n+1) overwrites dS(n)
+          if (!(ok = wait_all(bar_dq_done, n & 1, wc))) break;   // dP(n+1) overwrites dS(n)
           tc::tc_fence_after();
           issue_dp(st1);
         }
       }
-      tc::mma_commit(bar_fin);
-      tc::mbar_wait(bar_fin, 0, drain);
+      tc::mma_commit_w(bar_fin);
+      wait_all(bar_fin, 0, drain);
     }
   } else {
     // ---------------------------------------------- softmax warpgroups (key halves)
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(320, 1)
       for (int m = (n > NS ? n - NS : 0); m < n; ++m) tc::mbar_wait(bar_qd_full(m % NS), (m / NS) & 1, drain);
     }
   } else if (warp == 9) {
-    if (lane == 0) {
+    {   // the whole warp runs the issue loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idA = tc::idesc_bf16(128, D, false, true);
       const uint64_t ak0 = tc::kdesc0(sK), av0 = tc::kdesc0(sV);
@@ -481,19 +484,22 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t bq = tc::kdesc0(sQ(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + C::colS, ak0 + tc::koff(kTile, kk), bq + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
-        tc::mma_commit(bar_s_full);
+          tc::mma_ss_w(tmem + C::colS, ak0 + tc::koff(kTile, kk), bq + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit_w(bar_s_full);
       };
       auto issue_dp = [&](int st) {
         const uint64_t bo = tc::kdesc0(sDO(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(tmem + C::colDP, av0 + tc::koff(kTile, kk), bo + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
-        tc::mma_commit(bar_dp_full);
+          tc::mma_ss_w(tmem + C::colDP, av0 + tc::koff(kTile, kk), bo + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit_w(bar_dp_full);
       };
-      bool ok = tc::mbar_wait(bar_kv_full, 0, wc);
+      auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
+        return __all_sync(0xffffffffu, tc::mbar_wait(bar, par, w));
+      };
+      bool ok = wait_all(bar_kv_full, 0, wc);
       if (ok && ntot > 0) {
-        ok = tc::mbar_wait(bar_qd_full(0), 0, wc);
+        ok = wait_all(bar_qd_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0);
@@ -503,39 +509,39 @@ __global__ void __launch_bounds__(320, 1)
           const bool more = n + 1 < ntot;
           const int st = n % NS, st1 = (n + 1) % NS;
           const uint32_t acc0 = n > 0 ? 1u : 0u;
-          if (!(ok = tc::mbar_wait(bar_p_ready, n & 1, wc))) break;
+          if (!(ok = wait_all(bar_p_ready, n & 1, wc))) break;
           tc::tc_fence_after();
           {   // dV += P^T(n) dO(n)
             const uint64_t bo = tc::mndesc0(sDO(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts(tmem + C::colDV, tmem + C::colS + kk * 8 + (kk >= 4 ? 32 : 0), bo + tc::mnoff(kk), idA,
+              tc::mma_ts_w(tmem + C::colDV, tmem + C::colS + kk * 8 + (kk >= 4 ? 32 : 0), bo + tc::mnoff(kk), idA,
                          kk > 0 ? 1u : acc0);
-            tc::mma_commit(bar_dv_done);
+            tc::mma_commit_w(bar_dv_done);
           }
-          if (!(ok = tc::mbar_wait(bar_ds_ready, n & 1, wc))) break;
+          if (!(ok = wait_all(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
           {   // dK += dS^T(n) Q(n)
             const uint64_t bq = tc::mndesc0(sQ(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts(tmem + C::colDK, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bq + tc::mnoff(kk), idA,
+              tc::mma_ts_w(tmem + C::colDK, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bq + tc::mnoff(kk), idA,
                          kk > 0 ? 1u : acc0);
-            tc::mma_commit(bar_dk_done);
-            tc::mma_commit(bar_qd_empty(st));
+            tc::mma_commit_w(bar_dk_done);
+            tc::mma_commit_w(bar_qd_empty(st));
           }
           if (!more) break;
-          if (!(ok = tc::mbar_wait(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
-          if (!(ok = tc::mbar_wait(bar_dv_done, n & 1, wc))) break;     // S^T(n+1) overwrites P^T(n)
+          if (!(ok = wait_all(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
+          if (!(ok = wait_all(bar_dv_done, n & 1, wc))) break;     // S^T(n+1) overwrites P^T(n)
           tc::tc_fence_after();
           issue_s(st1);
-          if (!(ok = tc::mbar_wait(bar_dk_done, n & 1, wc))) break;     // dP^T(n+1) overwrites dS^T(n)
+          if (!(ok = wait_all(bar_dk_done, n & 1, wc))) break;     // dP^T(n+1) overwrites dS^T(n)
           tc::tc_fence_after();
           issue_dp(st1);
         }
       }
-      tc::mma_commit(bar_fin);
-      tc::mbar_wait(bar_fin, 0, drain);
+      tc::mma_commit_w(bar_fin);
+      wait_all(bar_fin, 0, drain);
     }
   } else {
     // -------------------------------------------- softmax warpgroups (query halves)

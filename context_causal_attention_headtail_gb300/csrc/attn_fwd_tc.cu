@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(320, 1)
       }
     }
   } else if (warp == 9) {
-    if (lane == 0) {
+    {   // the whole warp runs the issue loop; elect.sync picks the issuing lane
       constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idPV = tc::idesc_bf16(128, D, false, true);
       const uint64_t dq0[2] = {tc::kdesc0(sQ(0)), tc::kdesc0(sQ(1))};
@@ -452,8 +452,8 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t d = tmem + i * 128;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss(d, a0 + tc::koff(kTile, kk), b0 + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
-        tc::mma_commit(bar_s_full(i));
+          tc::mma_ss_w(d, a0 + tc::koff(kTile, kk), b0 + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+        tc::mma_commit_w(bar_s_full(i));
       };
       auto issue_pv = [&](int i, int st, int n) {
         const uint64_t b0 = tc::mndesc0(sV(st), kTile);
@@ -461,48 +461,51 @@ __global__ void __launch_bounds__(320, 1)
         const uint32_t acc0 = n > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
-          tc::mma_ts(d, a + kk * 8, b0 + tc::mnoff(kk), idPV, kk > 0 ? 1u : acc0);
-        tc::mma_commit(bar_o_done(i));
+          tc::mma_ts_w(d, a + kk * 8, b0 + tc::mnoff(kk), idPV, kk > 0 ? 1u : acc0);
+        tc::mma_commit_w(bar_o_done(i));
       };
-      bool ok = tc::mbar_wait(bar_q_full, 0, wc);
+      auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
+        return __all_sync(0xffffffffu, tc::mbar_wait(bar, par, w));
+      };
+      bool ok = wait_all(bar_q_full, 0, wc);
       if (ok && ntiles > 0) {
-        ok = tc::mbar_wait(bar_k_full(0), 0, wc);
+        ok = wait_all(bar_k_full(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0, 0);
           issue_s(1, 0);
-          tc::mma_commit(bar_k_empty(0));
+          tc::mma_commit_w(bar_k_empty(0));
         }
         for (int n = 0; ok; ++n) {
           const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           // ---- tile 0: PV0(n), then S0(n+1) once PV0(n) has read P0
-          if (!(ok = tc::mbar_wait(bar_p_full(0), n & 1, wc))) break;
-          if (!(ok = tc::mbar_wait(bar_v_full(st), (n / NS) & 1, wc))) break;
+          if (!(ok = wait_all(bar_p_full(0), n & 1, wc))) break;
+          if (!(ok = wait_all(bar_v_full(st), (n / NS) & 1, wc))) break;
           tc::tc_fence_after();
           issue_pv(0, st, n);
           if (more) {
-            if (!(ok = tc::mbar_wait(bar_k_full(st1), ((n + 1) / NS) & 1, wc))) break;
-            if (!(ok = tc::mbar_wait(bar_o_done(0), n & 1, wc))) break;
+            if (!(ok = wait_all(bar_k_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_o_done(0), n & 1, wc))) break;
             tc::tc_fence_after();
             issue_s(0, st1);
           }
           // ---- tile 1: PV1(n), then S1(n+1)
-          if (!(ok = tc::mbar_wait(bar_p_full(1), n & 1, wc))) break;
+          if (!(ok = wait_all(bar_p_full(1), n & 1, wc))) break;
           tc::tc_fence_after();
           issue_pv(1, st, n);
-          tc::mma_commit(bar_v_empty(st));
+          tc::mma_commit_w(bar_v_empty(st));
           if (more) {
-            if (!(ok = tc::mbar_wait(bar_o_done(1), n & 1, wc))) break;
+            if (!(ok = wait_all(bar_o_done(1), n & 1, wc))) break;
             tc::tc_fence_after();
             issue_s(1, st1);
-            tc::mma_commit(bar_k_empty(st1));
+            tc::mma_commit_w(bar_k_empty(st1));
           }
           if (!more) break;
         }
       }
-      tc::mma_commit(bar_fin);
-      tc::mbar_wait(bar_fin, 0, drain);
+      tc::mma_commit_w(bar_fin);
+      wait_all(bar_fin, 0, drain);
     }
   } else {
     // ----------------------------------------------- softmax warpgroups 0, 1
