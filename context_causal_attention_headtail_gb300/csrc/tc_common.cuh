@@ -43,33 +43,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-#ifndef CPATTN_WAIT_MODE
-#define CPATTN_WAIT_MODE 0
-#endif
-#ifndef CPATTN_WAIT_HINT_NS
-#define CPATTN_WAIT_HINT_NS 100u
-#endif
 // try_wait may suspend the thread while the phase is incomplete; the hint caps
-// one suspension at ~100 ns so a completed phase is seen within ~200 cycles.
+// one suspension at ~100 ns. (A test_wait spin measured slower: the spinning
+// warp takes issue slots from the softmax warps on its sub-partition.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-#if CPATTN_WAIT_MODE == 1
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(CPATTN_WAIT_HINT_NS)
+      : "r"(bar), "r"(parity), "r"(100u)
       : "memory");
-#endif
   return ok != 0;
 }
 
