@@ -42,9 +42,9 @@ DEFAULT_WORKLOAD = "window_32k"
 # on the 32k workload (profiles/tc_kernels_window_32k.md); a kernel missing
 # here has no capture of its current version. Only valid for that workload.
 NCU_TRAFFIC_BYTES = {
-    ("window_32k", "fwd"): 2.216601e9 + 0.115951e9,
-    ("window_32k", "bwd_dkdv"): 4.111218e9 + 0.238513e9,
-    ("window_32k", "bwd_dq"): 4.069039e9 + 0.120629e9,
+    ("window_32k", "fwd"): 2.219289e9 + 0.121222e9,
+    ("window_32k", "bwd_dkdv"): 4.114704e9 + 0.239087e9,
+    ("window_32k", "bwd_dq"): 4.067629e9 + 0.120716e9,
 }
 
 
@@ -350,7 +350,7 @@ def run_ours(args):
         cu_dev = cu_host.to(dev)
         docs = (torch.empty(w.T, dtype=torch.int32, device=dev), torch.empty(w.T, dtype=torch.int32, device=dev))
 
-    def step(evs=None):
+    def step(evs=None, nat=nat, outs_nat=outs_nat, lse=lse):
         for i, name in enumerate(("q", "k", "v", "do")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
@@ -425,35 +425,69 @@ def run_ours(args):
         ker_ms["bwd_dq"] += b[2].elapsed_time(b[3])
     ker_ms = {k: v / args.steps for k, v in ker_ms.items()}
 
-    # e2e through the same public API, host buffers in and out
+    # e2e through the same public API, host buffers in and out. Every step
+    # copies its inputs in from pinned host memory and its results (o, lse,
+    # dq, dk, dv) back out, on two copy streams with double-buffered device
+    # buffers: the inputs of step i+1 and the outputs of step i-1 move while
+    # step i computes, as an input pipeline of a training loop would do.
     e2e = None
     if not args.no_e2e:
+        nat_b = [nat, {k: torch.empty_like(v) for k, v in nat.items()}]
+        out_b = [outs_nat, {k: torch.empty_like(v) for k, v in outs_nat.items()}]
+        lse_b = [lse, torch.empty_like(lse)]
+        h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         for _ in range(2):
             step()
         torch.cuda.synchronize(dev)
         barrier()
+        mk = lambda: torch.cuda.Event()
+        h2d_done, done, d2h_done = [mk(), mk()], [mk(), mk()], [mk(), mk()]
         s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+        def h2d(j):
+            bj = j % 2
+            with torch.cuda.stream(h2d_s):
+                if j >= 2:
+                    h2d_s.wait_event(done[bj])          # step j-2 has read this buffer
+                for k_ in nat:
+                    nat_b[bj][k_].copy_(host_in[k_], non_blocking=True)
+                if cu_dev is not None:
+                    cu_dev.copy_(cu_host, non_blocking=True)
+                h2d_done[bj].record(h2d_s)
+
         s2.record(stream)
-        for _ in range(args.steps):
-            for k_ in nat:
-                nat[k_].copy_(host_in[k_], non_blocking=True)
-            if cu_dev is not None:
-                cu_dev.copy_(cu_host, non_blocking=True)
-            step()
-            for k_ in outs_nat:
-                host_out[k_].copy_(outs_nat[k_], non_blocking=True)
-            host_lse.copy_(lse, non_blocking=True)
+        h2d_s.wait_event(s2)
+        d2h_s.wait_event(s2)
+        h2d(0)
+        for i in range(args.steps):
+            bi = i % 2
+            if i + 1 < args.steps:
+                h2d(i + 1)
+            stream.wait_event(h2d_done[bi])
+            if i >= 2:
+                stream.wait_event(d2h_done[bi])          # outputs of step i-2 are out
+            step(nat=nat_b[bi], outs_nat=out_b[bi], lse=lse_b[bi])
+            done[bi].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(done[bi])
+                for k_ in outs_nat:
+                    host_out[k_].copy_(out_b[bi][k_], non_blocking=True)
+                host_lse.copy_(lse_b[bi], non_blocking=True)
+                d2h_done[bi].record(d2h_s)
+        stream.wait_event(d2h_done[(args.steps - 1) % 2])
         e2.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = max_over_ranks(s2.elapsed_time(e2) / args.steps, world, dev)
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        h2d_bytes = sum(t.numel() * t.element_size() for t in host_in.values())
         if cu_host is not None:
-            h2d += cu_host.numel() * 4
-        d2h = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
+            h2d_bytes += cu_host.numel() * 4
+        d2h_bytes = sum(t.numel() * t.element_size() for t in host_out.values()) + host_lse.numel() * 4
         e2e = {"value": weak_scaling_value(world, w.fwdbwd_flops(), e2e_ms), "unit": UNIT,
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "tokens_per_s": world * w.B * w.T_valid / (e2e_ms * 1e-3)}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+               "tokens_per_s": world * w.B * w.T_valid / (e2e_ms * 1e-3),
+               "copies": "every step: inputs in, outputs out, on two copy streams overlapping the "
+                         "neighbouring steps' compute (double-buffered)"}
 
     peaks = measured_peaks()
     unit_flops = w.fwd_flops() / 2.0          # one GEMM over the live causal pairs
