@@ -318,7 +318,7 @@ def run_ours(args):
     outs = {"o": o, "dq": dq, "dk": dk, "dv": dv}
     out_like = {"o": "q", "dq": "q", "dk": "k", "dv": "v"}
     outs_nat = {k: torch.empty_like(nat[out_like[k]]) for k in outs}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs_nat.items()}
     host_lse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
     stream = torch.cuda.current_stream(dev)
 
