@@ -472,3 +472,52 @@ def test_error_codes_on_device_buffers():
         cpattn.fwd(x, x, x, y, lse, cp=1, T_valid=11)
     assert e.value.status == cpattn.ERR_SHAPE
     cpattn.cpattn_sync_status(None)
+
+
+# ------------------------------------------------------------ edge cases ----
+
+EDGE_SMALL = [
+    # one row per chunk: every tile has a single valid row
+    make_workload("c1_bf16", B=1, T=4, H=1, d=64, cp=2, rope=True),
+    make_workload("c1_f32", B=1, T=8, H=2, d=128, cp=4, rope=True, dtype="f32", qkv_std=1.0),
+    # a single real token followed by padding
+    make_workload("one_valid_token", B=1, T=256, T_valid=1, H=2, d=128, cp=2, rope=True),
+    # many (b, h) problems in one launch
+    make_workload("many_heads", B=8, T=256, H=32, d=64, cp=2, rope=False),
+]
+
+
+@pytest.mark.parametrize("w", EDGE_SMALL, ids=lambda w: w.name)
+def test_edge_cases_full(w):
+    inp = make_inputs(w, seed=3 + w.T)
+    got = run_gpu(w, inp, rope_mode="shard")
+    _check_full(w, got, _oracle_full(w, inp))
+    if w.T_valid < w.T:
+        for g in ("dq", "dk", "dv"):
+            assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
+
+
+def test_one_million_tokens_sampled():
+    """T = 2^20 on one head (cp = 64, c = 8192: the one-tile kernels' schedule
+    of 8192 tiles per CTA): sampled rows of O, LSE and dQ against the oracle,
+    dK and dV through identities of the exact gradient (no RoPE): each row of
+    dS sums to zero, so sum_k dK_k = 0; each row of P sums to one, so
+    sum_k dV_k = sum_i dO_i."""
+    w = make_workload("one_million", B=1, T=1 << 20, H=1, d=64, cp=64, rope=False)
+    inp = make_inputs(w, seed=2024)
+    got = run_gpu(w, inp)
+    rows = np.array(sorted({0, 1, 8191, 8192, (1 << 19) - 1, 1 << 19, (1 << 20) - 1} |
+                           set(np.random.default_rng(9).integers(0, w.T, size=12).tolist())))
+    tol = TOL[w.dtype]
+    o_r, l_r = A.forward_rows(inp["q"], inp["k"], inp["v"], 0, 0, rows, True, w.T_valid, False)
+    compare("o", got["o"][0, 0, rows], o_r, tol["o"], tol["cos"])
+    compare("lse", got["lse"][0, 0, rows], l_r, tol["lse"])
+    dq_r = A.backward_dq_rows(inp["q"], inp["k"], inp["v"], inp["do"], 0, 0, rows, True, w.T_valid, False)
+    compare("dq", got["dq"][0, 0, rows], dq_r, tol["grad"], tol["cos"])
+    dk = got["dk"][0, 0].double().numpy()
+    dv = got["dv"][0, 0].double().numpy()
+    do = inp["do"][0, 0].double().numpy()
+    assert np.linalg.norm(dk.sum(0)) <= 5e-2 * np.sqrt((dk ** 2).sum())
+    # over 2^20 rows the sums carry the bf16 level of the path (P and dS are
+    # bf16 MMA operands, 2^-9 relative each): bound the mismatch at 2^-7 of |sum dO|
+    assert np.linalg.norm(dv.sum(0) - do.sum(0)) <= 2.0 ** -7 * np.linalg.norm(do.sum(0))
