@@ -57,6 +57,7 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-merge", action="store_true", help="skip timing the standalone merge kernel")
     ap.add_argument("--rope-in-kernel", action="store_true",
                     help="rotate q, k inside the attention kernels (rope=1) instead of in shard/unshard")
     return ap.parse_args()
@@ -513,6 +514,32 @@ def run_ours(args):
             ach = work / t / 1e9
             ker_rep[name] = {"ms": ker_ms[name], "bound": "hbm", "achieved": ach, "unit": "GB/s",
                              "frac": ach / peaks["hbm_gbs"]}
+    # The standalone SDPAMerger (cpattn_merge) is not on the step's path (the
+    # forward merges in its softmax epilogue); it is timed here on its own, on
+    # two fp32 partials of the workload's size, and reported beside the step's
+    # kernels with its HBM roofline.
+    if not args.no_merge:
+        n_parts = 2
+        o_parts = [torch.randn((Bx, Hx, w.T, w.d), device=dev, dtype=torch.float32) for _ in range(n_parts)]
+        l_parts = [torch.randn((Bx, Hx, w.T), device=dev, dtype=torch.float32) for _ in range(n_parts)]
+        o_m = torch.empty((Bx, Hx, w.T, w.d), device=dev, dtype=torch.bfloat16)
+        l_m = torch.empty((Bx, Hx, w.T), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            cpattn.merge(o_parts, l_parts, o_m, l_m, stream)
+        m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        m0.record(stream)
+        for _ in range(10):
+            cpattn.merge(o_parts, l_parts, o_m, l_m, stream)
+        m1.record(stream)
+        torch.cuda.synchronize(dev)
+        merge_ms = m0.elapsed_time(m1) / 10
+        rows = Bx * Hx * w.T
+        merge_bytes = n_parts * rows * (w.d + 1) * 4 + rows * (w.d * 2 + 4)
+        ach = merge_bytes / (merge_ms * 1e-3) / 1e9
+        ker_rep["merge_standalone"] = {"ms": merge_ms, "bound": "hbm", "achieved": ach, "unit": "GB/s",
+                                       "frac": ach / peaks["hbm_gbs"],
+                                       "note": "cpattn_merge of 2 fp32 partials, timed outside the step"}
+        del o_parts, l_parts, o_m, l_m
     dom = max(("fwd", "bwd_dkdv", "bwd_dq", "bwd_D"), key=lambda k: ker_ms[k])
     d = ker_rep[dom]
     roofline = {"kernel": dom, "bound": d["bound"], "achieved": d["achieved"],
