@@ -62,19 +62,58 @@ def all_to_all_inverse(x_head: np.ndarray) -> np.ndarray:
     return out
 
 
+def all_to_all_kv(x_seq: np.ndarray) -> np.ndarray:
+    """The K/V all-to-all: sequence shards [P, B, H_kv, Tl, d] -> head shards.
+
+    With H_kv >= P it is ``all_to_all``. With fewer K/V heads than ranks
+    (P = rep * H_kv) every K/V head is replicated to the rep ranks whose query
+    heads read it ("Claude Logs", 2026-07-01: partial replication by P / n_kv
+    when n_kv < P): rank s receives K/V head s // rep, all T tokens, as
+    [P, B, 1, T, d].
+    """
+    P, B, Hkv, Tl, d = x_seq.shape
+    if Hkv >= P:
+        return all_to_all(x_seq)
+    if P % Hkv:
+        raise ValueError(f"H_kv={Hkv} must divide P={P} when H_kv < P")
+    rep = P // Hkv
+    out = np.empty((P, B, 1, Tl * P, d), dtype=x_seq.dtype)
+    for s in range(P):
+        for r in range(P):
+            out[s, :, 0, r * Tl:(r + 1) * Tl] = x_seq[r, :, s // rep]
+    return out
+
+
+def all_to_all_kv_adjoint(g_head: np.ndarray, H_kv: int) -> np.ndarray:
+    """Adjoint of ``all_to_all_kv``: head-shard gradients back to sequence
+    shards; the rep replicas of a K/V head add up (the group reduce that is the
+    backward of a replication)."""
+    P, B, Hl, T, d = g_head.shape
+    if H_kv >= P:
+        return all_to_all_inverse(g_head)
+    rep = P // H_kv
+    Tl = T // P
+    out = np.zeros((P, B, H_kv, Tl, d), dtype=np.float64)
+    for s in range(P):
+        for r in range(P):
+            out[r, :, s // rep] += g_head[s, :, 0, r * Tl:(r + 1) * Tl]
+    return out
+
+
 def ulysses_forward(q, k, v, P: int, causal: bool = True, T_valid: int | None = None,
                     rope_on=False, docs=None):
     """The Ulysses schedule stated rank by rank; returns natural-order O and LSE.
 
-    q is [B, H, T, d]; k, v are [B, H_kv, T, d] with P dividing H_kv (the K/V
-    all-to-all moves K/V heads only). Rank s attends its Hl query heads over
-    all T tokens with its H_kv / P K/V heads.
+    q is [B, H, T, d]; k, v are [B, H_kv, T, d] with P dividing H_kv, or
+    H_kv dividing P (the K/V all-to-all moves K/V heads only, replicating each
+    to P / H_kv ranks when there are fewer than P). Rank s attends its Hl query
+    heads over all T tokens with the K/V heads it received.
     """
     q, k, v = (attention.as_f64(x) for x in (q, k, v))
     B, H, T, d = q.shape
     Tl, Hl = check_shape(T, H, P)
-    check_shape(T, k.shape[1], P)
-    qh, kh, vh = (all_to_all(seq_shards(x, P)) for x in (q, k, v))
+    qh = all_to_all(seq_shards(q, P))
+    kh, vh = (all_to_all_kv(np.stack([x[:, :, r * Tl:(r + 1) * Tl] for r in range(P)])) for x in (k, v))
     o_head = np.empty_like(qh)
     l_head = np.empty(qh.shape[:4])
     for s in range(P):

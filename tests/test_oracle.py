@@ -715,3 +715,26 @@ def test_ulysses_equals_single_pass(P, H_kv, rope_on, docs):
     assert np.abs(O - Ou).max() < 1e-13
     fin = np.isfinite(L)
     assert np.array_equal(fin, np.isfinite(Lu)) and np.abs(L[fin] - Lu[fin]).max() < 1e-13
+
+
+@pytest.mark.parametrize("P,H,H_kv", [(4, 8, 2), (4, 4, 1), (8, 8, 2), (2, 4, 1)])
+def test_ulysses_kv_replication_equals_single_pass_gqa(P, H, H_kv):
+    T, d = 32, 8
+    q, k, v = rnd(2, H, T, d), rnd(2, H_kv, T, d), rnd(2, H_kv, T, d)
+    O, L = A.forward(q, k, v, True, T, True)
+    Ou, Lu = U.ulysses_forward(q, k, v, P, True, T, True)
+    assert np.abs(O - Ou).max() < 1e-13 and np.abs(L - Lu).max() < 1e-13
+
+
+@pytest.mark.parametrize("P,H_kv", [(4, 2), (4, 1), (8, 2), (4, 4)])
+def test_ulysses_kv_adjoint(P, H_kv):
+    """<A x, y> = <x, A^T y> for the replicating all-to-all and its reduce."""
+    T, d = 16, 5
+    x = rnd(P, 2, H_kv, T // P, d)
+    y = rnd(*U.all_to_all_kv(x).shape)
+    lhs = np.sum(U.all_to_all_kv(x) * y)
+    rhs = np.sum(x * U.all_to_all_kv_adjoint(y, H_kv))
+    assert abs(lhs - rhs) < 1e-10
+    if H_kv < P:   # replication: each K/V head reaches exactly P / H_kv ranks
+        ones = np.ones_like(U.all_to_all_kv(x))
+        assert np.all(U.all_to_all_kv_adjoint(ones, H_kv) == P // H_kv)
