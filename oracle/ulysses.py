@@ -34,9 +34,13 @@ def check_shape(T: int, H: int, P: int) -> tuple[int, int]:
 
 
 def seq_shards(x: np.ndarray, P: int) -> np.ndarray:
-    """Natural [B, H, T, d] -> the P ranks' sequence shards [P, B, H, Tl, d]."""
+    """Natural [B, H, T, d] -> the P ranks' sequence shards [P, B, H, Tl, d]
+    (only the token count must split evenly; the head count matters to the
+    all-to-all)."""
     B, H, T, d = x.shape
-    Tl, _ = check_shape(T, H, P)
+    if P < 1 or T % P:
+        raise ValueError(f"P={P} must divide T={T}")
+    Tl = T // P
     return np.stack([x[:, :, r * Tl:(r + 1) * Tl] for r in range(P)])
 
 
@@ -113,7 +117,7 @@ def ulysses_forward(q, k, v, P: int, causal: bool = True, T_valid: int | None = 
     B, H, T, d = q.shape
     Tl, Hl = check_shape(T, H, P)
     qh = all_to_all(seq_shards(q, P))
-    kh, vh = (all_to_all_kv(np.stack([x[:, :, r * Tl:(r + 1) * Tl] for r in range(P)])) for x in (k, v))
+    kh, vh = (all_to_all_kv(seq_shards(x, P)) for x in (k, v))
     o_head = np.empty_like(qh)
     l_head = np.empty(qh.shape[:4])
     for s in range(P):

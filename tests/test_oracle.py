@@ -702,6 +702,10 @@ def test_ulysses_rejects_bad_shapes():
     with pytest.raises(ValueError):
         U.seq_shards(rnd(1, 4, 10, 2), 3)
     with pytest.raises(ValueError):
+        U.all_to_all(U.seq_shards(rnd(1, 3, 8, 2), 2))       # 2 ranks cannot split 3 heads
+    with pytest.raises(ValueError):
+        U.all_to_all_kv(U.seq_shards(rnd(1, 3, 8, 2), 4))    # nor replicate 3 heads over 4 ranks
+    with pytest.raises(ValueError):
         U.all_to_all(rnd(2, 1, 3, 5, 2))
 
 
