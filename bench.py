@@ -306,7 +306,7 @@ def run_ours(args):
     host_in = {k: v.pin_memory() for k, v in inp.items()}
     nat = {k: v.to(dev) for k, v in inp.items()}
     if P:
-        sh = {k: torch.empty((v.shape[0], v.shape[1] // P, w.T, w.d), dtype=v.dtype, device=dev)
+        sh = {k: torch.empty((v.shape[0], max(v.shape[1] // P, 1), w.T, w.d), dtype=v.dtype, device=dev)
               for k, v in nat.items()}
     else:
         sh = {k: torch.empty_like(v) for k, v in nat.items()}

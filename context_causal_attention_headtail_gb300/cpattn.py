@@ -283,17 +283,16 @@ def _kv_heads(q, *kv):
 
 
 def ulysses_a2a(src, dst, P, inverse=False, rope=False, cfg: RopeCfg | None = None, stream=None):
-    """Sequence shards [P*B, H, T/P, d] <-> head shards [P*B, H/P, T, d] (both
-    rank-major); rope=True also rotates rows at their natural positions, with
-    cfg (YaRN) when given. cfg is not used when rope is False."""
-    if not inverse:
-        PB, H, Tl, d = src.shape
-        B, T = PB // P, Tl * P
-    else:
-        PB, Hl, T, d = src.shape
-        B, H = PB // P, Hl * P
-    if dst.numel() != src.numel():
-        raise CpattnError(ERR_SHAPE, "dst must have as many elements as src")
+    """Sequence shards [P*B, H, T/P, d] <-> head shards [P*B, max(H/P, 1), T, d]
+    (both rank-major). With H < P each head goes to P/H ranks and the inverse
+    sums the replicas. rope=True also rotates rows at their natural positions,
+    with cfg (YaRN) when given; cfg is not used when rope is False."""
+    seq = dst if inverse else src
+    PB, H, Tl, d = seq.shape
+    B, T = PB // P, Tl * P
+    head = (PB, max(H // P, 1), T, d)
+    if tuple((src if inverse else dst).shape) != head:
+        raise CpattnError(ERR_SHAPE, f"head shards must be {head}")
     if rope:
         cpattn_ulysses_a2a_rope(_ptr(src), _ptr(dst), B, H, T, d, P, int(inverse), cfg, _dtype_code(src),
                                 _stream(stream))

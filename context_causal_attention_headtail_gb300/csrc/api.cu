@@ -283,18 +283,21 @@ static cpattn_status ulysses_common(const void *src, void *dst, int B, int H, in
   if (!src || !dst) return fail(CPATTN_ERR_ARG, "null pointer");
   if (B < 1 || H < 1 || T < 1 || d < 1 || P < 1)
     return fail(CPATTN_ERR_SHAPE, "sizes must be >= 1 (B=%d H=%d T=%d d=%d P=%d)", B, H, T, d, P);
-  if (T % P != 0 || H % P != 0)
-    return fail(CPATTN_ERR_SHAPE, "P=%d must divide T=%d and H=%d", P, T, H);
-  if ((long long)B * H * T > (1LL << 31) - 1) return fail(CPATTN_ERR_SHAPE, "B*H*T too large");
+  if (T % P != 0 || (H % P != 0 && (H > P || P % H != 0)))
+    return fail(CPATTN_ERR_SHAPE, "P=%d must divide T=%d, and P must divide H=%d or H divide P", P, T, H);
+  if ((long long)B * (H < P ? P : H) * T > (1LL << 31) - 1) return fail(CPATTN_ERR_SHAPE, "B*H*T too large");
   if (inverse != 0 && inverse != 1) return fail(CPATTN_ERR_ARG, "inverse must be 0 or 1");
   if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
   if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
   const int elt = dt == CPATTN_F32 ? 4 : 2;
   if ((d * elt) % 16 != 0) return fail(CPATTN_ERR_ALIGN, "row of d*elt=%d bytes is not a multiple of 16", d * elt);
   if (!aligned16(src) || !aligned16(dst)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
-  const size_t bytes = (size_t)B * H * T * d * elt;
-  if (overlaps(src, bytes, dst, bytes)) return fail(CPATTN_ERR_ARG, "src and dst overlap");
-  if (rope && d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: RoPE needs d in {64, 128}", d);
+  const size_t seq_bytes = (size_t)B * H * T * d * elt;                    // sequence shards
+  const size_t head_bytes = H < P ? (size_t)P * B * T * d * elt : seq_bytes;   // head shards (replicated)
+  if (overlaps(src, inverse ? head_bytes : seq_bytes, dst, inverse ? seq_bytes : head_bytes))
+    return fail(CPATTN_ERR_ARG, "src and dst overlap");
+  if ((rope || H < P) && d != 64 && d != 128)
+    return fail(CPATTN_ERR_SHAPE, "d=%d: RoPE and replication need d in {64, 128}", d);
   if (rope && T > (1 << 24)) return fail(CPATTN_ERR_SHAPE, "T=%d exceeds 2^24", T);
   Geometry g = geometry(B, H, T, T, d, 1, 1, rope ? 1 : 0);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -62,6 +62,11 @@ cpattn_status launch_ulysses(const void *src, void *dst, const Geometry &g, int 
                              bool inverse, cudaStream_t s);
 cpattn_status launch_ulysses_rope(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
                                   bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
+// With fewer heads than ranks (g.H < P, P a multiple of g.H) the forward
+// direction replicates each head to P / g.H ranks and the inverse is this
+// reduction over the replicas (fp32 sums; RoPE^T after the sum when rope).
+cpattn_status launch_ulysses_kv_reduce(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
+                                       bool rope, const cpattn_rope_cfg *cfg, cudaStream_t s);
 cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, float *o,
                              float *lse, const Geometry &g, cudaStream_t s);
 cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, const float *o,

@@ -65,6 +65,25 @@ struct UlyssesMap {
   }
 };
 
+// Ulysses K/V all-to-all when there are fewer heads than ranks (P = rep * H):
+// head shard rank s receives head s / rep, all T tokens, as [P][B][1][T].
+// Chunk (s, b, r) is rank r's Tl tokens of that head; chunks are enumerated
+// on the receiving side, so a sequence-shard chunk is read once per replica.
+// Forward direction only: the adjoint sums replicas (ulysses_kv_reduce_kernel).
+struct UlyssesRepMap {
+  int P, B, H, Tl;
+  __device__ __forceinline__ int rows() const { return Tl; }
+  __device__ __forceinline__ void at(long long ch, long long &nat, long long &perm, int &pos0) const {
+    const long long per_rank = (long long)B * P;
+    const int s = (int)(ch / per_rank);
+    const long long rem = ch % per_rank;
+    const int b = (int)(rem / P), r = (int)(rem % P);
+    nat = (((long long)r * B + b) * H + s / (P / H)) * (long long)Tl;
+    perm = ((long long)s * B + b) * (long long)Tl * P + (long long)r * Tl;
+    pos0 = r * Tl;
+  }
+};
+
 // Each grid row (y) takes whole chunks, each x-block a strided slice of the
 // chunk's 16-byte words.
 template <class Map, bool INVERSE>
@@ -117,6 +136,11 @@ cpattn_status launch_shard(const void *src, void *dst, const Geometry &g, int el
 
 cpattn_status launch_ulysses(const void *src, void *dst, const Geometry &g, int P, int elt_bytes,
                              bool inverse, cudaStream_t s) {
+  if (g.H < P) {   // replication; the inverse direction is a reduction
+    if (inverse) return launch_ulysses_kv_reduce(src, dst, g, P, elt_bytes == 4 ? CPATTN_F32 : CPATTN_BF16, false, nullptr, s);
+    const UlyssesRepMap map{P, g.B, g.H, g.T / P};
+    return launch_permute_t(src, dst, map, g.T / P, (long long)P * g.B * P, g.d * elt_bytes / 16, false, s);
+  }
   const UlyssesMap map{P, g.B, g.H, g.T / P};
   return launch_permute_t(src, dst, map, g.T / P, (long long)P * g.B * g.H, g.d * elt_bytes / 16,
                           inverse, s);
@@ -257,8 +281,81 @@ cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, c
 
 cpattn_status launch_ulysses_rope(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
                                   bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  if (g.H < P) {
+    if (inverse) return launch_ulysses_kv_reduce(src, dst, g, P, dt, true, cfg, s);
+    const UlyssesRepMap map{P, g.B, g.H, g.T / P};
+    return launch_rope_map(src, dst, map, g.T / P, (long long)P * g.B * P, g.d, dt, false, cfg, s);
+  }
   const UlyssesMap map{P, g.B, g.H, g.T / P};
   return launch_rope_map(src, dst, map, g.T / P, (long long)P * g.B * g.H, g.d, dt, inverse, cfg, s);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Adjoint of the replicating K/V all-to-all: sequence-shard row (r, b, h, t)
+// is the sum, in fp32, of the rep head-shard rows (s, b, 0, r*Tl + t) with
+// s / rep = h, rounded once to the storage type; with RoPE the sum is then
+// turned by (m R(p))^T at p = r*Tl + t. One thread per (row, rotation pair).
+template <typename T, int D, bool ROPE>
+__global__ void __launch_bounds__(256) ulysses_kv_reduce_kernel(const T *__restrict__ src, T *__restrict__ dst,
+                                                                int P, int B, int H, int Tl, long long rows,
+                                                                RopeTheta th) {
+  constexpr int HALF = D / 2;
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * HALF) return;
+  const long long row = idx / HALF;
+  const int i = (int)(idx % HALF);
+  const int t = (int)(row % Tl);
+  const long long rbh = row / Tl;                 // (r*B + b)*H + h
+  const int h = (int)(rbh % H);
+  const long long rb = rbh / H;
+  const int b = (int)(rb % B), r = (int)(rb / B);
+  const int rep = P / H;
+  float x = 0.f, y = 0.f;
+  for (int j = 0; j < rep; ++j) {
+    const int s = h * rep + j;
+    const T *in = src + (((long long)s * B + b) * (long long)Tl * P + (long long)r * Tl + t) * D;
+    x += to_f32(in[i]);
+    y += to_f32(in[i + HALF]);
+  }
+  if (ROPE) {
+    float sn, cs;
+    rope_sincos(r * Tl + t, th.hi[i], th.lo[i], sn, cs);
+    const float xr = fmaf(x, cs, y * sn), yr = fmaf(y, cs, -x * sn);
+    x = xr * th.mscale;
+    y = yr * th.mscale;
+  }
+  T *out = dst + row * D;
+  out[i] = from_f32<T>(x);
+  out[i + HALF] = from_f32<T>(y);
+}
+
+cpattn_status launch_ulysses_kv_reduce(const void *src, void *dst, const Geometry &g, int P, cpattn_dtype dt,
+                                       bool rope, const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  RopeTheta th;
+  make_rope_theta(g.d, &th, cfg);
+  const long long rows = (long long)P * g.B * g.H * (g.T / P);
+  const unsigned blocks = (unsigned)((rows * (g.d / 2) + 255) / 256);
+  const int Tl = g.T / P;
+#define CPATTN_REDUCE(TT, DD, RR)                                                                         \
+  ulysses_kv_reduce_kernel<TT, DD, RR><<<blocks, 256, 0, s>>>(static_cast<const TT *>(src), static_cast<TT *>(dst), \
+                                                               P, g.B, g.H, Tl, rows, th)
+  if (dt == CPATTN_BF16) {
+    if (g.d == 128) { if (rope) CPATTN_REDUCE(__nv_bfloat16, 128, true); else CPATTN_REDUCE(__nv_bfloat16, 128, false); }
+    else { if (rope) CPATTN_REDUCE(__nv_bfloat16, 64, true); else CPATTN_REDUCE(__nv_bfloat16, 64, false); }
+  } else {
+    if (g.d == 128) { if (rope) CPATTN_REDUCE(float, 128, true); else CPATTN_REDUCE(float, 128, false); }
+    else { if (rope) CPATTN_REDUCE(float, 64, true); else CPATTN_REDUCE(float, 64, false); }
+  }
+#undef CPATTN_REDUCE
+  return check_launch("Ulysses K/V reduce kernel");
 }
 
 // -------------------------------------------------- document bounds ---

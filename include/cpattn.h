@@ -235,9 +235,15 @@ cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, con
  * H_kv heads) on it with B' = P*B, H' = Hl and cp = 1. cpattn_ulysses_a2a_rope
  * also rotates each row at its natural position r*Tl + t (m R(p) forward,
  * (m R(p))^T with inverse = 1), cfg as for cpattn_shard_rope_cfg (NULL:
- * standard RoPE). P must divide T and H, else CPATTN_ERR_SHAPE; otherwise
- * as cpattn_shard / cpattn_shard_rope (out of place, 16-byte aligned,
- * d*elt a multiple of 16). */
+ * standard RoPE).
+ * Fewer heads than ranks (the K/V all-to-all of grouped heads when H_kv < P;
+ * Claude Logs, 2026-07-01: replicate by P / n_kv): with H dividing P, rank s
+ * receives head s / (P / H) -- head shards [P][B][1][T][d] -- and inverse = 1
+ * is the adjoint: the P / H replicas of a head are summed (in fp32, rounded
+ * once), then turned by (m R(p))^T for the _rope form. d must then be 64 or 128.
+ * P must divide T, and P must divide H or H divide P, else CPATTN_ERR_SHAPE;
+ * otherwise as cpattn_shard / cpattn_shard_rope (out of place, 16-byte
+ * aligned, d*elt a multiple of 16). */
 cpattn_status cpattn_ulysses_a2a(const void *src, void *dst, int B, int H, int T, int d, int P,
                                  int inverse, cpattn_dtype dt, cpattn_stream_t stream);
 cpattn_status cpattn_ulysses_a2a_rope(const void *src, void *dst, int B, int H, int T, int d, int P,

@@ -66,7 +66,7 @@ def run_gpu_ulysses(w: Workload, inp: dict, device="cuda:0") -> dict:
     head = {}
     for k, v in seq.items():
         PB, Hx, Tl, d = v.shape
-        head[k] = torch.empty((PB, Hx // P, Tl * P, d), dtype=v.dtype, device=dev)
+        head[k] = torch.empty((PB, max(Hx // P, 1), Tl * P, d), dtype=v.dtype, device=dev)
         cpattn.ulysses_a2a(v, head[k], P, rope=w.rope and k in ("q", "k"), cfg=cfg, stream=stream)
     Bp, Hl, T = w.B * P, w.H // P, w.T
     o = torch.empty_like(head["q"])
@@ -79,7 +79,8 @@ def run_gpu_ulysses(w: Workload, inp: dict, device="cuda:0") -> dict:
     out = {}
     for name, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
         PB, Hx, Tt, d = t.shape
-        back = torch.empty((PB, Hx * P, Tt // P, d), dtype=t.dtype, device=dev)
+        Hseq = w.H if name in ("o", "dq") else w.kv_heads
+        back = torch.empty((PB, Hseq, Tt // P, d), dtype=t.dtype, device=dev)
         cpattn.ulysses_a2a(t, back, P, inverse=True, rope=w.rope and name in ("dq", "dk"), cfg=cfg,
                            stream=stream)
         out[name] = from_seq_shards(back.float().cpu(), P)

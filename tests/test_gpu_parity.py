@@ -213,6 +213,41 @@ def test_ulysses_a2a_rope_against_oracle(dtype, B, H, T, d, P, yarn):
     assert worst <= 1.0, f"round trip: worst error/bound {worst:.3f}"
 
 
+@pytest.mark.parametrize("dtype,rope", [(torch.bfloat16, False), (torch.float32, True), (torch.bfloat16, True)])
+@pytest.mark.parametrize("B,H,T,d,P", [(1, 2, 1024, 128, 4), (2, 1, 512, 64, 4), (1, 2, 768, 128, 8)])
+def test_ulysses_kv_replication_against_oracle(dtype, rope, B, H, T, d, P):
+    """Forward: each K/V head to its P/H ranks (bit-exact without RoPE). Inverse:
+    the replicas summed (bit-exact for bf16: the fp32 sum of a few bf16 values
+    is exact, then one rounding, as the oracle's sum rounded once)."""
+    g = torch.Generator().manual_seed(T + H + P)
+    x = (torch.randn(B, H, T, d, generator=g) * 0.5).to(dtype)
+    xs = to_seq_shards(x, P).cuda()
+    head = torch.empty((B * P, 1, T, d), dtype=dtype, device="cuda")
+    cpattn.ulysses_a2a(xs, head, P, rope=rope)
+    y = (torch.randn(B * P, 1, T, d, generator=g) * 0.5).to(dtype)
+    back = torch.empty_like(xs)
+    cpattn.ulysses_a2a(y.cuda(), back, P, inverse=True, rope=rope)
+    torch.cuda.synchronize()
+    xd = x.double().numpy()
+    if rope:
+        xd = A.rope(xd, np.arange(T))
+    want = U.all_to_all_kv(U.seq_shards(xd, P)).reshape(B * P, 1, T, d)
+    yd = y.double().numpy().reshape(P, B, 1, T, d)
+    back_want = U.all_to_all_kv_adjoint(yd, H)          # [P, B, H, T/P, d]
+    if rope:   # (R^T) of the sum, at the natural positions of each sequence shard
+        Tl = T // P
+        for r in range(P):
+            back_want[r] = A.rope_transpose(back_want[r], np.arange(r * Tl, (r + 1) * Tl))
+    back_want = back_want.reshape(B * P, H, T // P, d)
+    if not rope:
+        assert torch.equal(head.cpu(), torch.from_numpy(want).to(dtype))
+        if dtype == torch.bfloat16:
+            assert torch.equal(back.cpu(), torch.from_numpy(back_want).to(dtype))
+    u = 2.0 ** -8 if dtype == torch.bfloat16 else 2.0 ** -23
+    compare("a2a_kv", head.cpu().double(), want, 4 * u * np.abs(want).max() + 1e-5)
+    compare("a2a_kv_adjoint", back.cpu().double(), back_want, 4 * u * np.abs(back_want).max() + 1e-5)
+
+
 ULYSSES_SMALL = [
     make_workload("ulysses2_rope", B=1, T=1024, T_valid=1021, H=4, d=128, cp=1, rope=True, ulysses=2),
     make_workload("ulysses4_gqa_d64", B=2, T=768, H=8, H_kv=4, d=64, cp=1, rope=True, ulysses=4),
@@ -220,6 +255,9 @@ ULYSSES_SMALL = [
                   ulysses=2),
     make_workload("ulysses2_yarn_noncausal", B=1, T=640, H=4, d=128, cp=1, causal=False, rope=True,
                   yarn_factor=2.0, yarn_original=320, ulysses=2),
+    # fewer K/V heads than ranks: K/V replicated to P / H_kv ranks, gradients summed
+    make_workload("ulysses4_kv2_rep", B=1, T=1024, H=8, H_kv=2, d=128, cp=1, rope=True, ulysses=4),
+    make_workload("ulysses4_mqa_d64", B=2, T=512, H=4, H_kv=1, d=64, cp=1, rope=True, ulysses=4),
 ]
 
 
