@@ -333,9 +333,9 @@ __global__ void __launch_bounds__(320, 1)
 // columns) at 64h and of dS^T at 128 + 64h, over the start of its own
 // halves, so neither warpgroup waits for the other; the dV and dK MMAs read
 // their A operands from the two 32-column pieces. Per query tile n:
-//   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | dK(n) once dS^T(n)
-//   is | S^T(n+1) once dV(n) has consumed P^T | dP^T(n+1) once dK(n) has
-// consumed dS^T.
+//   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | S^T(n+1) once dV(n)
+//   has consumed P^T | dK(n) once dS^T(n) is in TMEM | dP^T(n+1) once dK(n)
+// has consumed dS^T.
 template <int D>
 struct Dkdv3Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;  // Q/dO stages
@@ -519,6 +519,15 @@ __global__ void __launch_bounds__(320, 1)
                          kk > 0 ? 1u : acc0);
             tc::mma_commit_w(bar_dv_done);
           }
+          // S^T(n+1) goes ahead of dK(n): it starts the next tile's
+          // exponentials, the longest phase of a tile, while dK(n) and
+          // dP^T(n+1) run.
+          if (more) {
+            if (!(ok = wait_all(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_dv_done, n & 1, wc))) break;   // S^T(n+1) overwrites P^T(n)
+            tc::tc_fence_after();
+            issue_s(st1);
+          }
           if (!(ok = wait_all(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
           {   // dK += dS^T(n) Q(n)
@@ -531,10 +540,6 @@ __global__ void __launch_bounds__(320, 1)
             tc::mma_commit_w(bar_qd_empty(st));
           }
           if (!more) break;
-          if (!(ok = wait_all(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
-          if (!(ok = wait_all(bar_dv_done, n & 1, wc))) break;     // S^T(n+1) overwrites P^T(n)
-          tc::tc_fence_after();
-          issue_s(st1);
           if (!(ok = wait_all(bar_dk_done, n & 1, wc))) break;     // dP^T(n+1) overwrites dS^T(n)
           tc::tc_fence_after();
           issue_dp(st1);
