@@ -29,6 +29,7 @@ struct Bwd2Params {
   int group;   // query heads per K/V head
   const int *doc_lo, *doc_hi;   // packed documents: [T] bounds per natural position, or nullptr
   float scale, scale_log2;
+  RopeTheta theta;   // in-kernel RoPE frequencies (ROPE kernels)
 };
 
 // Scales 32-column chunks [c0, c0 + n*32) of a TMEM row and stores them as
@@ -52,6 +53,60 @@ __device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchu
   }
 }
 
+// Rotate-half RoPE of a bf16 row held as D/2 words in registers (word k holds
+// columns 2k, 2k+1; word k < D/4 pairs with word k + D/4) at natural
+// position pos: R for FORWARD, its transpose otherwise.
+template <int D, bool FORWARD>
+__device__ __forceinline__ void rope_row_words(uint32_t *w, int pos, const RopeTheta &th) {
+#pragma unroll
+  for (int k = 0; k < D / 4; ++k) {
+    float s0, c0, s1, c1;
+    rope_sincos(pos, th.hi[2 * k], th.lo[2 * k], s0, c0);
+    rope_sincos(pos, th.hi[2 * k + 1], th.lo[2 * k + 1], s1, c1);
+    if (!FORWARD) { s0 = -s0; s1 = -s1; }
+    const float x0 = bf16lo_to_f32(w[k]), x1 = bf16hi_to_f32(w[k]);
+    const float y0 = bf16lo_to_f32(w[k + D / 4]), y1 = bf16hi_to_f32(w[k + D / 4]);
+    w[k] = pack_bf16x2(fmaf(x0, c0, -y0 * s0), fmaf(x1, c1, -y1 * s1));
+    w[k + D / 4] = pack_bf16x2(fmaf(y0, c0, x0 * s0), fmaf(y1, c1, x1 * s1));
+  }
+}
+
+// Stores scale * R^T of one pair of 32-column chunks of a TMEM row: columns
+// 32a..32a+31 and their rotation partners D/2 further on (frequencies
+// 32a..32a+31), for the key or query at natural position pos, as bf16 at
+// dst + the same columns (every lane of the warp must call this).
+template <int D>
+__device__ __forceinline__ void store_tmem_pair_rope(uint32_t t_col0, int a, float scale, int pos,
+                                                     const RopeTheta &th, __nv_bfloat16 *dst, bool valid) {
+  uint32_t ra[32], rb[32];
+  tc::tmem_ld32(t_col0 + 32 * a, ra);
+  tc::tmem_ld32(t_col0 + 32 * a + D / 2, rb);
+  tc::tmem_ld_wait();
+  uint32_t pa[16], pb[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float o[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float sn, cs;
+      rope_sincos(pos, th.hi[32 * a + e + u], th.lo[32 * a + e + u], sn, cs);
+      const float x = __uint_as_float(ra[e + u]) * scale, y = __uint_as_float(rb[e + u]) * scale;
+      o[0][u] = fmaf(x, cs, y * sn);    // R^T: x cos + y sin
+      o[1][u] = fmaf(y, cs, -x * sn);   //      y cos - x sin
+    }
+    pa[e / 2] = pack_bf16x2(o[0][0], o[0][1]);
+    pb[e / 2] = pack_bf16x2(o[1][0], o[1][1]);
+  }
+  if (valid) {
+    uint4 *da = reinterpret_cast<uint4 *>(dst + 32 * a), *db = reinterpret_cast<uint4 *>(dst + 32 * a + D / 2);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      da[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+      db[v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
+    }
+  }
+}
+
 // ================================================================== dQ
 // Query-stationary. TMEM: Q (bf16 A operand) 0, dO 64, S 128, dP 256, dQ 384.
 // Warpgroup h owns key columns [64h, 64h+64) of each tile and writes its
@@ -60,6 +115,9 @@ __device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchu
 // its A operand from columns 256..287 then 320..351. Per key tile n the MMA
 // issuer runs S(n+1) as soon as both softmax warpgroups have read S(n), then
 // dQ(n) once dS(n) is in TMEM, then dP(n+1) once dQ(n) has consumed dS(n).
+// With in-kernel RoPE (ROPE) warpgroup 0 rotates its Q row before it goes to
+// TMEM, warps 10-11 rotate every K tile in shared memory (k_ready), and dQ
+// leaves through R^T at the query's position.
 template <int D>
 struct Dq3Cfg {
   static constexpr int NS = (D == 128) ? 3 : 4;  // K/V stages
@@ -67,16 +125,17 @@ struct Dq3Cfg {
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = NS * TILE;
   static constexpr int OFF_BAR = 2 * NS * TILE;
-  // qdo_ready, fin, s_full, dp_full, s_free, (spare), ds_ready, dq_done, kv_full[NS], kv_empty[NS]
-  static constexpr int NBAR = 8 + 2 * NS;
+  // qdo_ready, fin, s_full, dp_full, s_free, (spare), ds_ready, dq_done, kv_full[NS], kv_empty[NS],
+  // k_ready[NS]
+  static constexpr int NBAR = 8 + 3 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
   static constexpr uint32_t colQ = 0, colDO = 64, colS = 128, colDP = 256, colDQ = 384;
 };
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     dq2_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ Bwd2Params p) {
   using C = Dq3Cfg<D>;
@@ -91,6 +150,8 @@ __global__ void __launch_bounds__(320, 1)
                  bar_s_free = bar0 + 32, bar_ds_ready = bar0 + 48, bar_dq_done = bar0 + 56;
   auto bar_kv_full = [&](int st) { return bar0 + 64 + 8 * st; };
   auto bar_kv_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
+  auto bar_k_ready = [&](int st) { return bar0 + 64 + 16 * NS + 8 * st; };
+  auto bar_k_use = [&](int st) { return ROPE ? bar_k_ready(st) : bar_kv_full(st); };   // before S reads K
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
@@ -112,7 +173,9 @@ __global__ void __launch_bounds__(320, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
       const bool by_threads = b == bar_qdo || b == bar_s_free || b == bar_ds_ready;
-      tc::mbar_init(b, by_threads ? 256 : 1);
+      uint32_t cnt = by_threads ? 256 : 1;
+      if (b >= bar_k_ready(0)) cnt = 64;   // k_ready[]: the two rotation warps
+      tc::mbar_init(b, cnt);
     }
     abort_flag[0] = 0;
     abort_flag[1] = 0;
@@ -178,7 +241,7 @@ __global__ void __launch_bounds__(320, 1)
       };
       bool ok = wait_all(bar_qdo, 0, wc);
       if (ok && ntiles > 0) {
-        ok = wait_all(bar_kv_full(0), 0, wc);
+        ok = wait_all(bar_k_use(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0);
@@ -188,7 +251,7 @@ __global__ void __launch_bounds__(320, 1)
           const bool more = n + 1 < ntiles;
           const int st = n % NS, st1 = (n + 1) % NS;
           if (more) {   // S(n+1) once S(n) has been read
-            if (!(ok = wait_all(bar_kv_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_k_use(st1), ((n + 1) / NS) & 1, wc))) break;
             if (!(ok = wait_all(bar_s_free, n & 1, wc))) break;
             tc::tc_fence_after();
             issue_s(st1);
@@ -214,6 +277,18 @@ __global__ void __launch_bounds__(320, 1)
       tc::mma_commit_w(bar_fin);
       wait_all(bar_fin, 0, drain);
     }
+  } else if (ROPE && warp >= 10) {
+    // ------------------------------------------------ RoPE rotation warps (K tiles)
+    tc::RopeRows<D> rr;
+    rr.init((warp - 10) * 32 + lane, p.theta);
+    for (int n = 0; n < ntiles; ++n) {
+      decode_tile(tab[n], t);
+      const int st = n % NS;
+      if (!__all_sync(0xffffffffu, tc::mbar_wait(bar_kv_full(st), (n / NS) & 1, wc))) break;
+      rr.rotate(smem + C::OFF_K + st * C::TILE, t.pos0);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_k_ready(st));
+    }
   } else {
     // ---------------------------------------------- softmax warpgroups (key halves)
     const int h = warp >> 2;
@@ -224,17 +299,30 @@ __global__ void __launch_bounds__(320, 1)
     const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + qt * kTile + row);
     const float lse2 = valid ? p.lse[grow] * kLog2eB : INFINITY;
     const float Drow = valid ? p.D[grow] : 0.f;
-    {  // this thread's row of Q (warpgroup 0) or dO (warpgroup 1) into TMEM
+    {  // this thread's row of Q (warpgroup 0, rotated under ROPE) or dO (warpgroup 1) into TMEM
       const uint4 *src = reinterpret_cast<const uint4 *>((h == 0 ? p.q : p.dO) + grow * D);
-#pragma unroll 1
-      for (int cb = 0; cb < D / 64; ++cb) {
-        uint32_t r[32];
+      if (ROPE && h == 0) {
+        uint32_t r[D / 64][32];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = valid ? src[cb * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+        for (int v = 0; v < D / 8; ++v) {
+          const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+          uint32_t *rv = &r[v / 8][4 * (v % 8)];
+          rv[0] = x.x; rv[1] = x.y; rv[2] = x.z; rv[3] = x.w;
         }
-        tc::tmem_st32(t_row + (h == 0 ? C::colQ : C::colDO) + cb * 32, r);
+        rope_row_words<D, true>(&r[0][0], q_pos, p.theta);
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb) tc::tmem_st32(t_row + C::colQ + cb * 32, r[cb]);
+      } else {
+#pragma unroll 1
+        for (int cb = 0; cb < D / 64; ++cb) {
+          uint32_t r[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 x = valid ? src[cb * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
+            r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
+          }
+          tc::tmem_st32(t_row + (h == 0 ? C::colQ : C::colDO) + cb * 32, r);
+        }
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -310,7 +398,10 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done, (n - 1) & 1, wc));
       if (ok) {
         tc::tc_fence_after();
-        store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
+        if (!ROPE)
+          store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
+        else if (D == 128 || h == 0)   // warpgroup h: frequencies 32h..32h+31 (D = 64: warpgroup 0, all 32)
+          store_tmem_pair_rope<D>(t_row + C::colDQ, h, p.scale, q_pos, p.theta, p.dq + grow * D, valid);
       }
     } else if (ok && valid) {   // no key tile at all (rows outside every document)
       uint4 *d4 = reinterpret_cast<uint4 *>(p.dq + grow * D + h * (D / 2));
@@ -336,6 +427,9 @@ __global__ void __launch_bounds__(320, 1)
 //   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | S^T(n+1) once dV(n)
 //   has consumed P^T | dK(n) once dS^T(n) is in TMEM | dP^T(n+1) once dK(n)
 // has consumed dS^T.
+// With in-kernel RoPE (ROPE), warps 10-11 rotate the K tile once (k_ready)
+// and every Q tile in shared memory (q_ready), and dK leaves through R^T at
+// the key's position.
 template <int D>
 struct Dkdv3Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;  // Q/dO stages
@@ -346,16 +440,17 @@ struct Dkdv3Cfg {
   static constexpr int OFF_DO = OFF_Q + NS * TILE;
   static constexpr int OFF_LD = OFF_DO + NS * TILE;  // per stage: lse*log2e [128], D [128]
   static constexpr int OFF_BAR = OFF_LD + NS * 1024;
-  // kv_full, fin, s_full, dp_full, (spare), (spare), p_ready, ds_ready, dv_done, dk_done, qd_full[NS], qd_empty[NS]
-  static constexpr int NBAR = 10 + 2 * NS;
+  // kv_full, fin, s_full, dp_full, k_ready, (spare), p_ready, ds_ready, dv_done, dk_done, qd_full[NS],
+  // qd_empty[NS], q_ready[NS]
+  static constexpr int NBAR = 10 + 3 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
   static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
 };
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     dkdv2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ Bwd2Params p) {
@@ -375,6 +470,11 @@ __global__ void __launch_bounds__(320, 1)
                  bar_ds_ready = bar0 + 56, bar_dv_done = bar0 + 64, bar_dk_done = bar0 + 72;
   auto bar_qd_full = [&](int st) { return bar0 + 80 + 8 * st; };
   auto bar_qd_empty = [&](int st) { return bar0 + 80 + 8 * NS + 8 * st; };
+  const uint32_t bar_k_ready = bar0 + 32;
+  auto bar_q_ready = [&](int st) { return bar0 + 80 + 16 * NS + 8 * st; };
+  // the barriers the MMA issuer waits on before reading K and Q
+  const uint32_t bar_k_use = ROPE ? bar_k_ready : bar_kv_full;
+  auto bar_q_use = [&](int st) { return ROPE ? bar_q_ready(st) : bar_qd_full(st); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
@@ -398,8 +498,11 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t b = bar0 + 8 * i;
       uint32_t cnt = 1;
       if (b == bar_p_ready || b == bar_ds_ready) cnt = 256;
-      for (int st = 0; st < NS; ++st)
+      if (b == bar_k_ready) cnt = 64;       // the two rotation warps
+      for (int st = 0; st < NS; ++st) {
         if (b == bar_qd_full(st)) cnt = 33;   // expect_tx arrive + 32 producer lanes
+        if (b == bar_q_ready(st)) cnt = 64;
+      }
       tc::mbar_init(b, cnt);
     }
     abort_flag[0] = 0;
@@ -497,9 +600,9 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
         return __all_sync(0xffffffffu, tc::mbar_wait(bar, par, w));
       };
-      bool ok = wait_all(bar_kv_full, 0, wc);
+      bool ok = wait_all(bar_k_use, 0, wc);
       if (ok && ntot > 0) {
-        ok = wait_all(bar_qd_full(0), 0, wc);
+        ok = wait_all(bar_q_use(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0);
@@ -523,7 +626,7 @@ __global__ void __launch_bounds__(320, 1)
           // exponentials, the longest phase of a tile, while dK(n) and
           // dP^T(n+1) run.
           if (more) {
-            if (!(ok = wait_all(bar_qd_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_q_use(st1), ((n + 1) / NS) & 1, wc))) break;
             if (!(ok = wait_all(bar_dv_done, n & 1, wc))) break;   // S^T(n+1) overwrites P^T(n)
             tc::tc_fence_after();
             issue_s(st1);
@@ -547,6 +650,26 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc::mma_commit_w(bar_fin);
       wait_all(bar_fin, 0, drain);
+    }
+  } else if (ROPE && warp >= 10) {
+    // ------------------------------------------------ RoPE rotation warps (K once, Q tiles)
+    tc::RopeRows<D> rr;
+    rr.init((warp - 10) * 32 + lane, p.theta);
+    if (__all_sync(0xffffffffu, tc::mbar_wait(bar_kv_full, 0, wc))) {
+      rr.rotate(smem + C::OFF_K, k_pos0);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_k_ready);
+      int n = 0, ent = 0;
+      while (n < ntot) {
+        decode_tile(tab[ent], t);
+        const int st = n % NS;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(bar_qd_full(st), (n / NS) & 1, wc))) break;
+        rr.rotate(smem + C::OFF_Q + st * C::TILE, t.pos0);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(bar_q_ready(st));
+        ++n;
+        if (++ent == ntiles) ent = 0;
+      }
     }
   } else {
     // -------------------------------------------- softmax warpgroups (query halves)
@@ -661,7 +784,13 @@ __global__ void __launch_bounds__(320, 1)
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dk_done, (n - 1) & 1, wc));
         if (ok) {
           tc::tc_fence_after();
-          store_tmem_cols(t_row + (h == 0 ? C::colDV : C::colDK), 0, D / 32, h == 0 ? 1.f : p.scale, dst, valid);
+          if (ROPE && h == 1) {   // dK = R^T dK' at the key's position
+#pragma unroll 1
+            for (int a = 0; a < D / 64; ++a)
+              store_tmem_pair_rope<D>(t_row + C::colDK, a, p.scale, k_pos, p.theta, dst, valid);
+          } else {
+            store_tmem_cols(t_row + (h == 0 ? C::colDV : C::colDK), 0, D / 32, h == 0 ? 1.f : p.scale, dst, valid);
+          }
         }
       } else if (valid) {   // no query sees these keys (all padding): zero gradients
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -679,24 +808,25 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-template <int D>
+template <int D, bool ROPE>
 cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
+  constexpr int threads = ROPE ? 384 : 320;
   {
     constexpr int smem = Dkdv3Cfg<D>::SMEM;
-    auto kern = dkdv2_tc_kernel<D>;
+    auto kern = dkdv2_tc_kernel<D, ROPE>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
-    kern<<<grid / bp.group, 320, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
+    kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
     cpattn_status st = check_launch("tensor-core dK/dV kernel (pipelined)");
     if (st != CPATTN_OK) return st;
     trace_record(2, s);
   }
   constexpr int smem = Dq3Cfg<D>::SMEM;
-  auto kern = dq2_tc_kernel<D>;
+  auto kern = dq2_tc_kernel<D, ROPE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dQ kernel", smem);
-  kern<<<grid, 320, smem, s>>>(mk, mv, bp);
+  kern<<<grid, threads, smem, s>>>(mk, mv, bp);
   return check_launch("tensor-core dQ kernel (pipelined)");
 }
 
@@ -733,10 +863,14 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   bp.tpc = (g.c + kTile - 1) / kTile;
   bp.scale = (float)(1.0 / sqrt((double)g.d));
   bp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
+  make_rope_theta(g.d, &bp.theta);
   const long long grid = BH * 2 * g.cp * bp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
-  return g.d == 128 ? launch_bwd2_t<128>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
-                    : launch_bwd2_t<64>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
+  if (g.d == 128)
+    return g.rope ? launch_bwd2_t<128, true>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
+                  : launch_bwd2_t<128, false>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
+  return g.rope ? launch_bwd2_t<64, true>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
+                : launch_bwd2_t<64, false>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
 }
 
 }  // namespace cpattn

@@ -588,11 +588,11 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
                               float *D, const Geometry &g, cudaStream_t s) {
   (void)o;
   // Pipelined kernels with a tile table in shared memory, where the schedule fits it.
-  if (!g.rope && 2LL * g.cp * ((g.c + kTile - 1) / kTile) <= kMaxTiles)
+  if (2LL * g.cp * ((g.c + kTile - 1) / kTile) <= kMaxTiles)
     return launch_bwd2_bf16(q, k, v, lse, dO, dq, dk, dv, D, g, s);
   if (g.doc_lo)
     return fail(CPATTN_ERR_UNSUPPORTED, "packed documents need 2*cp*ceil(c/128) <= %d tiles per chunk "
-                "schedule and RoPE in the shard pass (rope=0)", kMaxTiles);
+                "schedule", kMaxTiles);
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
   const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;

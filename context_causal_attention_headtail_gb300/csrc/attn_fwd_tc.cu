@@ -329,6 +329,9 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
 //   S0(n) S1(n) | PV0(n) S0(n+1) | PV1(n) S1(n+1) | PV0(n+1) ...
 // TMEM columns: S0/P0 0, S1/P1 128, O0 256, O1 256 + D (512 allocated).
 // Warp 8: TMA producer (lane 0) and TMEM allocator; warp 9: MMA issuer.
+// With in-kernel RoPE (ROPE), warps 10-11 rotate Q0, Q1 once and every K
+// tile in shared memory between its TMA landing and its first MMA (q_ready,
+// k_ready); the issuer waits for those instead of the TMA barriers.
 template <int D>
 struct Fwd2Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;   // stages of the K ring and of the V ring
@@ -337,15 +340,16 @@ struct Fwd2Cfg {
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
   static constexpr int OFF_BAR = OFF_V + NS * TILE;
-  // q_full, fin, s_full[2], p_full[2], o_done[2], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS]
-  static constexpr int NBAR = 8 + 4 * NS;
+  // q_full, fin, s_full[2], p_full[2], o_done[2], k_full[NS], k_empty[NS], v_full[NS], v_empty[NS],
+  // q_ready, k_ready[NS]
+  static constexpr int NBAR = 9 + 5 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
 };
 
-template <int D>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     fwd2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
   using C = Fwd2Cfg<D>;
@@ -365,6 +369,11 @@ __global__ void __launch_bounds__(320, 1)
   auto bar_k_empty = [&](int st) { return bar0 + 64 + 8 * NS + 8 * st; };
   auto bar_v_full = [&](int st) { return bar0 + 64 + 16 * NS + 8 * st; };
   auto bar_v_empty = [&](int st) { return bar0 + 64 + 24 * NS + 8 * st; };
+  const uint32_t bar_q_ready = bar0 + 64 + 32 * NS;
+  auto bar_k_ready = [&](int st) { return bar0 + 72 + 32 * NS + 8 * st; };
+  // the barriers the MMA issuer waits on before reading Q and K
+  const uint32_t bar_q_use = ROPE ? bar_q_ready : bar_q_full;
+  auto bar_k_use = [&](int st) { return ROPE ? bar_k_ready(st) : bar_k_full(st); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
@@ -389,7 +398,9 @@ __global__ void __launch_bounds__(320, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
-      tc::mbar_init(b, (b == bar_p_full(0) || b == bar_p_full(1)) ? 128 : 1);
+      uint32_t cnt = (b == bar_p_full(0) || b == bar_p_full(1)) ? 128 : 1;
+      if (b >= bar_q_ready) cnt = 64;   // q_ready, k_ready[]: the two rotation warps
+      tc::mbar_init(b, cnt);
     }
     abort_flag[0] = 0;
     abort_flag[1] = 0;
@@ -467,9 +478,9 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
         return __all_sync(0xffffffffu, tc::mbar_wait(bar, par, w));
       };
-      bool ok = wait_all(bar_q_full, 0, wc);
+      bool ok = wait_all(bar_q_use, 0, wc);
       if (ok && ntiles > 0) {
-        ok = wait_all(bar_k_full(0), 0, wc);
+        ok = wait_all(bar_k_use(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
           issue_s(0, 0);
@@ -485,7 +496,7 @@ __global__ void __launch_bounds__(320, 1)
           tc::tc_fence_after();
           issue_pv(0, st, n);
           if (more) {
-            if (!(ok = wait_all(bar_k_full(st1), ((n + 1) / NS) & 1, wc))) break;
+            if (!(ok = wait_all(bar_k_use(st1), ((n + 1) / NS) & 1, wc))) break;
             if (!(ok = wait_all(bar_o_done(0), n & 1, wc))) break;
             tc::tc_fence_after();
             issue_s(0, st1);
@@ -506,6 +517,24 @@ __global__ void __launch_bounds__(320, 1)
       }
       tc::mma_commit_w(bar_fin);
       wait_all(bar_fin, 0, drain);
+    }
+  } else if (ROPE && warp >= 10) {
+    // ------------------------------------------------ RoPE rotation warps
+    tc::RopeRows<D> rr;
+    rr.init((warp - 10) * 32 + lane, p.theta);
+    if (__all_sync(0xffffffffu, tc::mbar_wait(bar_q_full, 0, wc))) {
+      rr.rotate(smem + C::OFF_Q, q_pos0);
+      rr.rotate(smem + C::OFF_Q + C::TILE, q_pos0 + kTile);
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(bar_q_ready);
+      for (int n = 0; n < ntiles; ++n) {
+        decode_tile(tab[n], t);
+        const int st = n % NS;
+        if (!__all_sync(0xffffffffu, tc::mbar_wait(bar_k_full(st), (n / NS) & 1, wc))) break;
+        rr.rotate(smem + C::OFF_K + st * C::TILE, t.pos0);
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(bar_k_ready(st));
+      }
     }
   } else {
     // ----------------------------------------------- softmax warpgroups 0, 1
@@ -680,14 +709,14 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 
 namespace {
 
-template <int D>
+template <int D, bool ROPE>
 cpattn_status launch_fwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                             const FwdParams &fp, unsigned grid, cudaStream_t s) {
   constexpr int smem = Fwd2Cfg<D>::SMEM;
-  auto kern = fwd2_tc_kernel<D>;
+  auto kern = fwd2_tc_kernel<D, ROPE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the forward kernel", smem);
-  kern<<<grid, 320, smem, s>>>(mq, mk, mv, fp);
+  kern<<<grid, ROPE ? 384 : 320, smem, s>>>(mq, mk, mv, fp);
   return check_launch("tensor-core forward kernel (paired tiles)");
 }
 
@@ -729,17 +758,21 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   fp.tpc = (g.c + kTile - 1) / kTile;
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
   make_rope_theta(g.d, &fp.theta);
-  // Paired query tiles with a tile table in shared memory; q, k are used as
-  // given. Longer schedules take the one-tile kernel below.
-  if (!g.rope && 2LL * g.cp * fp.tpc <= kMaxTiles) {
+  // Paired query tiles with a tile table in shared memory (RoPE, if asked
+  // for, rotates the tiles in shared memory). Longer schedules take the
+  // one-tile kernel below.
+  if (2LL * g.cp * fp.tpc <= kMaxTiles) {
     const long long grid2 = BH * 2 * g.cp * ((fp.tpc + 1) / 2);
     if (grid2 > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
-    return g.d == 128 ? launch_fwd2_t<128>(mq, mk, mv, fp, (unsigned)grid2, s)
-                      : launch_fwd2_t<64>(mq, mk, mv, fp, (unsigned)grid2, s);
+    if (g.d == 128)
+      return g.rope ? launch_fwd2_t<128, true>(mq, mk, mv, fp, (unsigned)grid2, s)
+                    : launch_fwd2_t<128, false>(mq, mk, mv, fp, (unsigned)grid2, s);
+    return g.rope ? launch_fwd2_t<64, true>(mq, mk, mv, fp, (unsigned)grid2, s)
+                  : launch_fwd2_t<64, false>(mq, mk, mv, fp, (unsigned)grid2, s);
   }
   if (g.doc_lo)
     return fail(CPATTN_ERR_UNSUPPORTED, "packed documents need 2*cp*ceil(c/128) <= %d tiles per chunk "
-                "schedule and RoPE in the shard pass (rope=0)", kMaxTiles);
+                "schedule", kMaxTiles);
   const long long grid = BH * 2 * g.cp * fp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
   if (g.d == 128)

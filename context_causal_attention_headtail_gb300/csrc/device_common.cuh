@@ -45,6 +45,20 @@ __device__ __forceinline__ void rope_sincos(int pos, float th_hi, float th_lo, f
   sincosf(r, &s, &c);
 }
 
+// The same reduction with the reduced angle on the MUFU sin/cos units
+// (absolute error ~2^-21 for |r| <= pi), for seeds that are recomputed often.
+__device__ __forceinline__ void rope_sincos_fast(int pos, float th_hi, float th_lo, float &s, float &c) {
+  const float p = (float)pos;
+  const float a_hi = p * th_hi;
+  const float a_lo = fmaf(p, th_hi, -a_hi) + p * th_lo;
+  const float k = rintf(a_hi * 0.159154943091895336f);
+  float r = fmaf(-k, 6.28125f, a_hi);
+  r = fmaf(-k, 1.9353071693331003e-3f, r);
+  r = fmaf(-k, 1.0253376273028358e-11f, r);
+  r += a_lo;
+  __sincosf(r, &s, &c);
+}
+
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 // Round two floats to bf16 (RNE) and pack: lo in bits 0..15, hi in 16..31.

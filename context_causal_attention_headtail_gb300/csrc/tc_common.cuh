@@ -319,6 +319,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2_2(uint64_t v) {
   return pack_bf16x2(lo, hi);
 }
 
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // ------------------------------------------------------ swizzled smem access ---
 // Byte offset of element (row, col) in a 128B-swizzled tile of R rows.
 __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int R) {
@@ -360,6 +366,84 @@ __device__ __forceinline__ void rope_tile(uint8_t *tile, int pos0, int wid, int 
     c0 = nc0; s0 = ns0; c1 = nc1; s1 = ns1;
   }
 }
+
+// Rotate-half RoPE of a 128-row, 128B-swizzled bf16 tile in place (row i at
+// natural position pos0 + i) by two warps (u = 0..63), 16 bytes at a time.
+// Thread u owns one 16-byte chunk c of the first half of every row it visits
+// and the matching chunk of the second half: the eight pairs (i, i + D/2),
+// i = 8c..8c+7, which sit at the same swizzled column in both halves for
+// D = 128 (two 64-column blocks) and four chunks apart for D = 64. It visits
+// rows r0, r0 + RS, ... (RS a multiple of 8, so the swizzle phase r & 7 is
+// fixed); a warp's 32 lanes cover four (D = 128) or eight (D = 64) whole
+// consecutive rows per step, which keeps the 16-byte accesses free of bank
+// conflicts. cos/sin are seeded per tile at row r0 and advanced row to row by
+// the exact angle-addition step of RS * theta_i.
+template <int D>
+struct RopeRows {
+  static constexpr int kRows = 128;               // rows of a tile
+  static constexpr int RS = (D == 128) ? 8 : 16;   // row stride of one thread
+  static constexpr int NI = kRows / RS;            // rows per thread per tile
+  uint32_t xoff, yoff;                             // byte offsets in row r0
+  int r0;
+  float th_hi[8], th_lo[8];
+  uint64_t cd[4], sd[4];                           // cos, sin of RS * theta, frequency pairs
+
+  __device__ __forceinline__ void init(int u, const RopeTheta &th) {
+    const int c = (D == 128) ? (u & 7) : (u & 3);
+    r0 = (D == 128) ? (u >> 3) : (u >> 2);
+    const uint32_t sw = (uint32_t)(r0 & 7);
+    xoff = (uint32_t)r0 * 128u + (((uint32_t)c ^ sw) << 4);
+    yoff = (D == 128) ? (uint32_t)kRows * 128u + xoff : (uint32_t)r0 * 128u + ((((uint32_t)c + 4u) ^ sw) << 4);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      th_hi[e] = th.hi[8 * c + e];
+      th_lo[e] = th.lo[8 * c + e];
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float s0, c0, s1, c1;
+      rope_sincos(RS, th_hi[2 * w], th_lo[2 * w], s0, c0);
+      rope_sincos(RS, th_hi[2 * w + 1], th_lo[2 * w + 1], s1, c1);
+      cd[w] = f2(c0, c1);
+      sd[w] = f2(s0, s1);
+    }
+  }
+
+  __device__ __forceinline__ void rotate(uint8_t *tile, int pos0) const {
+    uint64_t C[4], S[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float s0, c0, s1, c1;
+      rope_sincos_fast(pos0 + r0, th_hi[2 * w], th_lo[2 * w], s0, c0);
+      rope_sincos_fast(pos0 + r0, th_hi[2 * w + 1], th_lo[2 * w + 1], s1, c1);
+      C[w] = f2(c0, c1);
+      S[w] = f2(s0, s1);
+    }
+#pragma unroll 2
+    for (int j = 0; j < NI; ++j) {
+      uint4 *px = reinterpret_cast<uint4 *>(tile + xoff + (uint32_t)j * (RS * 128));
+      uint4 *py = reinterpret_cast<uint4 *>(tile + yoff + (uint32_t)j * (RS * 128));
+      const uint4 xv = *px, yv = *py;
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, yw[4] = {yv.x, yv.y, yv.z, yv.w};
+      uint32_t ox[4], oy[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint64_t X = f2(bf16lo_to_f32(xw[w]), bf16hi_to_f32(xw[w]));
+        const uint64_t Y = f2(bf16lo_to_f32(yw[w]), bf16hi_to_f32(yw[w]));
+        ox[w] = pack_bf16x2_2(fsub2(fmul2(X, C[w]), fmul2(Y, S[w])));   // x cos - y sin
+        oy[w] = pack_bf16x2_2(ffma2(X, S[w], fmul2(Y, C[w])));          // y cos + x sin
+      }
+      *px = make_uint4(ox[0], ox[1], ox[2], ox[3]);
+      *py = make_uint4(oy[0], oy[1], oy[2], oy[3]);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {   // advance to row r + RS
+        const uint64_t nc = fsub2(fmul2(C[w], cd[w]), fmul2(S[w], sd[w]));
+        S[w] = ffma2(C[w], sd[w], fmul2(S[w], cd[w]));
+        C[w] = nc;
+      }
+    }
+  }
+};
 
 }  // namespace tc
 }  // namespace cpattn
