@@ -425,17 +425,65 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const T *__restrict__ o
   }
 }
 
+// bf16 rows read as 16-byte words: DD/8 lanes share a row (16 for d = 128),
+// so a warp covers 32/(DD/8) rows per step and takes two steps per iteration
+// (four independent 16-byte loads per lane in flight); the partial dot
+// products are summed over the row's lanes with shuffles.
+template <int DD>
+__global__ void __launch_bounds__(256) preprocess_bf16_kernel(const uint4 *__restrict__ o,
+                                                              const uint4 *__restrict__ dO,
+                                                              float *__restrict__ D, long long rows) {
+  constexpr int LPR = DD / 8;    // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp step
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / LPR, w = lane % LPR;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long base = gw * (2 * RPW); base < rows; base += nw * (2 * RPW)) {
+    uint4 a[2], b[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const long long row = base + u * RPW + sub;
+      a[u] = row < rows ? o[row * LPR + w] : make_uint4(0u, 0u, 0u, 0u);
+      b[u] = row < rows ? dO[row * LPR + w] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t aw[4] = {a[u].x, a[u].y, a[u].z, a[u].w}, bw[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc = fmaf(bf16lo_to_f32(aw[k]), bf16lo_to_f32(bw[k]), acc);
+        acc = fmaf(bf16hi_to_f32(aw[k]), bf16hi_to_f32(bw[k]), acc);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      const long long row = base + u * RPW + sub;
+      if (w == 0 && row < rows) D[row] = acc;
+    }
+  }
+}
+
 cpattn_status launch_bwd_preprocess(const void *o, const void *dO, float *D, long long rows,
                                     int d, cpattn_dtype dt, cudaStream_t s) {
-  long long blocks = (rows + 7) / 8;
-  long long cap = (long long)sm_count() * 16;
-  if (blocks > cap) blocks = cap;
-  if (dt == CPATTN_F32)
+  const long long cap = (long long)sm_count() * 16;
+  if (dt == CPATTN_F32) {
+    long long blocks = (rows + 7) / 8;
+    if (blocks > cap) blocks = cap;
     preprocess_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(
         static_cast<const float *>(o), static_cast<const float *>(dO), D, rows, d);
-  else
-    preprocess_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(dO), D, rows, d);
+  } else {
+    const long long rows_per_block = 8 * 2 * (32 / (d / 8));   // 8 warps, two steps each
+    long long blocks = (rows + rows_per_block - 1) / rows_per_block;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (d == 128)
+      preprocess_bf16_kernel<128><<<(unsigned)blocks, 256, 0, s>>>(
+          static_cast<const uint4 *>(o), static_cast<const uint4 *>(dO), D, rows);
+    else
+      preprocess_bf16_kernel<64><<<(unsigned)blocks, 256, 0, s>>>(
+          static_cast<const uint4 *>(o), static_cast<const uint4 *>(dO), D, rows);
+  }
   return check_launch("backward preprocess kernel");
 }
 
