@@ -42,9 +42,9 @@ DEFAULT_WORKLOAD = "window_32k"
 # on the 32k workload (profiles/tc_kernels_window_32k.md); a kernel missing
 # here has no capture of its current version. Only valid for that workload.
 NCU_TRAFFIC_BYTES = {
-    ("window_32k", "fwd"): 2.219289e9 + 0.121222e9,
-    ("window_32k", "bwd_dkdv"): 4.114704e9 + 0.239087e9,
-    ("window_32k", "bwd_dq"): 4.067629e9 + 0.120716e9,
+    ("window_32k", "fwd"): 2.219422e9 + 0.121415e9,
+    ("window_32k", "bwd_dkdv"): 4.113598e9 + 0.239080e9,
+    ("window_32k", "bwd_dq"): 4.066322e9 + 0.120361e9,
 }
 
 
@@ -61,6 +61,39 @@ def parse_args():
     ap.add_argument("--rope-in-kernel", action="store_true",
                     help="rotate q, k inside the attention kernels (rope=1) instead of in shard/unshard")
     return ap.parse_args()
+
+
+def host_link_gbs(host_in, dev_in, host_out, dev_out, h2d_s, d2h_s, reps=2):
+    """Pinned host <-> device copy rates of this machine, measured with the e2e
+    buffers before the timed region: H2D alone, D2H alone and both at once on
+    the two copy streams (GB/s). The e2e step cannot be faster than its copies."""
+    import torch
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return time.perf_counter() - t0
+
+    def h2d():
+        with torch.cuda.stream(h2d_s):
+            for k in dev_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(d2h_s):
+            for k in dev_out:
+                host_out[k].copy_(dev_out[k], non_blocking=True)
+
+    bi = sum(t.numel() * t.element_size() for t in host_in.values())
+    bo = sum(t.numel() * t.element_size() for t in host_out.values())
+    h2d(), d2h()
+    t_in, t_out = timed(h2d), timed(d2h)
+    t_both = timed(lambda: (h2d(), d2h()))
+    return {"h2d": round(reps * bi / t_in / 1e9, 1), "d2h": round(reps * bo / t_out / 1e9, 1),
+            "both": round(reps * (bi + bo) / t_both / 1e9, 1)}
 
 
 def measured_peaks():
@@ -437,6 +470,7 @@ def run_ours(args):
         out_b = [outs_nat, {k: torch.empty_like(v) for k, v in outs_nat.items()}]
         lse_b = [lse, torch.empty_like(lse)]
         h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        link = host_link_gbs(host_in, nat_b[1], host_out, out_b[1], h2d_s, d2h_s)
         for _ in range(2):
             step()
         torch.cuda.synchronize(dev)
@@ -488,7 +522,11 @@ def run_ours(args):
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                "tokens_per_s": world * w.B * w.T_valid / (e2e_ms * 1e-3),
                "copies": "every step: inputs in, outputs out, on two copy streams overlapping the "
-                         "neighbouring steps' compute (double-buffered)"}
+                         "neighbouring steps' compute (double-buffered)",
+               "host_link_gbs": link,
+               "copy_bound_ms_per_step": round(max(h2d_bytes / (link["h2d"] * 1e9),
+                                                   d2h_bytes / (link["d2h"] * 1e9),
+                                                   (h2d_bytes + d2h_bytes) / (link["both"] * 1e9)) * 1e3, 3)}
 
     peaks = measured_peaks()
     unit_flops = w.fwd_flops() / 2.0          # one GEMM over the live causal pairs

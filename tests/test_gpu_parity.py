@@ -535,6 +535,28 @@ def test_edge_cases_full(w):
             assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
 
 
+# Schedules above the pipelined kernels' 1024-entry tile table run on the
+# one-tile kernels, which rotate Q and K themselves when asked to (rope=1).
+# One- and two-row chunks at cp > 512 exceed the table with few tokens, so the
+# whole problem is compared with the oracle in both RoPE modes.
+ONE_TILE = [
+    make_workload("one_tile_c1_pad", B=1, T=1026, T_valid=1023, H=2, d=128, cp=513, rope=True),
+    make_workload("one_tile_c2_gqa_d64", B=1, T=2080, H=2, H_kv=1, d=64, cp=520, rope=True),
+]
+
+
+@pytest.mark.parametrize("mode", ROPE_MODES)
+@pytest.mark.parametrize("w", ONE_TILE, ids=lambda w: w.name)
+def test_one_tile_kernels_full(w, mode):
+    assert 2 * w.cp * -(-w.chunk // 128) > 1024
+    inp = make_inputs(w, seed=11 + w.cp)
+    got = run_gpu(w, inp, rope_mode=mode)
+    _check_full(w, got, _oracle_full(w, inp))
+    if w.T_valid < w.T:
+        for g in ("dq", "dk", "dv"):
+            assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
+
+
 def test_one_million_tokens_sampled():
     """T = 2^20 on one head (cp = 64, c = 8192: the one-tile kernels' schedule
     of 8192 tiles per CTA): sampled rows of O, LSE and dQ against the oracle,
