@@ -59,7 +59,7 @@ typedef enum {
   CPATTN_ERR_ALIGN = 4,       /* pointer not 16-byte aligned                   */
   CPATTN_ERR_CUDA = 5,        /* a CUDA runtime call or kernel launch failed   */
   CPATTN_ERR_TIMEOUT = 6,     /* a kernel's bounded wait expired (device flag) */
-  CPATTN_ERR_UNSUPPORTED = 7  /* valid request this build does not implement   */
+  CPATTN_ERR_UNSUPPORTED = 7  /* valid request the library does not implement  */
 } cpattn_status;
 
 typedef enum { CPATTN_F32 = 0, CPATTN_BF16 = 1 } cpattn_dtype;
