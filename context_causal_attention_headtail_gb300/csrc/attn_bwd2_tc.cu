@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     }
   } else if (ROPE && warp >= 10) {
     // ------------------------------------------------ RoPE rotation warps (K tiles)
-    tc::RopeRows<D> rr;
+    tc::RopeRows<D, 64> rr;   // warps 10-11
     rr.init((warp - 10) * 32 + lane, p.theta);
     for (int n = 0; n < ntiles; ++n) {
       decode_tile(tab[n], t);
@@ -653,7 +653,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     }
   } else if (ROPE && warp >= 10) {
     // ------------------------------------------------ RoPE rotation warps (K once, Q tiles)
-    tc::RopeRows<D> rr;
+    tc::RopeRows<D, 64> rr;   // warps 10-11
     rr.init((warp - 10) * 32 + lane, p.theta);
     if (__all_sync(0xffffffffu, tc::mbar_wait(bar_kv_full, 0, wc))) {
       rr.rotate(smem + C::OFF_K, k_pos0);

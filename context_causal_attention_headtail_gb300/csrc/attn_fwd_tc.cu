@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     }
   } else if (ROPE && warp >= 10) {
     // ------------------------------------------------ RoPE rotation warps
-    tc::RopeRows<D> rr;
+    tc::RopeRows<D, 64> rr;   // warps 10-11
     rr.init((warp - 10) * 32 + lane, p.theta);
     if (__all_sync(0xffffffffu, tc::mbar_wait(bar_q_full, 0, wc))) {
       rr.rotate(smem + C::OFF_Q, q_pos0);

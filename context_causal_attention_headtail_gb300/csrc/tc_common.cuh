@@ -368,29 +368,32 @@ __device__ __forceinline__ void rope_tile(uint8_t *tile, int pos0, int wid, int 
 }
 
 // Rotate-half RoPE of a 128-row, 128B-swizzled bf16 tile in place (row i at
-// natural position pos0 + i) by two warps (u = 0..63), 16 bytes at a time.
+// natural position pos0 + i) by NT threads (u = 0..NT-1), 16 bytes at a time.
 // Thread u owns one 16-byte chunk c of the first half of every row it visits
 // and the matching chunk of the second half: the eight pairs (i, i + D/2),
 // i = 8c..8c+7, which sit at the same swizzled column in both halves for
 // D = 128 (two 64-column blocks) and four chunks apart for D = 64. It visits
-// rows r0, r0 + RS, ... (RS a multiple of 8, so the swizzle phase r & 7 is
-// fixed); a warp's 32 lanes cover four (D = 128) or eight (D = 64) whole
-// consecutive rows per step, which keeps the 16-byte accesses free of bank
-// conflicts. cos/sin are seeded per tile at row r0 and advanced row to row by
-// the exact angle-addition step of RS * theta_i.
-template <int D>
+// rows r0, r0 + RS, ... below 128 (RS = NT / chunks per row, a multiple of 8,
+// so the swizzle phase r & 7 is fixed); a warp's 32 lanes cover four (D = 128)
+// or eight (D = 64) whole consecutive rows per step, which keeps the 16-byte
+// accesses free of bank conflicts. cos/sin are seeded per tile at row r0 and
+// advanced row to row by the exact angle-addition step of RS * theta_i.
+template <int D, int NT>
 struct RopeRows {
   static constexpr int kRows = 128;               // rows of a tile
-  static constexpr int RS = (D == 128) ? 8 : 16;   // row stride of one thread
-  static constexpr int NI = kRows / RS;            // rows per thread per tile
-  uint32_t xoff, yoff;                             // byte offsets in row r0
+  static constexpr int CPR = (D == 128) ? 8 : 4;  // chunks per row owned (first half)
+  static constexpr int RS = NT / CPR;             // row stride of one thread
+  static constexpr int NI = kRows / RS;           // rows per thread per tile
+  static_assert(NT % (CPR * 8) == 0 && NT % 32 == 0, "row stride must keep the swizzle phase");
+  static_assert(kRows % RS == 0, "every thread visits the same number of rows");
+  uint32_t xoff, yoff;                            // byte offsets in row r0
   int r0;
   float th_hi[8], th_lo[8];
-  uint64_t cd[4], sd[4];                           // cos, sin of RS * theta, frequency pairs
+  uint64_t cd[4], sd[4];                          // cos, sin of RS * theta, frequency pairs
 
   __device__ __forceinline__ void init(int u, const RopeTheta &th) {
-    const int c = (D == 128) ? (u & 7) : (u & 3);
-    r0 = (D == 128) ? (u >> 3) : (u >> 2);
+    const int c = u % CPR;
+    r0 = u / CPR;
     const uint32_t sw = (uint32_t)(r0 & 7);
     xoff = (uint32_t)r0 * 128u + (((uint32_t)c ^ sw) << 4);
     yoff = (D == 128) ? (uint32_t)kRows * 128u + xoff : (uint32_t)r0 * 128u + ((((uint32_t)c + 4u) ^ sw) << 4);
@@ -436,7 +439,7 @@ struct RopeRows {
       *px = make_uint4(ox[0], ox[1], ox[2], ox[3]);
       *py = make_uint4(oy[0], oy[1], oy[2], oy[3]);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {   // advance to row r + RS
+      for (int w = 0; w < 4; ++w) {   // advance to row + RS
         const uint64_t nc = fsub2(fmul2(C[w], cd[w]), fmul2(S[w], sd[w]));
         S[w] = ffma2(C[w], sd[w], fmul2(S[w], cd[w]));
         C[w] = nc;
