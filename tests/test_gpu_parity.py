@@ -420,10 +420,11 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
 
 
 @pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
-                                       ("long_16k", "shard"), ("window_32k", "shard"),
-                                       ("window_32k", "kernel"), ("padded_12289", "shard"),
-                                       ("gqa_32k", "shard"), ("yarn_32k", "shard"),
-                                       ("varlen_32k", "shard")])
+                                       ("long_16k", "shard"), ("long_16k", "kernel"),
+                                       ("window_32k", "shard"), ("window_32k", "kernel"),
+                                       ("padded_12289", "shard"), ("padded_12289", "kernel"),
+                                       ("gqa_32k", "shard"), ("gqa_32k", "kernel"),
+                                       ("yarn_32k", "shard"), ("varlen_32k", "shard")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])
