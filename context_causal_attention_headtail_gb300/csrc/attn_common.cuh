@@ -124,26 +124,27 @@ struct GroupQSchedule {
 // QSchedule enumerate: groups (step s, half) in ring order, and inside a
 // group the live tiles form one contiguous range, found in closed form.
 // A kernel that uses a table runs only when 2*cp*tiles_per_chunk <= kMaxTiles,
-// so both the tile index and the slot fit in 10 bits.
-constexpr int kMaxTiles = 1024;   // entries per CTA (8 KiB of shared memory)
+// so the tile index in its chunk fits in 10 bits (tiles_per_chunk <= 1024)
+// and the slot 2r + half in 11 bits (2*cp <= 2048).
+constexpr int kMaxTiles = 2048;   // entries per CTA (16 KiB of shared memory)
 
 struct TileEntry {
   int pos0;
-  uint32_t packed;   // bits 0-9 tile index in chunk, 10-19 slot, 20-26 nvalid-1, 31 need_mask
+  uint32_t packed;   // bits 0-9 tile index in chunk, 10-20 slot, 21-27 nvalid-1, 31 need_mask
 };
 
 __device__ __forceinline__ void decode_tile(const TileEntry &e, TileInfo &t) {
   t.pos0 = e.pos0;
   t.y0 = (int)(e.packed & 0x3ffu) * kTile;
-  t.slot = (int)((e.packed >> 10) & 0x3ffu);
-  t.nvalid = (int)((e.packed >> 20) & 0x7fu) + 1;
+  t.slot = (int)((e.packed >> 10) & 0x7ffu);
+  t.nvalid = (int)((e.packed >> 21) & 0x7fu) + 1;
   t.need_mask = (int)(e.packed >> 31);
 }
 
 __device__ __forceinline__ TileEntry encode_tile(int pos0, int kt, int slot, int nv, int need_mask) {
   TileEntry e;
   e.pos0 = pos0;
-  e.packed = (uint32_t)kt | ((uint32_t)slot << 10) | ((uint32_t)(nv - 1) << 20) | ((uint32_t)need_mask << 31);
+  e.packed = (uint32_t)kt | ((uint32_t)slot << 10) | ((uint32_t)(nv - 1) << 21) | ((uint32_t)need_mask << 31);
   return e;
 }
 

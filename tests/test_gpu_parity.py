@@ -162,7 +162,7 @@ def test_doc_bounds_rejects_a_bad_list():
 
 
 def test_varlen_long_schedule_is_refused():
-    w = make_workload("long_varlen", B=1, T=2 * 128 * 513, H=1, d=64, cp=128, doc_len=(100, 5000))
+    w = make_workload("long_varlen", B=1, T=2 * 256 * 513, H=1, d=64, cp=256, doc_len=(100, 5000))
     inp = make_inputs(w, seed=1)
     with pytest.raises(cpattn.CpattnError) as e:
         run_gpu(w, inp)
@@ -450,9 +450,9 @@ def test_workload_full_size_sampled(name, mode):
 
 
 # Schedules longer than the pipelined kernels' shared-memory tile table
-# (2*cp*ceil(c/128) > 1024 entries) run on the one-tile kernels. cp=128 and
-# c=513 give 1280 entries per CTA, and every chunk ends in a one-row tile.
-LONG_SCHEDULE = dict(B=1, T=2 * 128 * 513, H=1, d=64, cp=128, rope=False)
+# (2*cp*ceil(c/128) > 2048 entries) run on the one-tile kernels. cp=256 and
+# c=513 give 2560 entries per CTA, and every chunk ends in a one-row tile.
+LONG_SCHEDULE = dict(B=1, T=2 * 256 * 513, H=1, d=64, cp=256, rope=False)
 
 
 def test_long_schedule_sampled_rows():
@@ -536,20 +536,38 @@ def test_edge_cases_full(w):
             assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g
 
 
-# Schedules above the pipelined kernels' 1024-entry tile table run on the
+# Schedules above the pipelined kernels' 2048-entry tile table run on the
 # one-tile kernels, which rotate Q and K themselves when asked to (rope=1).
-# One- and two-row chunks at cp > 512 exceed the table with few tokens, so the
-# whole problem is compared with the oracle in both RoPE modes.
+# One- and two-row chunks at cp > 1024 exceed the table with few tokens, so the
+# whole problem is compared with the oracle in both RoPE modes. Between 1024
+# and 2048 entries (cp > 512 with one- and two-row chunks) the pipelined
+# kernels run with slots above 1023, the top of the table's slot field.
 ONE_TILE = [
-    make_workload("one_tile_c1_pad", B=1, T=1026, T_valid=1023, H=2, d=128, cp=513, rope=True),
-    make_workload("one_tile_c2_gqa_d64", B=1, T=2080, H=2, H_kv=1, d=64, cp=520, rope=True),
+    make_workload("one_tile_c1_pad", B=1, T=2050, T_valid=2047, H=2, d=128, cp=1025, rope=True),
+    make_workload("one_tile_c2_gqa_d64", B=1, T=4160, H=2, H_kv=1, d=64, cp=1040, rope=True),
 ]
+WIDE_TABLE = [
+    make_workload("wide_table_c1_pad", B=1, T=1026, T_valid=1023, H=2, d=128, cp=513, rope=True),
+    make_workload("wide_table_c2_gqa_d64", B=1, T=2080, H=2, H_kv=1, d=64, cp=520, rope=True,
+                  doc_len=(1, 300), doc_seed=6),
+]
+
+
+@pytest.mark.parametrize("mode", ROPE_MODES)
+@pytest.mark.parametrize("w", WIDE_TABLE, ids=lambda w: w.name)
+def test_wide_tile_tables_full(w, mode):
+    assert 1024 < 2 * w.cp * -(-w.chunk // 128) <= 2048
+    if mode == "kernel" and w.packed:
+        pytest.skip("packed documents take RoPE from the shard / unshard passes")
+    inp = make_inputs(w, seed=13 + w.cp)
+    got = run_gpu(w, inp, rope_mode=mode)
+    _check_full(w, got, _oracle_full(w, inp))
 
 
 @pytest.mark.parametrize("mode", ROPE_MODES)
 @pytest.mark.parametrize("w", ONE_TILE, ids=lambda w: w.name)
 def test_one_tile_kernels_full(w, mode):
-    assert 2 * w.cp * -(-w.chunk // 128) > 1024
+    assert 2 * w.cp * -(-w.chunk // 128) > 2048
     inp = make_inputs(w, seed=11 + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     _check_full(w, got, _oracle_full(w, inp))
