@@ -63,19 +63,22 @@ def parse_args():
     return ap.parse_args()
 
 
-def host_link_gbs(host_in, dev_in, host_out, dev_out, h2d_s, d2h_s, reps=2):
+def host_link_gbs(host_in, dev_in, host_out, dev_out, h2d_s, d2h_s, reps=3):
     """Pinned host <-> device copy rates of this machine, measured with the e2e
     buffers before the timed region: H2D alone, D2H alone and both at once on
-    the two copy streams (GB/s). The e2e step cannot be faster than its copies."""
+    the two copy streams (GB/s, the best of a few rounds after a warm-up round).
+    The e2e step cannot be faster than its copies."""
     import torch
 
-    def timed(fn):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+    def best(fn):
+        times = []
         for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
             fn()
-        torch.cuda.synchronize()
-        return time.perf_counter() - t0
+            torch.cuda.synchronize()
+            times.append(time.perf_counter() - t0)
+        return min(times)
 
     def h2d():
         with torch.cuda.stream(h2d_s):
@@ -90,10 +93,11 @@ def host_link_gbs(host_in, dev_in, host_out, dev_out, h2d_s, d2h_s, reps=2):
     bi = sum(t.numel() * t.element_size() for t in host_in.values())
     bo = sum(t.numel() * t.element_size() for t in host_out.values())
     h2d(), d2h()
-    t_in, t_out = timed(h2d), timed(d2h)
-    t_both = timed(lambda: (h2d(), d2h()))
-    return {"h2d": round(reps * bi / t_in / 1e9, 1), "d2h": round(reps * bo / t_out / 1e9, 1),
-            "both": round(reps * (bi + bo) / t_both / 1e9, 1)}
+    torch.cuda.synchronize()
+    t_in, t_out = best(h2d), best(d2h)
+    t_both = best(lambda: (h2d(), d2h()))
+    return {"h2d": round(bi / t_in / 1e9, 1), "d2h": round(bo / t_out / 1e9, 1),
+            "both": round((bi + bo) / t_both / 1e9, 1)}
 
 
 def measured_peaks():
