@@ -32,6 +32,7 @@ struct BwdParams {
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
   int group;   // query heads per K/V head
+  const int *doc_lo, *doc_hi;   // packed documents: [T] bounds per natural position, or nullptr
   float scale;       // 1/sqrt(d)
   float scale_log2;  // log2(e)/sqrt(d)
   RopeTheta theta;
@@ -169,7 +170,11 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
   GroupQSchedule sched;
-  sched.init(p.group, cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1);
+  {
+    const QBounds qb = q_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, k_pos0, k_pos0 + k_rows - 1);
+    sched.init(p.group, cp, c, rk, p.causal, p.T_valid, k_pos0, k_pos0 + k_rows - 1, qb.q_lo, qb.q_hi,
+               qb.doc_lo_max, qb.doc_hi_min);
+  }
   const int k_ragged = k_rows < kTile;
   TileInfo t;
 
@@ -260,6 +265,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     const int k_pos = k_pos0 + row;
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this key's document [dlo, dhi) (everything without packed documents)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(k_pos, p.T - 1), p.T, dlo, dhi);
     int n = 0;
     bool ok = true;
     while (sched.next(t, k_ragged)) {
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
             float pr = exp2f(fmaf(__uint_as_float(rs[2 * e + h]), sl2, -sl[q]));
             if (t.need_mask) {
               const int q_pos = t.pos0 + q;
-              if ((p.causal && k_pos > q_pos) || k_pos >= p.T_valid) pr = 0.f;
+              if ((p.causal && k_pos > q_pos) || k_pos >= p.T_valid || q_pos < dlo || q_pos >= dhi) pr = 0.f;
             }
             pv[h] = pr;
             dsv[h] = pr * (__uint_as_float(rd[2 * e + h]) - sd[q]);
@@ -418,7 +425,11 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
   KvSchedule sched;
-  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
+  {
+    const KvBounds kb = kv_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, q_pos0, q_pos0 + q_rows - 1);
+    sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, kb.key_lo, kb.key_hi,
+               kb.doc_lo_max, kb.doc_hi_min);
+  }
   TileInfo t;
 
   if (warp == 4) {
@@ -484,6 +495,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     const float Drow = valid ? p.D[grow] : 0.f;
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this row's document [dlo, dhi) (everything without packed documents)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(q_pos, p.T - 1), p.T, dlo, dhi);
     int n = 0;
     bool ok = true;
     while (sched.next(t)) {
@@ -506,7 +519,7 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
             float pr = exp2f(fmaf(__uint_as_float(rs[2 * e + h]), sl2, -lse2));
             if (t.need_mask) {
               const int kp = t.pos0 + j;
-              if (j >= t.nvalid || kp >= p.T_valid || (p.causal && kp > q_pos)) pr = 0.f;
+              if (j >= t.nvalid || kp >= p.T_valid || (p.causal && kp > q_pos) || kp < dlo || kp >= dhi) pr = 0.f;
             }
             dsv[h] = pr * (__uint_as_float(rd[2 * e + h]) - Drow);
           }
@@ -525,6 +538,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         tc::tc_fence_after();
         epilogue_row<D, ROPE>(t_row + colDQ, p.scale, q_pos, p.theta, p.out0 + grow * D, valid);
       }
+    } else if (ok && valid) {   // no key tile at all (rows outside every document)
+      store_zero_row<D>(p.out0 + grow * D);
     }
   } else if (ROPE) {
     const int wid = warp - 6;
@@ -590,9 +605,6 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
   // Pipelined kernels with a tile table in shared memory, where the schedule fits it.
   if (2LL * g.cp * ((g.c + kTile - 1) / kTile) <= kMaxTiles)
     return launch_bwd2_bf16(q, k, v, lse, dO, dq, dk, dv, D, g, s);
-  if (g.doc_lo)
-    return fail(CPATTN_ERR_UNSUPPORTED, "packed documents need 2*cp*ceil(c/128) <= %d tiles per chunk "
-                "schedule", kMaxTiles);
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
   const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;
@@ -607,6 +619,8 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
   bp.err = device_err_flag();
   bp.BH = (int)BH;
   bp.group = g.H / g.Hkv;
+  bp.doc_lo = g.doc_lo;
+  bp.doc_hi = g.doc_hi;
   bp.T = g.T;
   bp.T_valid = g.T_valid;
   bp.c = g.c;

@@ -22,15 +22,20 @@ struct TileInfo {
 // [qmin, qmax], the K/V tiles it attends to, in ring order: step s visits
 // rank j = (r - s) mod cp (Claude Logs, 2026-03-20 ring; 2026-06-17 shapes),
 // its head chunk then its tail chunk. Tiles wholly above the causal diagonal
-// or wholly at positions >= T_valid are skipped.
+// or wholly at positions >= T_valid are skipped, and with packed documents
+// those wholly outside the keys [key_lo, key_hi] the tile's queries may see;
+// a tile reaching before doc_lo_max or past doc_hi_min needs the element mask.
 struct KvSchedule {
   int cp, c, tpc, r, causal, T_valid, qmin, qmax;
+  int key_lo, key_hi, doc_lo_max, doc_hi_min;
   int s, half, kt;
 
   __device__ __forceinline__ void init(int cp_, int c_, int r_, int causal_, int T_valid_,
-                                       int qmin_, int qmax_) {
+                                       int qmin_, int qmax_, int key_lo_ = 0, int key_hi_ = 0x7fffffff,
+                                       int doc_lo_max_ = 0, int doc_hi_min_ = 0x7fffffff) {
     cp = cp_; c = c_; tpc = (c_ + kTile - 1) / kTile; r = r_; causal = causal_;
     T_valid = T_valid_; qmin = qmin_; qmax = qmax_;
+    key_lo = key_lo_; key_hi = key_hi_; doc_lo_max = doc_lo_max_; doc_hi_min = doc_hi_min_;
     s = 0; half = 0; kt = -1;
   }
   __device__ __forceinline__ bool next(TileInfo &t) {
@@ -45,11 +50,13 @@ struct KvSchedule {
       if (pos0 >= T_valid) continue;
       if (causal && pos0 > qmax) continue;
       const int nv = min(kTile, c - kt * kTile);
+      if (pos0 > key_hi || pos0 + nv - 1 < key_lo) continue;
       t.slot = 2 * j + half;
       t.y0 = kt * kTile;
       t.pos0 = pos0;
       t.nvalid = nv;
-      t.need_mask = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > qmin);
+      t.need_mask = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > qmin) ||
+                    (pos0 < doc_lo_max) || (pos0 + nv > doc_hi_min);
       return true;
     }
   }
@@ -61,17 +68,22 @@ struct KvSchedule {
 // Logs, 2026-06-22: the dK/dV accumulator travels with K/V around the ring).
 struct QSchedule {
   int cp, c, tpc, j, causal, kmin, kmax, kvalid_max;
+  int q_lo, q_hi, doc_lo_max, doc_hi_min;
   int s, half, qt;
 
   __device__ __forceinline__ void init(int cp_, int c_, int j_, int causal_, int T_valid_,
-                                       int kmin_, int kmax_) {
+                                       int kmin_, int kmax_, int q_lo_ = -0x7fffffff, int q_hi_ = 0x7fffffff,
+                                       int doc_lo_max_ = 0, int doc_hi_min_ = 0x7fffffff) {
     cp = cp_; c = c_; tpc = (c_ + kTile - 1) / kTile; j = j_; causal = causal_;
     kmin = kmin_; kmax = kmax_;
     kvalid_max = T_valid_;
+    q_lo = q_lo_; q_hi = q_hi_; doc_lo_max = doc_lo_max_; doc_hi_min = doc_hi_min_;
     s = 0; half = 0; qt = -1;
   }
   // need_mask is set when any pair of the tile may be masked: causal
-  // overlap, a ragged query or key tile, or keys at positions >= T_valid.
+  // overlap, a ragged query or key tile, keys at positions >= T_valid, or
+  // (packed documents) queries outside the document of some key. Query tiles
+  // wholly outside [q_lo, q_hi] see none of the keys and are skipped.
   __device__ __forceinline__ bool next(TileInfo &t, int k_ragged) {
     while (true) {
       if (++qt >= tpc) {
@@ -84,11 +96,13 @@ struct QSchedule {
       const int nv = min(kTile, c - qt * kTile);
       if (causal && pos0 + nv - 1 < kmin) continue;   // every query before every key
       if (kmin >= kvalid_max) continue;               // keys all padding
+      if (pos0 > q_hi || pos0 + nv - 1 < q_lo) continue;
       t.slot = 2 * r + half;
       t.y0 = qt * kTile;
       t.pos0 = pos0;
       t.nvalid = nv;
-      t.need_mask = (nv < kTile) || k_ragged || (kmax >= kvalid_max) || (causal && kmax > pos0);
+      t.need_mask = (nv < kTile) || k_ragged || (kmax >= kvalid_max) || (causal && kmax > pos0) ||
+                    (pos0 < doc_lo_max) || (pos0 + nv > doc_hi_min);
       return true;
     }
   }
@@ -102,10 +116,11 @@ struct GroupQSchedule {
   int group, gi;
 
   __device__ __forceinline__ void init(int group_, int cp_, int c_, int j_, int causal_, int T_valid_,
-                                       int kmin_, int kmax_) {
+                                       int kmin_, int kmax_, int q_lo_ = -0x7fffffff, int q_hi_ = 0x7fffffff,
+                                       int doc_lo_max_ = 0, int doc_hi_min_ = 0x7fffffff) {
     group = group_;
     gi = 0;
-    q.init(cp_, c_, j_, causal_, T_valid_, kmin_, kmax_);
+    q.init(cp_, c_, j_, causal_, T_valid_, kmin_, kmax_, q_lo_, q_hi_, doc_lo_max_, doc_hi_min_);
   }
   __device__ __forceinline__ bool next(TileInfo &t, int k_ragged) {
     while (!q.next(t, k_ragged)) {

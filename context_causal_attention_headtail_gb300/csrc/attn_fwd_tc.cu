@@ -112,7 +112,11 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
   const tc::WaitCtx wc{abort_flag, p.err};
 
   KvSchedule sched;
-  sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1);
+  {
+    const KvBounds kb = kv_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, q_pos0, q_pos0 + q_rows - 1);
+    sched.init(cp, c, rq, p.causal, p.T_valid, q_pos0, q_pos0 + q_rows - 1, kb.key_lo, kb.key_hi,
+               kb.doc_lo_max, kb.doc_hi_min);
+  }
   TileInfo t;
 
   if (warp == 4) {
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
     const int q_pos = q_pos0 + row;
     const uint32_t t_row = tmem + ((uint32_t)(warp * 32) << 16);
     const float sl2 = p.scale_log2;
+    int dlo, dhi;   // this row's document [dlo, dhi) (everything without packed documents)
+    doc_bounds_at(p.doc_lo, p.doc_hi, min(q_pos, p.T - 1), p.T, dlo, dhi);
     float m_run = -INFINITY, l = 0.f;
     int n = 0;
     bool ok = true;
@@ -210,7 +216,8 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
           float v = __uint_as_float(r[e]);
           if (t.need_mask) {
             const int j = cb * 32 + e, kp = t.pos0 + j;
-            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v = -INFINITY;
+            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos) && kp >= dlo && kp < dhi))
+              v = -INFINITY;
           }
           mt = fmaxf(mt, v);
         }
@@ -253,8 +260,11 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
           float v0 = __uint_as_float(r[2 * e]), v1 = __uint_as_float(r[2 * e + 1]);
           if (t.need_mask) {
             const int j = cb * 32 + 2 * e, kp = t.pos0 + j;
-            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos))) v0 = -INFINITY;
-            if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos))) v1 = -INFINITY;
+            if (!((j < t.nvalid) && (kp < p.T_valid) && (!p.causal || kp <= q_pos) && kp >= dlo && kp < dhi))
+              v0 = -INFINITY;
+            if (!((j + 1 < t.nvalid) && (kp + 1 < p.T_valid) && (!p.causal || kp + 1 <= q_pos) && kp + 1 >= dlo &&
+                  kp + 1 < dhi))
+              v1 = -INFINITY;
           }
           pk[e] = pack_bf16x2(exp2f(fmaf(v0, sl2, -m_use)), exp2f(fmaf(v1, sl2, -m_use)));
           l += bf16lo_to_f32(pk[e]) + bf16hi_to_f32(pk[e]);
@@ -291,6 +301,12 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
         }
         if (valid) p.lse[grow] = l > 0.f ? (m_run + log2f(l)) * 0.693147180559945309f : -INFINITY;
       }
+    } else if (ok && row < q_rows) {   // no key tile at all (rows outside every document)
+      const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + qt * kTile + row);
+      uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
+#pragma unroll 1
+      for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[grow] = -INFINITY;
     }
   } else if (ROPE) {
     // ------------------------------------------------ RoPE transform warps
@@ -770,9 +786,6 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
     return g.rope ? launch_fwd2_t<64, true>(mq, mk, mv, fp, (unsigned)grid2, s)
                   : launch_fwd2_t<64, false>(mq, mk, mv, fp, (unsigned)grid2, s);
   }
-  if (g.doc_lo)
-    return fail(CPATTN_ERR_UNSUPPORTED, "packed documents need 2*cp*ceil(c/128) <= %d tiles per chunk "
-                "schedule", kMaxTiles);
   const long long grid = BH * 2 * g.cp * fp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
   if (g.d == 128)

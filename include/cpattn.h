@@ -206,9 +206,10 @@ cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const 
  * with that same-document condition, rope = 0 (rotate q, k with
  * cpattn_shard_rope: scores inside one document depend only on position
  * differences, so global positions give the per-document result), and
- * T_valid = cu[n_docs] (any T_valid >= it gives the same result). bf16
- * needs 2*cp*ceil(T/(2*cp*128)) <= 2048, else CPATTN_ERR_UNSUPPORTED; fp32
- * has no limit. doc_lo / doc_hi are read during the kernels only. */
+ * T_valid = cu[n_docs] (any T_valid >= it gives the same result). Any
+ * schedule length (the bf16 kernels past 2*cp*ceil(T/(2*cp*128)) = 2048 tiles
+ * per CTA are the one-tile ones). doc_lo / doc_hi are read during the kernels
+ * only. */
 cpattn_status cpattn_doc_bounds(const int32_t *cu_seqlens, int n_docs, int T, int32_t *doc_lo,
                                 int32_t *doc_hi, cpattn_stream_t stream);
 cpattn_status cpattn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
