@@ -19,7 +19,7 @@ from context_causal_attention_headtail_gb300.synth import SEEDS, WORKLOADS, make
 from oracle import attention as A
 from oracle import headtail as HT
 
-from harness import (TOL, compare, gpu_rope_cfg, oracle_docs, oracle_rope, run_gpu, run_gpu_ulysses,
+from harness import (TOL, compare, oracle_docs, oracle_rope, run_gpu, run_gpu_ulysses,
                      sample_rows, to_seq_shards)
 from oracle import ulysses as U
 
