@@ -378,8 +378,8 @@ def run_ours(args):
     # and dq, dk (default), or applied inside the attention kernels.
     fused = w.rope and not args.rope_in_kernel
     rope_flag = w.rope and not fused
-    if w.yarn and not fused:
-        raise SystemExit("YaRN RoPE runs in the shard / unshard passes; drop --rope-in-kernel")
+    if w.packed and not fused and w.rope:
+        raise SystemExit("packed documents take RoPE from the shard / unshard passes; drop --rope-in-kernel")
     rope_cfg = (cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original)
                 if w.yarn else None)
     docs = cu_dev = cu_host = None
@@ -404,11 +404,11 @@ def run_ours(args):
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["fwd"]])
         cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, cp_attn, w.T_valid, w.causal, rope_flag, stream,
-                   docs=docs)
+                   docs=docs, rope_cfg=rope_cfg if rope_flag else None)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["bwd"]])
         cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
-                   w.causal, rope_flag, stream, docs=docs)
+                   w.causal, rope_flag, stream, docs=docs, rope_cfg=rope_cfg if rope_flag else None)
         for i, name in enumerate(("o", "dq", "dk", "dv")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])

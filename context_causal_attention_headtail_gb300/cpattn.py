@@ -25,7 +25,7 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
            "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
            "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen", "cpattn_ulysses_a2a",
-           "cpattn_ulysses_a2a_rope")
+           "cpattn_ulysses_a2a_rope", "cpattn_fwd_rope_cfg", "cpattn_bwd_rope_cfg")
 
 
 class CpattnError(RuntimeError):
@@ -69,6 +69,8 @@ def _declare(lib):
         "cpattn_shard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
         "cpattn_unshard_rope_cfg": [_vp, _vp, _i, _i, _i, _i, _i, _i, _c.POINTER(RopeCfg), _vp],
         "cpattn_bwd_gqa": [_vp] * 10 + [_i] * 10 + [_vp],
+        "cpattn_fwd_rope_cfg": [_vp] * 5 + [_i] * 8 + [_c.POINTER(RopeCfg), _i, _vp],
+        "cpattn_bwd_rope_cfg": [_vp] * 10 + [_i] * 8 + [_c.POINTER(RopeCfg), _i, _vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
@@ -158,6 +160,18 @@ def cpattn_fwd_varlen(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, do
                       stream=None):
     _check(lib().cpattn_fwd_varlen(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, doc_lo,
                                    doc_hi, dt, stream))
+
+
+def cpattn_fwd_rope_cfg(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, cfg, dt, stream=None):
+    _check(lib().cpattn_fwd_rope_cfg(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal,
+                                     None if cfg is None else ctypes.byref(cfg), dt, stream))
+
+
+def cpattn_bwd_rope_cfg(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp,
+                        causal, cfg, dt, stream=None):
+    _check(lib().cpattn_bwd_rope_cfg(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv,
+                                     d, cp, causal, None if cfg is None else ctypes.byref(cfg), dt,
+                                     stream))
 
 
 def cpattn_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, stream=None):
@@ -315,9 +329,11 @@ def _torch():
     return torch
 
 
-def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None, docs=None):
+def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None, docs=None,
+        rope_cfg: RopeCfg | None = None):
     """o, lse = attention(q, k, v); k, v may have fewer heads than q (grouped K/V);
-    docs = (doc_lo, doc_hi) from doc_bounds restricts attention to documents."""
+    docs = (doc_lo, doc_hi) from doc_bounds restricts attention to documents;
+    rope=True rotates q, k inside the kernels, with rope_cfg (YaRN) when given."""
     B, H, T, d = q.shape
     H_kv = _kv_heads(q, k, v)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, T, T if T_valid is None else T_valid)
@@ -327,6 +343,9 @@ def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None,
         cpattn_fwd_varlen(*args, H, H_kv, d, cp, int(causal), _ptr(docs[0]), _ptr(docs[1]),
                           _dtype_code(q), _stream(stream))
         return
+    if rope and rope_cfg is not None:
+        cpattn_fwd_rope_cfg(*args, H, H_kv, d, cp, int(causal), rope_cfg, _dtype_code(q), _stream(stream))
+        return
     tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
     if H_kv == H:
         cpattn_fwd(*args, H, *tail)
@@ -335,9 +354,9 @@ def fwd(q, k, v, o, lse, cp, T_valid=None, causal=True, rope=False, stream=None,
 
 
 def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=True, rope=False,
-        stream=None, docs=None):
+        stream=None, docs=None, rope_cfg: RopeCfg | None = None):
     """dq, dk, dv of sum(dO * o); k, v, dk, dv may have fewer heads than q;
-    docs as for fwd."""
+    docs, rope and rope_cfg as for fwd."""
     B, H, T, d = q.shape
     H_kv = _kv_heads(q, k, v, dk, dv)
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk), _ptr(dv),
@@ -347,6 +366,9 @@ def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=Tru
             raise CpattnError(ERR_ARG, "packed documents take RoPE from shard_rope (rope=False)")
         cpattn_bwd_varlen(*args, H, H_kv, d, cp, int(causal), _ptr(docs[0]), _ptr(docs[1]),
                           _dtype_code(q), _stream(stream))
+        return
+    if rope and rope_cfg is not None:
+        cpattn_bwd_rope_cfg(*args, H, H_kv, d, cp, int(causal), rope_cfg, _dtype_code(q), _stream(stream))
         return
     tail = (d, cp, int(causal), int(rope), _dtype_code(q), _stream(stream))
     if H_kv == H:

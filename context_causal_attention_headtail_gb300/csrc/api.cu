@@ -328,7 +328,7 @@ cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, f
 static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
                               int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
-                              cpattn_stream_t stream);
+                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg = nullptr);
 
 cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
@@ -346,10 +346,21 @@ cpattn_status cpattn_fwd_varlen(const void *q, const void *k, const void *v, voi
   return fwd_impl(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, 0, doc_lo, doc_hi, dt, stream);
 }
 
+cpattn_status cpattn_fwd_rope_cfg(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int B, int T, int T_valid, int H, int H_kv, int d, int cp,
+                                  int causal, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                  cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  cpattn_status st = check_rope_cfg(cfg);
+  if (st != CPATTN_OK) return st;
+  return fwd_impl(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, 1, nullptr, nullptr, dt, stream,
+                  cfg);
+}
+
 static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
                               int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
-                              cpattn_stream_t stream) {
+                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
@@ -366,6 +377,7 @@ static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void 
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
   g.doc_lo = doc_lo;
   g.doc_hi = doc_hi;
+  g.rope_cfg = rope_cfg;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   trace_record(0, s);
   if (dt == CPATTN_F32)
@@ -396,7 +408,8 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                               int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
-                              cpattn_dtype dt, cpattn_stream_t stream);
+                              cpattn_dtype dt, cpattn_stream_t stream,
+                              const cpattn_rope_cfg *rope_cfg = nullptr);
 
 cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
@@ -417,6 +430,18 @@ cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, con
                   doc_lo, doc_hi, dt, stream);
 }
 
+cpattn_status cpattn_bwd_rope_cfg(const void *q, const void *k, const void *v, const void *o,
+                                  const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                  void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                                  int cp, int causal, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                  cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  cpattn_status st = check_rope_cfg(cfg);
+  if (st != CPATTN_OK) return st;
+  return bwd_impl(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal, 1,
+                  nullptr, nullptr, dt, stream, cfg);
+}
+
 cpattn_status cpattn_doc_bounds(const int32_t *cu_seqlens, int n_docs, int T, int32_t *doc_lo,
                                 int32_t *doc_hi, cpattn_stream_t stream) {
   g_msg[0] = 0;
@@ -435,7 +460,7 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                               int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
-                              cpattn_dtype dt, cpattn_stream_t stream) {
+                              cpattn_dtype dt, cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(CPATTN_ERR_ARG, "null pointer");
@@ -465,6 +490,7 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
   Geometry g = geometry(B, H, T, T_valid, d, cp, causal, rope, H_kv);
   g.doc_lo = doc_lo;
   g.doc_hi = doc_hi;
+  g.rope_cfg = rope_cfg;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
   trace_record(0, s);

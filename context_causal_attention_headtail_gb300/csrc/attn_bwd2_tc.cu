@@ -55,7 +55,8 @@ __device__ __forceinline__ void store_tmem_cols(uint32_t t_row, int c0, int nchu
 
 // Rotate-half RoPE of a bf16 row held as D/2 words in registers (word k holds
 // columns 2k, 2k+1; word k < D/4 pairs with word k + D/4) at natural
-// position pos: R for FORWARD, its transpose otherwise.
+// position pos: m R for FORWARD, its transpose otherwise (m the temperature
+// of the RoPE configuration, 1 for the standard rotation).
 template <int D, bool FORWARD>
 __device__ __forceinline__ void rope_row_words(uint32_t *w, int pos, const RopeTheta &th) {
 #pragma unroll
@@ -63,6 +64,7 @@ __device__ __forceinline__ void rope_row_words(uint32_t *w, int pos, const RopeT
     float s0, c0, s1, c1;
     rope_sincos(pos, th.hi[2 * k], th.lo[2 * k], s0, c0);
     rope_sincos(pos, th.hi[2 * k + 1], th.lo[2 * k + 1], s1, c1);
+    c0 *= th.mscale; s0 *= th.mscale; c1 *= th.mscale; s1 *= th.mscale;   // m R (YaRN temperature)
     if (!FORWARD) { s0 = -s0; s1 = -s1; }
     const float x0 = bf16lo_to_f32(w[k]), x1 = bf16hi_to_f32(w[k]);
     const float y0 = bf16lo_to_f32(w[k + D / 4]), y1 = bf16hi_to_f32(w[k + D / 4]);
@@ -71,7 +73,8 @@ __device__ __forceinline__ void rope_row_words(uint32_t *w, int pos, const RopeT
   }
 }
 
-// Stores scale * R^T of one pair of 32-column chunks of a TMEM row: columns
+// Stores scale * m R^T of one pair of 32-column chunks of a TMEM row (m the
+// attention temperature of the RoPE configuration, 1 for the standard one): columns
 // 32a..32a+31 and their rotation partners D/2 further on (frequencies
 // 32a..32a+31), for the key or query at natural position pos, as bf16 at
 // dst + the same columns (every lane of the warp must call this).
@@ -90,6 +93,8 @@ __device__ __forceinline__ void store_tmem_pair_rope(uint32_t t_col0, int a, flo
     for (int u = 0; u < 2; ++u) {
       float sn, cs;
       rope_sincos(pos, th.hi[32 * a + e + u], th.lo[32 * a + e + u], sn, cs);
+      sn *= th.mscale;
+      cs *= th.mscale;
       const float x = __uint_as_float(ra[e + u]) * scale, y = __uint_as_float(rb[e + u]) * scale;
       o[0][u] = fmaf(x, cs, y * sn);    // R^T: x cos + y sin
       o[1][u] = fmaf(y, cs, -x * sn);   //      y cos - x sin
@@ -863,7 +868,7 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   bp.tpc = (g.c + kTile - 1) / kTile;
   bp.scale = (float)(1.0 / sqrt((double)g.d));
   bp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
-  make_rope_theta(g.d, &bp.theta);
+  make_rope_theta(g.d, &bp.theta, g.rope_cfg);
   const long long grid = BH * 2 * g.cp * bp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
   if (g.d == 128)

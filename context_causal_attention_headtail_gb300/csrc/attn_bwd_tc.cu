@@ -39,7 +39,8 @@ struct BwdParams {
 };
 
 // Epilogue of one accumulator row (D fp32 columns in TMEM at `taddr`):
-// x = scale * acc, then R(pos)^T when ROPE (pairs (i, i + D/2)), rounded to
+// x = scale * acc, then m R(pos)^T when ROPE (pairs (i, i + D/2); m the
+// RoPE configuration's temperature, 1 for the standard rotation), rounded to
 // bf16 and stored at `dst` when `valid`. Columns are taken as pairs of 32-wide
 // chunks [32h, 32h+32) and [D/2 + 32h, D/2 + 32h + 32) so each RoPE pair is
 // in registers at once. Every lane of the warp must call this (tcgen05.ld).
@@ -61,6 +62,7 @@ __device__ __forceinline__ void epilogue_row(uint32_t taddr, float scale, int po
         float s0, c0, s1, c1;
         rope_sincos(pos, th.hi[32 * h + e], th.lo[32 * h + e], s0, c0);
         rope_sincos(pos, th.hi[32 * h + e + 1], th.lo[32 * h + e + 1], s1, c1);
+        c0 *= th.mscale; s0 *= th.mscale; c1 *= th.mscale; s1 *= th.mscale;
         const float u0 = fmaf(x0, c0, y0 * s0), w0 = fmaf(y0, c0, -x0 * s0);
         const float u1 = fmaf(x1, c1, y1 * s1), w1 = fmaf(y1, c1, -x1 * s1);
         x0 = u0; y0 = w0; x1 = u1; y1 = w1;
@@ -629,7 +631,7 @@ cpattn_status launch_bwd_bf16(const void *q, const void *k, const void *v, const
   bp.tpc = (g.c + kTile - 1) / kTile;
   bp.scale = (float)(1.0 / sqrt((double)g.d));
   bp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
-  make_rope_theta(g.d, &bp.theta);
+  make_rope_theta(g.d, &bp.theta, g.rope_cfg);
   const long long grid = BH * 2 * g.cp * bp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
   auto *pdq = static_cast<__nv_bfloat16 *>(dq);

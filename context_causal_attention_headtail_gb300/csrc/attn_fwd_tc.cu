@@ -773,7 +773,7 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   fp.causal = g.causal;
   fp.tpc = (g.c + kTile - 1) / kTile;
   fp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
-  make_rope_theta(g.d, &fp.theta);
+  make_rope_theta(g.d, &fp.theta, g.rope_cfg);
   // Paired query tiles with a tile table in shared memory (RoPE, if asked
   // for, rotates the tiles in shared memory). Longer schedules take the
   // one-tile kernel below.

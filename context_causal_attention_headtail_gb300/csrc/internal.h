@@ -44,6 +44,9 @@ struct Geometry {
   // Packed documents: per natural position, its document's [doc_lo, doc_hi)
   // (device int32 [T]); nullptr when the sequence is one document.
   const int *doc_lo = nullptr, *doc_hi = nullptr;
+  // In-kernel RoPE frequencies and temperature (host pointer read by the
+  // launchers; nullptr: the standard rotation, base 10000).
+  const cpattn_rope_cfg *rope_cfg = nullptr;
 };
 
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------

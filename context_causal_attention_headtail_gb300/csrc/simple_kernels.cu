@@ -570,17 +570,20 @@ __device__ __forceinline__ int natural_pos(int i, int c, int cp) {
 
 // A lane holds elements lane + 32*e of a row (e < D/32); for rotate-half
 // RoPE the partner of e is e +- D/64, held by the same lane. Angles are taken
-// in double: this path is about exactness, not speed.
+// in double from the frequency pair (hi + lo) of the RoPE configuration, and
+// the rotation carries its temperature m (m R, or m R^T for gradients): this
+// path is about exactness, not speed.
 template <int D>
-__device__ __forceinline__ void rope_row_f32(float (&x)[D / 32], int pos, int lane, bool transpose) {
+__device__ __forceinline__ void rope_row_f32(float (&x)[D / 32], int pos, int lane, bool transpose,
+                                             const RopeTheta &th) {
   constexpr int V = D / 32, HV = V / 2;
 #pragma unroll
   for (int e = 0; e < HV; ++e) {
     const int i = lane + 32 * e;  // frequency index < D/2
-    const double th = pow(10000.0, -2.0 * i / D);
+    const double theta = (double)th.hi[i] + (double)th.lo[i];
     double sn, cs;
-    sincos((double)pos * th, &sn, &cs);
-    const float c = (float)cs, s = transpose ? -(float)sn : (float)sn;
+    sincos((double)pos * theta, &sn, &cs);
+    const float c = (float)cs * th.mscale, s = (transpose ? -(float)sn : (float)sn) * th.mscale;
     const float a = x[e], b = x[e + HV];
     x[e] = a * c - b * s;
     x[e + HV] = b * c + a * s;
@@ -619,7 +622,8 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float *__restrict__ 
                                                       const float *__restrict__ k,
                                                       const float *__restrict__ v,
                                                       float *__restrict__ o, float *__restrict__ lse,
-                                                      Geometry g) {
+                                                      Geometry g,
+    const __grid_constant__ RopeTheta th) {
   constexpr int V = D / 32;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -633,7 +637,7 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float *__restrict__ 
   const float *kb = k + bkv * g.T * D, *vb = v + bkv * g.T * D;
   float qr[V];
   load_row<D>(q + row * D, lane, qr);
-  if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+  if (g.rope) rope_row_f32<D>(qr, qp, lane, false, th);
   float O[V], L = -INFINITY;
 #pragma unroll
   for (int e = 0; e < V; ++e) O[e] = 0.f;
@@ -650,7 +654,7 @@ __global__ void __launch_bounds__(128) fwd_f32_kernel(const float *__restrict__ 
         if (!pair_allowed(qp, kp, g)) continue;
         float kr[V], vr[V];
         load_row<D>(kb + (long long)(row0 + u) * D, lane, kr);
-        if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+        if (g.rope) rope_row_f32<D>(kr, kp, lane, false, th);
         load_row<D>(vb + (long long)(row0 + u) * D, lane, vr);
         const float sc = warp_dot<D>(qr, kr) * scale;
         const float m_new = fmaxf(m_s, sc);
@@ -685,7 +689,8 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
                                                          const float *__restrict__ lse,
                                                          const float *__restrict__ dO,
                                                          const float *__restrict__ Dv,
-                                                         float *__restrict__ dq, Geometry g) {
+                                                         float *__restrict__ dq, Geometry g,
+    const __grid_constant__ RopeTheta th) {
   constexpr int V = D / 32;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -699,7 +704,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
   const float *kb = k + bkv * g.T * D, *vb = v + bkv * g.T * D;
   float qr[V], dor[V], acc[V];
   load_row<D>(q + row * D, lane, qr);
-  if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+  if (g.rope) rope_row_f32<D>(qr, qp, lane, false, th);
   load_row<D>(dO + row * D, lane, dor);
   const float L = lse[row], Dt = Dv[row];
 #pragma unroll
@@ -714,7 +719,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
         if (!pair_allowed(qp, kp, g)) continue;
         float kr[V], vr[V];
         load_row<D>(kb + (long long)(row0 + u) * D, lane, kr);
-        if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+        if (g.rope) rope_row_f32<D>(kr, kp, lane, false, th);
         load_row<D>(vb + (long long)(row0 + u) * D, lane, vr);
         const float p = expf(warp_dot<D>(qr, kr) * scale - L);
         const float ds = p * (warp_dot<D>(dor, vr) - Dt);
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(128) bwd_dq_f32_kernel(const float *__restrict
   }
 #pragma unroll
   for (int e = 0; e < V; ++e) acc[e] *= scale;
-  if (g.rope) rope_row_f32<D>(acc, qp, lane, true);
+  if (g.rope) rope_row_f32<D>(acc, qp, lane, true, th);
 #pragma unroll
   for (int e = 0; e < V; ++e) dq[row * D + lane + 32 * e] = acc[e];
 }
@@ -742,7 +747,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restri
                                                            const float *__restrict__ dO,
                                                            const float *__restrict__ Dv,
                                                            float *__restrict__ dk,
-                                                           float *__restrict__ dv, Geometry g) {
+                                                           float *__restrict__ dv, Geometry g,
+    const __grid_constant__ RopeTheta th) {
   constexpr int V = D / 32;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -755,7 +761,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restri
   const int group = g.H / g.Hkv;
   float kr[V], vr[V], adk[V], adv[V];
   load_row<D>(k + row * D, lane, kr);
-  if (g.rope) rope_row_f32<D>(kr, kp, lane, false);
+  if (g.rope) rope_row_f32<D>(kr, kp, lane, false, th);
   load_row<D>(v + row * D, lane, vr);
 #pragma unroll
   for (int e = 0; e < V; ++e) { adk[e] = 0.f; adv[e] = 0.f; }
@@ -774,7 +780,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restri
           const int t = row0 + u;
           float qr[V], dor[V];
           load_row<D>(qb + (long long)t * D, lane, qr);
-          if (g.rope) rope_row_f32<D>(qr, qp, lane, false);
+          if (g.rope) rope_row_f32<D>(qr, qp, lane, false, th);
           load_row<D>(dob + (long long)t * D, lane, dor);
           const float p = expf(warp_dot<D>(qr, kr) * scale - lb[t]);
           const float ds = p * (warp_dot<D>(dor, vr) - Db[t]);
@@ -789,7 +795,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_f32_kernel(const float *__restri
   }
 #pragma unroll
   for (int e = 0; e < V; ++e) adk[e] *= scale;
-  if (g.rope) rope_row_f32<D>(adk, kp, lane, true);
+  if (g.rope) rope_row_f32<D>(adk, kp, lane, true, th);
 #pragma unroll
   for (int e = 0; e < V; ++e) {
     dk[row * D + lane + 32 * e] = adk[e];
@@ -801,8 +807,10 @@ cpattn_status launch_fwd_f32(const float *q, const float *k, const float *v, flo
                              const Geometry &g, cudaStream_t s) {
   const long long rows = (long long)g.B * g.H * g.T;
   const unsigned blocks = (unsigned)((rows + 3) / 4);
-  if (g.d == 128) fwd_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g);
-  else fwd_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g);
+  RopeTheta th;
+  make_rope_theta(g.d, &th, g.rope_cfg);
+  if (g.d == 128) fwd_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g, th);
+  else fwd_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, o, lse, g, th);
   return check_launch("fp32 forward kernel");
 }
 
@@ -813,14 +821,16 @@ cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, con
   const long long rows = (long long)g.B * g.H * g.T;
   const unsigned blocks = (unsigned)((rows + 3) / 4);
   const unsigned kv_blocks = (unsigned)(((long long)g.B * g.Hkv * g.T + 3) / 4);
+  RopeTheta th;
+  make_rope_theta(g.d, &th, g.rope_cfg);
   if (g.d == 128) {
-    bwd_dkdv_f32_kernel<128><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    bwd_dkdv_f32_kernel<128><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
     trace_record(2, s);
-    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
+    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
   } else {
-    bwd_dkdv_f32_kernel<64><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g);
+    bwd_dkdv_f32_kernel<64><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
     trace_record(2, s);
-    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g);
+    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
   }
   return check_launch("fp32 backward kernels");
 }

@@ -350,6 +350,7 @@ __device__ __forceinline__ void rope_tile(uint8_t *tile, int pos0, int wid, int 
   float c0, s0, c1, s1, cd0, sd0, cd1, sd1;
   rope_sincos(pos0 + row0, th.hi[f], th.lo[f], s0, c0);
   rope_sincos(pos0 + row0, th.hi[f + 1], th.lo[f + 1], s1, c1);
+  c0 *= th.mscale; s0 *= th.mscale; c1 *= th.mscale; s1 *= th.mscale;   // m R (temperature, YaRN)
   rope_sincos(STEP, th.hi[f], th.lo[f], sd0, cd0);
   rope_sincos(STEP, th.hi[f + 1], th.lo[f + 1], sd1, cd1);
 #pragma unroll 4
@@ -389,11 +390,13 @@ struct RopeRows {
   uint32_t xoff, yoff;                            // byte offsets in row r0
   int r0;
   float th_hi[8], th_lo[8];
+  float m;                                        // attention temperature (YaRN), 1 otherwise
   uint64_t cd[4], sd[4];                          // cos, sin of RS * theta, frequency pairs
 
   __device__ __forceinline__ void init(int u, const RopeTheta &th) {
     const int c = u % CPR;
     r0 = u / CPR;
+    m = th.mscale;
     const uint32_t sw = (uint32_t)(r0 & 7);
     xoff = (uint32_t)r0 * 128u + (((uint32_t)c ^ sw) << 4);
     yoff = (D == 128) ? (uint32_t)kRows * 128u + xoff : (uint32_t)r0 * 128u + ((((uint32_t)c + 4u) ^ sw) << 4);
@@ -419,8 +422,8 @@ struct RopeRows {
       float s0, c0, s1, c1;
       rope_sincos_fast(pos0 + r0, th_hi[2 * w], th_lo[2 * w], s0, c0);
       rope_sincos_fast(pos0 + r0, th_hi[2 * w + 1], th_lo[2 * w + 1], s1, c1);
-      C[w] = f2(c0, c1);
-      S[w] = f2(s0, s1);
+      C[w] = f2(m * c0, m * c1);   // m R: the angle step below keeps the factor
+      S[w] = f2(m * s0, m * s1);
     }
 #pragma unroll 2
     for (int j = 0; j < NI; ++j) {

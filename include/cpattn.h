@@ -185,6 +185,24 @@ cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const 
                              void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                              int cp, int causal, int rope, cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ------------------------------------- in-kernel RoPE with a configuration ---
+ * cpattn_fwd_gqa / cpattn_bwd_gqa with rope = 1 and the rotation of cfg
+ * (standard base, or YaRN: NTK-by-parts frequencies and the attention
+ * temperature m; Claude Logs, 2026-07-09) instead of the standard one: the
+ * kernels use m R(p) q, m R(p) k, and the gradients leave through (m R(p))^T,
+ * so the result equals cpattn_shard_rope_cfg followed by the rope = 0 call.
+ * cfg (host, read during the call only) must be valid for
+ * cpattn_shard_rope_cfg, else CPATTN_ERR_ARG; NULL is CPATTN_ERR_ARG. */
+cpattn_status cpattn_fwd_rope_cfg(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int B, int T, int T_valid, int H, int H_kv, int d, int cp,
+                                  int causal, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                  cpattn_stream_t stream);
+cpattn_status cpattn_bwd_rope_cfg(const void *q, const void *k, const void *v, const void *o,
+                                  const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                  void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                                  int cp, int causal, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                  cpattn_stream_t stream);
+
 /* ------------------------------------------ packed documents (varlen) ---
  * Several documents packed along T (the THD layout of "fix(cp): preserve
  * gradients when sharding VLM inputs - #2931"; Claude Logs, 2026-07-16:

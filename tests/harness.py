@@ -95,16 +95,17 @@ def run_gpu_ulysses(w: Workload, inp: dict, device="cuda:0") -> dict:
 
 def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
             rope_mode: str = "kernel") -> dict:
-    """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd;
-    "shard" rotates q, k in cpattn_shard_rope (cpattn_shard_rope_cfg for YaRN),
-    runs the attention with rope=0 and takes dq, dk back through
-    cpattn_unshard_rope. YaRN exists only on the "shard" path."""
+    """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd
+    (cpattn_fwd_rope_cfg / cpattn_bwd_rope_cfg for YaRN); "shard" rotates q, k in
+    cpattn_shard_rope (cpattn_shard_rope_cfg for YaRN), runs the attention with
+    rope=0 and takes dq, dk back through cpattn_unshard_rope. Packed documents
+    take RoPE from the "shard" path only."""
     dev = torch.device(device)
     stream = torch.cuda.current_stream(dev)
     fused = w.rope and rope_mode == "shard"
     rope_flag = w.rope and not fused
-    if (w.yarn or w.packed) and w.rope and not fused:
-        raise ValueError("YaRN and packed documents take RoPE from the shard / unshard passes")
+    if w.packed and w.rope and not fused:
+        raise ValueError("packed documents take RoPE from the shard / unshard passes")
     cfg = gpu_rope_cfg(w)
     docs = None
     if w.packed:
@@ -123,14 +124,14 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     out = {}
     for _ in range(repeat):
         cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
-                   docs=docs)
+                   docs=docs, rope_cfg=cfg if rope_flag else None)
     if with_bwd:
         dq, dk, dv = torch.empty_like(sh["q"]), torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
         ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
                          device=dev)
         for _ in range(repeat):
             cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
-                       w.causal, rope_flag, stream, docs=docs)
+                       w.causal, rope_flag, stream, docs=docs, rope_cfg=cfg if rope_flag else None)
         for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
             nt = torch.empty_like(t)
             if fused and name in ("dq", "dk"):

@@ -371,8 +371,8 @@ SMALL_BF16 = [
 def test_fp32_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
-    if mode == "kernel" and (w.yarn or (w.packed and w.rope)):
-        pytest.skip("YaRN and packed documents take RoPE from the shard / unshard passes")
+    if mode == "kernel" and w.packed and w.rope:
+        pytest.skip("packed documents take RoPE from the shard / unshard passes")
     inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
     _check_full(w, run_gpu(w, inp, rope_mode=mode), _oracle_full(w, inp))
 
@@ -382,8 +382,8 @@ def test_fp32_path_full(w, mode):
 def test_bf16_path_full(w, mode):
     if mode == "shard" and not w.rope:
         pytest.skip("no RoPE: one path")
-    if mode == "kernel" and (w.yarn or (w.packed and w.rope)):
-        pytest.skip("YaRN and packed documents take RoPE from the shard / unshard passes")
+    if mode == "kernel" and w.packed and w.rope:
+        pytest.skip("packed documents take RoPE from the shard / unshard passes")
     inp = make_inputs(w, seed=7 + w.T + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     want = _oracle_full(w, inp)
@@ -455,7 +455,8 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
                                        ("window_32k", "shard"), ("window_32k", "kernel"),
                                        ("padded_12289", "shard"), ("padded_12289", "kernel"),
                                        ("gqa_32k", "shard"), ("gqa_32k", "kernel"),
-                                       ("yarn_32k", "shard"), ("varlen_32k", "shard")])
+                                       ("yarn_32k", "shard"), ("yarn_32k", "kernel"),
+                                       ("varlen_32k", "shard")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])

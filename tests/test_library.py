@@ -123,6 +123,10 @@ def test_rope_cfg_is_validated(lib, kw):
         st = fn(P[0], P[1], 1, 1, 1024, 128, 2, cpattn.BF16, ctypes.byref(cfg), None)
         assert st == cpattn.ERR_ARG
     assert lib.cpattn_shard_rope_cfg(P[0], P[1], 1, 1, 1024, 128, 2, cpattn.BF16, None, None) == cpattn.ERR_ARG
+    # the in-kernel RoPE entry points validate the same configuration, and need one
+    for c in (ctypes.byref(cfg), None):
+        assert lib.cpattn_fwd_rope_cfg(*P[:5], 1, 1024, 1024, 2, 2, 128, 2, 1, c, cpattn.BF16, None) == cpattn.ERR_ARG
+        assert lib.cpattn_bwd_rope_cfg(*P, 1, 1024, 1024, 2, 2, 128, 2, 1, c, cpattn.BF16, None) == cpattn.ERR_ARG
 
 
 def test_rope_cfg_layout_matches_header():
