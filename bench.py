@@ -42,9 +42,9 @@ DEFAULT_WORKLOAD = "window_32k"
 # on the 32k workload (profiles/tc_kernels_window_32k.md); a kernel missing
 # here has no capture of its current version. Only valid for that workload.
 NCU_TRAFFIC_BYTES = {
-    ("window_32k", "fwd"): 2.219422e9 + 0.121415e9,
-    ("window_32k", "bwd_dkdv"): 4.113598e9 + 0.239080e9,
-    ("window_32k", "bwd_dq"): 4.066322e9 + 0.120361e9,
+    ("window_32k", "fwd"): 2.217879e9 + 0.120774e9,
+    ("window_32k", "bwd_dkdv"): 4.115046e9 + 0.239118e9,
+    ("window_32k", "bwd_dq"): 4.067247e9 + 0.120400e9,
 }
 
 
