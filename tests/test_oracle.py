@@ -77,6 +77,23 @@ def test_headtail_balances_causal_work(T, cp):
     assert cp == 1 or len(set(contiguous)) > 1
 
 
+@pytest.mark.parametrize("T,cp,T_valid", [(8, 2, 8), (8, 2, 6), (24, 3, 20), (64, 4, 64), (60, 5, 41)])
+def test_rank_causal_work_counts_pairs(T, cp, T_valid):
+    """Independent count: a causal row t sees keys 0..min(t, T_valid - 1), i.e.
+    min(t + 1, T_valid) of them; a non-causal row sees T_valid. Rows come from
+    the enumerated pairing, not from the oracle's index map."""
+    order = _pairing_by_enumeration(T, cp)
+    per_rank = T // cp
+    want_causal = [sum(min(t + 1, T_valid) for t in order[r * per_rank:(r + 1) * per_rank])
+                   for r in range(cp)]
+    assert A.rank_causal_work(T, cp, True, T_valid) == want_causal
+    assert A.rank_causal_work(T, cp, False, T_valid) == [per_rank * T_valid] * cp
+    if (T, cp) == (8, 2):
+        # by hand: rank 0 = {0,1,6,7}, rank 1 = {2,3,4,5}
+        assert want_causal == ([1 + 2 + 7 + 8, 3 + 4 + 5 + 6] if T_valid == 8
+                               else [1 + 2 + 6 + 6, 3 + 4 + 5 + 6])
+
+
 def test_headtail_rejects_bad_shapes():
     with pytest.raises(ValueError):
         HT.shard_index(10, 2)
@@ -270,6 +287,76 @@ def test_merge_algebra():
     Om, Lm = A.merge(*pa, *pb)
     assert np.allclose(Om, special.softmax(S, axis=1) @ v, atol=1e-13)
     assert np.allclose(Lm, special.logsumexp(S, axis=1), atol=1e-13)
+
+
+def check_merge_many(merge_many_fn):
+    """Max error of an n-way SDPAMerger fold against scipy over the union of keys.
+
+    "Claude Logs", 2026-03-20 (an SDPAMerger folds the per-step partials) and
+    2026-05-20 (partials that see no key must not disturb the result). Each
+    partial is built here directly with scipy from its own key subset, so the
+    check rests on nothing else in the oracle. Keys are split into n disjoint,
+    interleaved subsets; a causal mask leaves some rows empty in some partials
+    and some rows (position -1) empty in all of them. An empty partial carries
+    LSE = -inf and an arbitrary finite O, which must not leak into the result.
+    """
+    err = 0.0
+    d = 6
+    for n in (1, 2, 5, 16):
+        Tk = 3 * n + 2
+        nq = 9
+        q, k, v = rnd(nq, d), rnd(Tk, d), rnd(Tk, d)
+        q_pos = np.array([-1, 0, 1, 2, 5, Tk // 2, Tk - 2, Tk - 1, -1])
+        k_pos = np.arange(Tk)
+        S = np.where(k_pos[None, :] <= q_pos[:, None], q @ k.T / math.sqrt(d), -np.inf)
+        subset = rng.permutation(Tk) % n                      # key j belongs to partial subset[j]
+        o_parts, l_parts = [], []
+        for i in range(n):
+            Si = np.where(subset[None, :] == i, S, -np.inf)
+            with np.errstate(invalid="ignore"):
+                Pi = special.softmax(Si, axis=1)
+            live = np.isfinite(Si).any(axis=1)
+            o_parts.append(np.where(live[:, None], np.nan_to_num(Pi) @ v, rnd(nq, d)))
+            l_parts.append(np.where(live, special.logsumexp(Si, axis=1), -np.inf))
+        O, L = merge_many_fn(o_parts, l_parts)
+        live = np.isfinite(S).any(axis=1)
+        with np.errstate(invalid="ignore"):
+            want_o = np.where(live[:, None], np.nan_to_num(special.softmax(S, axis=1)) @ v, 0.0)
+        want_l = np.where(live, special.logsumexp(S, axis=1), -np.inf)
+        if not (np.array_equal(np.isfinite(L), live) and np.all(L[~live] == -np.inf)
+                and np.all(O[~live] == 0.0)):
+            return np.inf
+        err = max(err, np.abs(O - want_o).max(), np.abs(L[live] - want_l[live]).max())
+    return err
+
+
+def test_merge_many_against_scipy_union():
+    assert check_merge_many(A.merge_many) < 1e-13
+
+
+def test_planted_merge_many_mistakes_are_caught():
+    def from_zero(o_parts, l_parts):                          # fold starts at L = 0, not -inf
+        O, L = np.zeros_like(o_parts[0]), np.zeros(np.shape(l_parts[0]))
+        for o_s, l_s in zip(o_parts, l_parts):
+            O, L = A.merge(O, L, o_s, l_s)
+        return O, L
+
+    def first_twice(o_parts, l_parts):                        # partial 0 merged twice
+        return A.merge_many([o_parts[0]] + list(o_parts), [l_parts[0]] + list(l_parts))
+
+    def last_dropped(o_parts, l_parts):                       # loop stops one short
+        n = max(len(o_parts) - 1, 1)
+        return A.merge_many(o_parts[:n], l_parts[:n])
+
+    def plain_average(o_parts, l_parts):                      # no LSE weights at all
+        w = [np.isfinite(l).astype(float) for l in l_parts]
+        tot = np.maximum(sum(w), 1.0)
+        O = sum(wi[:, None] * o for wi, o in zip(w, o_parts)) / tot[:, None]
+        return O, A.merge_many(o_parts, l_parts)[1]
+
+    with np.errstate(all="ignore"):
+        for bad in (from_zero, first_twice, last_dropped, plain_average):
+            assert not check_merge_many(bad) < 1e-6, bad.__name__
 
 
 # ------------------------------------------------------------ backward ----
