@@ -93,3 +93,48 @@ def test_rank_dropout_is_an_error_not_a_hang():
     for p in ctx.processes:
         p.join(120)
     assert out.get(0, "").startswith("error"), out.get(0)
+
+
+def test_launch_plan_honours_gpus():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.launch_plan(1, {}) == ("run", "")
+    assert bench.launch_plan(4, {})[0] == "relaunch"
+    assert bench.launch_plan(2, {"WORLD_SIZE": "2"}) == ("run", "")
+    assert bench.launch_plan(8, {"WORLD_SIZE": "1"})[0] == "refuse"
+    assert bench.launch_plan(0, {})[0] == "refuse"
+    cmd = bench.relaunch_cmd(2, ["--gpus", "2", "--steps", "1"], 29999)
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=2" in cmd and cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-4:] == ["--gpus", "2", "--steps", "1"]
+
+
+def _bench(args, extra_env=None, timeout=300):
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env.update(extra_env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args, env=env,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+@pytest.mark.timeout(120)
+def test_bench_refuses_a_world_size_other_than_gpus():
+    r = _bench(["--gpus", "2", "--impl", "reference"], {"WORLD_SIZE": "1", "RANK": "0"})
+    assert r.returncode == 2 and "WORLD_SIZE=1" in r.stderr
+    assert r.stdout.strip() == ""
+
+
+@pytest.mark.timeout(400)
+def test_bench_gpus_2_starts_two_ranks():
+    """--gpus 2 without a launcher starts two ranks (gloo-free: the oracle arm
+    needs no collective); rank 0 alone prints, with n_gpus = 2."""
+    import json
+    r = _bench(["--gpus", "2", "--impl", "reference", "--workload", "tiny_fp32",
+                "--steps", "1", "--warmup", "0"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+
