@@ -35,22 +35,62 @@ cpattn_status check_launch(const char *what) {
   return CPATTN_OK;
 }
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId: unique
+// for the life of the process, so a context created after a device reset, or
+// a non-primary context, gets a new one). 0 if it cannot be read.
+static unsigned long long current_context_id() {
+  typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+  typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of a file-scope __device__ symbol in the current context.
+// A symbol's name in host code is a host-side stand-in, not a device address,
+// so it is resolved with cudaGetSymbolAddress and cached per context (the
+// module, and with it the symbol, is loaded again in every new context). When
+// the context id cannot be read, the address is resolved on every call.
+void *symbol_address(const void *symbol) {
+  struct Entry { const void *sym; unsigned long long ctx; void *addr; };
+  static std::mutex mu;
+  static Entry cache[64];
+  static int next = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  unsigned long long ctx = current_context_id();
+  if (ctx)
+    for (const Entry &e : cache)
+      if (e.sym == symbol && e.ctx == ctx) return e.addr;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+  ctx = current_context_id();        // the runtime has made the device's context current by now
+  if (ctx) {
+    cache[next] = Entry{symbol, ctx, p};
+    next = (next + 1) % 64;
+  }
+  return p;
+}
+
 // One flag per device, written by kernels whose bounded waits expire.
 __device__ int g_err_flag;
 
-int *device_err_flag() {
-  static std::mutex mu;
-  static int *addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_err_flag) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<int *>(p);
-  }
-  return addr[dev];
-}
+int *device_err_flag() { return static_cast<int *>(symbol_address(&g_err_flag)); }
 
 void make_rope_theta(int d, RopeTheta *t, const cpattn_rope_cfg *cfg) {
   const double base = cfg ? cfg->base : 10000.0;
@@ -514,23 +554,11 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
 // (CPATTN_NOALLOC_MAX_ROWS floats) until the process exits.
 static __device__ __align__(256) float g_noalloc_scratch[CPATTN_NOALLOC_MAX_ROWS];
 
-// Device address of this device's copy of the array. Host code must not pass
-// the symbol itself to a kernel (on the host it names a stand-in, not device
-// memory), so the address is resolved once per device, with that device
-// current, and cached.
-static float *noalloc_scratch() {
-  static std::mutex mu;
-  static float *addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<float *>(ptr);
-  }
-  return addr[dev];
-}
+// Device address of the current context's copy of the array. Host code must
+// not pass the symbol itself to a kernel (on the host it names a stand-in, not
+// device memory), so the address is resolved with the device current, checked,
+// and cached per context (symbol_address).
+static float *noalloc_scratch() { return static_cast<float *>(symbol_address(g_noalloc_scratch)); }
 
 cpattn_status cpattn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                                  const float *lse, const void *dO, void *dq, void *dk, void *dv,

@@ -17,6 +17,9 @@ cpattn_status check_launch(const char *what);
 // Device address of this device's error flag (set by kernels, read and
 // cleared by cpattn_sync_status). nullptr if it could not be resolved.
 int *device_err_flag();
+// Device address of a file-scope __device__ symbol in the current context,
+// cached per context; nullptr on failure.
+void *symbol_address(const void *symbol);
 
 // Device error codes written to the flag.
 enum : int { ERR_FLAG_TIMEOUT = 1, ERR_FLAG_BAD_DOCS = 2 };

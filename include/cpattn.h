@@ -281,9 +281,10 @@ cpattn_status cpattn_ulysses_a2a_rope(const void *src, void *dst, int B, int H, 
  * library holds until the process exits. The call itself allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).
  *  - B*H*T must be <= CPATTN_NOALLOC_MAX_ROWS, else CPATTN_ERR_SHAPE.
- *  - The first call on each device resolves the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture.
+ *  - The first call in each CUDA context (per device; again after a device
+ *    reset, and in any non-primary context) resolves the array's device
+ *    address (cudaGetSymbolAddress, with that device current) and caches it
+ *    for that context; make that first call before any stream capture.
  *  - All calls share the one array. Each call overwrites the rows it uses
  *    before reading them, so nothing stale leaks into a result, but calls
  *    whose kernels overlap on the GPU (different streams, or different host

@@ -161,25 +161,43 @@ def allowed(q_pos: np.ndarray, k_pos: np.ndarray, causal: bool, T_valid: int,
     return ok
 
 
+def allowed_sum(W: np.ndarray, ok: np.ndarray, X: np.ndarray) -> np.ndarray:
+    """out[t, :] = sum over the j with ok[t, j] of W[t, j] * X[j, :].
+
+    The attention sums run over allowed pairs only: a pair the mask excludes
+    contributes nothing, even where W or X holds an Inf or a NaN (which a dense
+    product with zeros at masked pairs would turn into NaN, 0 * Inf). Finite
+    entries of X go through one matrix product; each non-finite entry is then
+    added on its own into the rows allowed to see it.
+    """
+    W = np.where(ok, W, 0.0)
+    bad = ~np.isfinite(X)
+    out = W @ np.where(bad, 0.0, X)
+    for j, c in zip(*np.nonzero(bad)):
+        out[:, c] += np.where(ok[:, j], W[:, j] * X[j, c], 0.0)
+    return out
+
+
 def partial_attention(qr: np.ndarray, kr: np.ndarray, vr: np.ndarray, q_pos: np.ndarray,
                       k_pos: np.ndarray, causal: bool, T_valid: int, docs=None):
     """Softmax attention of query rows over a key set, with the global mask.
 
     qr, kr are already rotated (if RoPE is on). Returns (O, LSE); a row with no
-    allowed key gets the merge identity (O = 0, LSE = -inf).
+    allowed key gets the merge identity (O = 0, LSE = -inf). Only allowed pairs
+    enter the max, the sums and the product with V, so a NaN or an Inf reaches
+    exactly the rows whose allowed pairs hold it.
     """
     d = qr.shape[-1]
     S = (qr @ kr.T) / math.sqrt(d)
     ok = allowed(q_pos, k_pos, causal, T_valid, docs)
+    has = ok.any(axis=1)                               # a row is empty iff no pair is allowed
     S = np.where(ok, S, -np.inf)
-    m = S.max(axis=1, initial=-np.inf)
-    has = np.isfinite(m)
-    m_safe = np.where(has, m, 0.0)
-    E = np.exp(S - m_safe[:, None])                    # exp(-inf) = 0 on masked pairs
+    m = np.where(has, np.max(S, axis=1, initial=-np.inf), 0.0)
+    E = np.where(ok, np.exp(S - m[:, None]), 0.0)      # exp(-inf) = 0 on masked pairs
     ssum = E.sum(axis=1)
-    lse = np.where(has, m_safe + np.log(np.where(has, ssum, 1.0)), -np.inf)
+    lse = np.where(has, m + np.log(np.where(has, ssum, 1.0)), -np.inf)
     P = np.where(has[:, None], E / np.where(has, ssum, 1.0)[:, None], 0.0)
-    return P @ vr, lse
+    return allowed_sum(P, ok, vr), lse
 
 
 def _heads(x):
@@ -258,12 +276,12 @@ def _backward_head(qh, kh, vh, oh, lseh, doh, causal, T_valid, rope_on, docs=Non
     S = (qr @ kr.T) / math.sqrt(d)
     ok = allowed(pos, pos, causal, T_valid, docs)
     P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lseh[:, None]), 0.0)
-    dV = P.T @ doh
+    dV = allowed_sum(P.T, ok.T, doh)
     dP = doh @ vh.T
     D = np.sum(doh * oh, axis=1)
-    dS = P * (dP - D[:, None])
-    dQr = dS @ kr / math.sqrt(d)
-    dKr = dS.T @ qr / math.sqrt(d)
+    dS = np.where(ok, P * (dP - D[:, None]), 0.0)
+    dQr = allowed_sum(dS, ok, kr) / math.sqrt(d)
+    dKr = allowed_sum(dS.T, ok.T, qr) / math.sqrt(d)
     if rope_on:
         return rope_transpose(dQr, pos, _spec(rope_on)), rope_transpose(dKr, pos, _spec(rope_on)), dV
     return dQr, dKr, dV
@@ -309,7 +327,7 @@ def backward_dq_rows(q, k, v, do, b: int, h: int, rows, causal: bool = True,
     P = np.where(ok, np.exp(np.where(ok, S, 0.0) - lse_r[:, None]), 0.0)
     dP = doh[rows] @ vh.T
     D = np.sum(doh[rows] * o_r, axis=1)
-    dQr = (P * (dP - D[:, None])) @ kr / math.sqrt(d)
+    dQr = allowed_sum(np.where(ok, P * (dP - D[:, None]), 0.0), ok, kr) / math.sqrt(d)
     return rope_transpose(dQr, rows, _spec(rope_on)) if rope_on else dQr
 
 
@@ -343,10 +361,10 @@ def backward_dkdv_cols(q, k, v, do, b: int, h: int, cols, causal: bool = True,
         ok = allowed(pos, cols, causal, T_valid, docs)      # [T, n_cols]
         S = (qr @ kr[cols].T) / math.sqrt(d)
         P = np.where(ok, np.exp(np.where(ok, S, 0.0) - L[:, None]), 0.0)
-        dV += P.T @ doh
+        dV += allowed_sum(P.T, ok.T, doh)
         dP = doh @ vh[cols].T
-        dS = P * (dP - D[:, None])
-        dK += dS.T @ qr / math.sqrt(d)
+        dS = np.where(ok, P * (dP - D[:, None]), 0.0)
+        dK += allowed_sum(dS.T, ok.T, qr) / math.sqrt(d)
     return (rope_transpose(dK, cols, _spec(rope_on)) if rope_on else dK), dV
 
 
@@ -360,11 +378,12 @@ def merge(o_a: np.ndarray, l_a: np.ndarray, o_b: np.ndarray, l_b: np.ndarray):
     empty partials give (-inf, 0).
     """
     l_a, l_b = np.asarray(l_a, np.float64), np.asarray(l_b, np.float64)
-    m = np.maximum(l_a, l_b)
-    empty = ~np.isfinite(m)
+    none_a, none_b = l_a == -np.inf, l_b == -np.inf     # partials that saw no key
+    empty = none_a & none_b
+    m = np.maximum(l_a, l_b)                           # a NaN LSE stays NaN
     m_safe = np.where(empty, 0.0, m)
-    wa = np.where(np.isfinite(l_a), np.exp(l_a - m_safe), 0.0)
-    wb = np.where(np.isfinite(l_b), np.exp(l_b - m_safe), 0.0)
+    wa = np.where(none_a, 0.0, np.exp(l_a - m_safe))
+    wb = np.where(none_b, 0.0, np.exp(l_b - m_safe))
     tot = wa + wb
     L = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, tot)))
     scale_a = np.where(empty, 0.0, wa / np.where(empty, 1.0, tot))

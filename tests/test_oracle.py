@@ -359,6 +359,80 @@ def test_planted_merge_many_mistakes_are_caught():
             assert not check_merge_many(bad) < 1e-6, bad.__name__
 
 
+# ------------------------------------------------- non-finite inputs ----
+# The sums of attention run over allowed pairs only, so a NaN or an Inf in an
+# input reaches exactly the outputs whose allowed pairs hold it: every other
+# output equals the result on the same inputs with that value made finite.
+
+def _poisoned(T=12, d=4, t0=5, j0=7):
+    q, k, v, do = (rnd(1, 1, T, d) for _ in range(4))
+    qn, vi = q.copy(), v.copy()
+    qn[0, 0, t0, 1] = np.nan
+    vi[0, 0, j0, 2] = np.inf
+    return q, k, v, do, qn, vi, t0, j0
+
+
+def check_nonfinite(forward, backward):
+    """0 if NaN / Inf inputs reach exactly the outputs that see them, else 1."""
+    q, k, v, do, qn, vi, t0, j0 = _poisoned()
+    T = q.shape[2]
+    with np.errstate(invalid="ignore", over="ignore"):
+        O0, L0 = forward(q, k, v, True, T)
+        g0 = backward(q, k, v, O0, L0, do, True, T)
+        # NaN in q[t0]: O, LSE, dq of row t0; dk, dv of keys j <= t0
+        O, L = forward(qn, k, v, True, T)
+        dq, dk, dv = backward(qn, k, v, O, L, do, True, T)
+        rows = np.arange(T) != t0
+        ok = (np.all(~np.isfinite(O[0, 0, t0])) and np.isnan(L[0, 0, t0])
+              and np.allclose(O[0, 0, rows], O0[0, 0, rows], rtol=0, atol=1e-13)
+              and np.allclose(L[0, 0, rows], L0[0, 0, rows], rtol=0, atol=1e-13)
+              and np.all(np.isnan(dq[0, 0, t0]))
+              and np.allclose(dq[0, 0, rows], g0[0][0, 0, rows], rtol=0, atol=1e-12))
+        for g, g_ref in ((dk, g0[1]), (dv, g0[2])):
+            ok = ok and np.all(~np.isfinite(g[0, 0, :t0 + 1])) and np.allclose(
+                g[0, 0, t0 + 1:], g_ref[0, 0, t0 + 1:], rtol=0, atol=1e-12)
+        # +Inf in v[j0, 2]: column 2 of O for rows t >= j0; D, hence dq rows
+        # t >= j0 and every dk row (the last query sees every key); dv untouched
+        O, L = forward(q, k, vi, True, T)
+        dq, dk, dv = backward(q, k, vi, O, L, do, True, T)
+        fin = np.ones((T, q.shape[3]), bool)
+        fin[j0:, 2] = False
+        ok = ok and (np.array_equal(np.isfinite(O[0, 0]), fin) and np.all(O[0, 0, j0:, 2] == np.inf)
+                     and np.allclose(O[0, 0][fin], O0[0, 0][fin], rtol=0, atol=1e-13)
+                     and np.allclose(L, L0, rtol=0, atol=1e-13)
+                     and np.all(~np.isfinite(dq[0, 0, j0:]))
+                     and np.allclose(dq[0, 0, :j0], g0[0][0, 0, :j0], rtol=0, atol=1e-12)
+                     and np.all(~np.isfinite(dk)) and np.allclose(dv, g0[2], rtol=0, atol=1e-12))
+    return 0 if ok else 1
+
+
+def test_nonfinite_inputs_reach_only_the_outputs_that_see_them():
+    assert check_nonfinite(A.forward, A.backward) == 0
+
+
+def test_planted_nonfinite_mistakes_are_caught(monkeypatch):
+    def dense(W, ok, X):                                      # masked pairs as zeros of a dense product
+        return np.where(ok, W, 0.0) @ X
+    monkeypatch.setattr(A, "allowed_sum", dense)
+    assert check_nonfinite(A.forward, A.backward) == 1
+    monkeypatch.undo()
+    real_pa = A.partial_attention
+
+    def nan_row_is_empty(qr, kr, vr, q_pos, k_pos, causal, T_valid, docs=None):
+        O, L = real_pa(qr, kr, vr, q_pos, k_pos, causal, T_valid, docs)
+        bad = ~np.isfinite(L)
+        return np.where(bad[:, None], 0.0, O), np.where(bad, -np.inf, L)
+    monkeypatch.setattr(A, "partial_attention", nan_row_is_empty)
+    assert check_nonfinite(A.forward, A.backward) == 1
+
+
+def test_merge_keeps_nan_and_empty_apart():
+    o, l = rnd(3, 2), np.array([0.5, np.nan, -np.inf])
+    O, L = A.merge(o, l, np.zeros((3, 2)), np.full(3, -np.inf))
+    assert L[0] == 0.5 and np.isnan(L[1]) and L[2] == -np.inf
+    assert np.all(np.isnan(O[1])) and np.all(O[2] == 0.0)
+
+
 # ------------------------------------------------------------ backward ----
 
 def check_gradients_fd(bwd, causal, T_valid, rope_on, h=1e-6):
