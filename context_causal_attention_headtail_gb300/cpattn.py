@@ -25,7 +25,8 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_sync_status", "cpattn_version", "cpattn_set_trace_events", "cpattn_bwd_noalloc",
            "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
            "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen", "cpattn_ulysses_a2a",
-           "cpattn_ulysses_a2a_rope", "cpattn_fwd_rope_cfg", "cpattn_bwd_rope_cfg")
+           "cpattn_ulysses_a2a_rope", "cpattn_fwd_rope_cfg", "cpattn_bwd_rope_cfg",
+           "cpattn_check_wait_timeout")
 
 
 class CpattnError(RuntimeError):
@@ -73,6 +74,7 @@ def _declare(lib):
         "cpattn_bwd_rope_cfg": [_vp] * 10 + [_i] * 8 + [_c.POINTER(RopeCfg), _i, _vp],
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
+        "cpattn_check_wait_timeout": [_c.c_ulonglong, _vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
     }
     for name, args in sig.items():
@@ -215,6 +217,10 @@ def cpattn_merge(o_parts, lse_parts, o, lse, B, H, T, d, dt, stream=None):
 
 def cpattn_sync_status(stream=None):
     _check(lib().cpattn_sync_status(stream))
+
+
+def cpattn_check_wait_timeout(limit_ns, stream=None):
+    _check(lib().cpattn_check_wait_timeout(limit_ns, stream))
 
 
 def cpattn_set_trace_events(events):

@@ -243,6 +243,13 @@ cpattn_status cpattn_sync_status(cpattn_stream_t stream) {
   return CPATTN_OK;
 }
 
+cpattn_status cpattn_check_wait_timeout(unsigned long long limit_ns, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (limit_ns < 1000ull || limit_ns > 1000000000ull)
+    return fail(CPATTN_ERR_ARG, "limit_ns=%llu must be in [1e3, 1e9]", limit_ns);
+  return launch_wait_probe(limit_ns, reinterpret_cast<cudaStream_t>(stream));
+}
+
 cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host) {
   g_msg[0] = 0;
   if (!idx_host) return fail(CPATTN_ERR_ARG, "idx_host is NULL");

@@ -94,6 +94,10 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
                                const void *dO, void *dq, void *dk, void *dv, float *D,
                                const Geometry &g, cudaStream_t s);
 
+// One thread waits on an mbarrier that nothing arrives at, with the given
+// limit, so that the bounded wait expires (diagnostics.cu).
+cpattn_status launch_wait_probe(unsigned long long limit_ns, cudaStream_t s);
+
 // Tracing events registered by cpattn_set_trace_events for this host thread:
 // records event i on stream s if one is registered (no-op otherwise).
 void trace_record(int i, cudaStream_t s);

@@ -59,12 +59,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Shared state for bounded waits: a CTA-wide abort flag in shared memory and
-// the device error flag. A wait that has not completed after kWaitLimitNs,
+// the device error flag. A wait that has not completed after limit_ns
+// (kWaitLimitNs in every attention kernel),
 // or that sees another role abort, records the failure and returns false; its
 // caller then leaves its loop and the kernel runs its teardown.
 struct WaitCtx {
-  volatile int *abort;  // shared memory
-  int *err;             // global memory
+  volatile int *abort;              // shared memory
+  int *err;                         // global memory
+  uint64_t limit_ns = kWaitLimitNs;
 };
 
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, WaitCtx w) {
@@ -74,7 +76,7 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*w.abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > w.limit_ns) {
       *w.abort = 1;
       if (w.err) atomicOr(w.err, ERR_FLAG_TIMEOUT);
       return false;

@@ -318,6 +318,17 @@ const char *cpattn_last_error(void);
  * check, CPATTN_ERR_CUDA if the stream reports an error, else CPATTN_OK. */
 cpattn_status cpattn_sync_status(cpattn_stream_t stream);
 
+/* Exercises the bounded-wait path on the device ("Fused Linear LogP TP Test
+ * Runbook", hang triage: a stuck wait must surface as an error, not a hang).
+ * Enqueues one single-thread kernel that waits, with the same bounded wait
+ * every attention kernel uses, on an mbarrier that nothing arrives at; after
+ * limit_ns nanoseconds (1e3 <= limit_ns <= 1e9, else CPATTN_ERR_ARG) the wait
+ * gives up, sets the device error flag and the kernel returns. Nothing else is
+ * in flight, so the context stays usable: the next cpattn_sync_status(stream)
+ * returns CPATTN_ERR_TIMEOUT and clears the flag, and later calls work as
+ * before. The attention kernels wait up to 2 s. */
+cpattn_status cpattn_check_wait_timeout(unsigned long long limit_ns, cpattn_stream_t stream);
+
 /* Tracing hook for timing single kernels inside a longer region. Registers
  * up to 8 caller-created CUDA events (cudaEvent_t handles, borrowed, never
  * destroyed here) that later calls from this host thread record on their

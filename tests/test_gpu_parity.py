@@ -305,7 +305,7 @@ def test_ulysses_32k_sampled():
     got = run_gpu_ulysses(w, inp)
     for g in ("o", "lse", "dq", "dk", "dv"):
         assert torch.isfinite(got[g]).all(), g
-    _sampled_check(w, inp, got, [(0, 0), (0, 7), (0, 15)], kv_head=(0, 9))
+    _sampled_check(w, inp, got, [(0, 0), (0, 7), (0, 15)], kv_heads=[(0, 9), (0, 2)])
 
 
 def test_shard_index_matches_oracle():
@@ -430,7 +430,7 @@ def test_merge_against_oracle(n, d, dtype):
 
 # ------------------------------------------------- full-size workloads ----
 
-def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
+def _sampled_check(w, inp, got, heads, kv_heads, n_random=24):
     tol = TOL[w.dtype]
     q, k, v, do = (inp[n] for n in ("q", "k", "v", "do"))
     rows = sample_rows(w, n_random, seed=w.T)
@@ -443,11 +443,11 @@ def _sampled_check(w, inp, got, heads, kv_head, n_random=24):
         dq_r = A.backward_dq_rows(q, k, v, do, b, h, real, w.causal, w.T_valid, oracle_rope(w),
                                   docs=oracle_docs(w))
         compare(f"dq[{b},{h}]", got["dq"][b, h, real], dq_r, tol["grad"], tol["cos"])
-    b, h = kv_head
-    dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, oracle_rope(w),
-                                      docs=oracle_docs(w))
-    compare(f"dk[{b},{h}]", got["dk"][b, h, rows], dk_c, tol["grad"], tol["cos"])
-    compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
+    for b, h in kv_heads:
+        dk_c, dv_c = A.backward_dkdv_cols(q, k, v, do, b, h, rows, w.causal, w.T_valid, oracle_rope(w),
+                                          docs=oracle_docs(w))
+        compare(f"dk[{b},{h}]", got["dk"][b, h, rows], dk_c, tol["grad"], tol["cos"])
+        compare(f"dv[{b},{h}]", got["dv"][b, h, rows], dv_c, tol["grad"], tol["cos"])
 
 
 @pytest.mark.parametrize("name,mode", [("gpt2_small", "shard"), ("gpt2_small", "kernel"),
@@ -464,7 +464,7 @@ def test_workload_full_size_sampled(name, mode):
     for g in ("o", "lse", "dq", "dk", "dv"):
         assert torch.isfinite(got[g][:, :, : w.T_valid]).all(), g
     heads = [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]
-    _sampled_check(w, inp, got, heads, kv_head=(w.B - 1, w.kv_heads // 3))
+    _sampled_check(w, inp, got, heads, kv_heads=[(w.B - 1, w.kv_heads // 3), (0, w.kv_heads - 1)])
     if w.T_valid < w.T:
         for g in ("dq", "dk", "dv"):
             assert torch.count_nonzero(got[g][:, :, w.T_valid:]) == 0, g

@@ -75,6 +75,12 @@ def test_fwd_validation(lib, args, status):
     assert cpattn.cpattn_last_error() != ""
 
 
+def test_wait_probe_limit_is_validated(lib):
+    for bad in (0, 999, 10 ** 9 + 1):
+        assert lib.cpattn_check_wait_timeout(bad, None) == cpattn.ERR_ARG
+        assert "limit_ns" in cpattn.cpattn_last_error()
+
+
 def test_bwd_and_merge_validation(lib):
     ws = cpattn.cpattn_bwd_workspace_bytes(2, 4096, 12, 64)
     assert ws >= 2 * 4096 * 12 * 4 and ws % 256 == 0
