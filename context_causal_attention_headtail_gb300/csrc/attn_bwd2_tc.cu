@@ -164,9 +164,9 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
-  const int bh = blockIdx.x % p.BH;
+  const int bh = blockIdx.x / (2 * cp * tpc);     // heads vary slowest (K/V tiles shared in L2)
   const int bkv = bh / p.group;                   // K/V head of this query head
-  const int g = blockIdx.x / p.BH;
+  const int g = blockIdx.x % (2 * cp * tpc);
   const int kq = 2 * cp - 1 - g / tpc;
   const int qt = tpc - 1 - g % tpc;
   int rq, hq;
@@ -487,9 +487,10 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
-  const int BHkv = p.BH / p.group;
-  const int bkv = blockIdx.x % BHkv;  // K/V head; its group's query heads are bkv*group + [0, group)
-  const int g = blockIdx.x / BHkv;
+  // K/V head, varying slowest so that the CTAs in flight share its query
+  // heads' Q/dO tiles in L2; its group's query heads are bkv*group + [0, group)
+  const int bkv = blockIdx.x / (2 * cp * tpc);
+  const int g = blockIdx.x % (2 * cp * tpc);
   const int kk_chunk = g / tpc;     // earliest keys first: they are seen by the most queries
   const int kt = g % tpc;
   int rk, hk;
@@ -814,19 +815,21 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 }
 
 template <int D, bool ROPE>
-cpattn_status launch_bwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
+cpattn_status launch_dkdv2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                             const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
   constexpr int threads = ROPE ? 384 : 320;
-  {
-    constexpr int smem = Dkdv3Cfg<D>::SMEM;
-    auto kern = dkdv2_tc_kernel<D, ROPE>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
-    kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
-    cpattn_status st = check_launch("tensor-core dK/dV kernel (pipelined)");
-    if (st != CPATTN_OK) return st;
-    trace_record(2, s);
-  }
+  constexpr int smem = Dkdv3Cfg<D>::SMEM;
+  auto kern = dkdv2_tc_kernel<D, ROPE>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
+  kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
+  return check_launch("tensor-core dK/dV kernel (pipelined)");
+}
+
+template <int D, bool ROPE>
+cpattn_status launch_dq2_t(const CUtensorMap &mk, const CUtensorMap &mv, const Bwd2Params &bp, unsigned grid,
+                           cudaStream_t s) {
+  constexpr int threads = ROPE ? 384 : 320;
   constexpr int smem = Dq3Cfg<D>::SMEM;
   auto kern = dq2_tc_kernel<D, ROPE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -871,11 +874,21 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   make_rope_theta(g.d, &bp.theta, g.rope_cfg);
   const long long grid = BH * 2 * g.cp * bp.tpc;
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
+  const unsigned gr = (unsigned)grid;
+  cpattn_status st;
   if (g.d == 128)
-    return g.rope ? launch_bwd2_t<128, true>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
-                  : launch_bwd2_t<128, false>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
-  return g.rope ? launch_bwd2_t<64, true>(mq, mk, mv, mdo, bp, (unsigned)grid, s)
-                : launch_bwd2_t<64, false>(mq, mk, mv, mdo, bp, (unsigned)grid, s);
+    st = g.rope ? launch_dkdv2_t<128, true>(mq, mk, mv, mdo, bp, gr, s)
+                : launch_dkdv2_t<128, false>(mq, mk, mv, mdo, bp, gr, s);
+  else
+    st = g.rope ? launch_dkdv2_t<64, true>(mq, mk, mv, mdo, bp, gr, s)
+                : launch_dkdv2_t<64, false>(mq, mk, mv, mdo, bp, gr, s);
+  if (st != CPATTN_OK) return st;
+  trace_record(2, s);
+  // dQ: CTA pairs with two-SM MMAs at d = 128 (inputs already rotated); the
+  // one-CTA pipelined kernel otherwise.
+  if (g.d == 128 && !g.rope) return launch_dq_pair_bf16(q, k, v, lse, dO, dq, D, g, s);
+  if (g.d == 128) return launch_dq2_t<128, true>(mk, mv, bp, gr, s);
+  return g.rope ? launch_dq2_t<64, true>(mk, mv, bp, gr, s) : launch_dq2_t<64, false>(mk, mv, bp, gr, s);
 }
 
 }  // namespace cpattn

@@ -710,12 +710,12 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 
 }  // namespace
 
-bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots) {
+bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots, int box_rows) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)c, (cuuint64_t)n_slots};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)c * D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

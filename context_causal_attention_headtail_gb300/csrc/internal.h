@@ -109,7 +109,13 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 // 3-D tensor map over a sharded [B*H*2cp chunk slots][c rows][D] bf16 tensor,
-// box {64 columns, 128 rows, 1 slot}, 128-byte swizzle, zero fill past row c.
-bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots);
+// box {64 columns, box_rows rows, 1 slot}, 128-byte swizzle, zero fill past row c.
+bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_slots, int box_rows = 128);
+
+// dQ of the pipelined backward by CTA pairs (two-SM MMAs), d = 128, inputs
+// already rotated (attn_dq_pair.cu); D = rowsum(dO * O) precomputed.
+cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, const float *lse,
+                                  const void *dO, void *dq, const float *D, const Geometry &g,
+                                  cudaStream_t s);
 
 }  // namespace cpattn
