@@ -117,7 +117,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-merge", action="store_true", help="skip timing the standalone merge kernel")
     ap.add_argument("--rope-in-kernel", action="store_true",
-                    help="rotate q, k inside the attention kernels (rope=1) instead of in shard/unshard")
+                    help="rotate q, k inside the attention calls (cpattn_fwd_rope_save / cpattn_bwd_rotated) "
+                         "instead of in shard/unshard")
     return ap.parse_args()
 
 
@@ -436,10 +437,14 @@ def run_ours(args):
     # and dq, dk (default), or applied inside the attention kernels.
     fused = w.rope and not args.rope_in_kernel
     rope_flag = w.rope and not fused
-    if w.packed and not fused and w.rope:
-        raise SystemExit("packed documents take RoPE from the shard / unshard passes; drop --rope-in-kernel")
+    if rope_flag and P:
+        raise SystemExit("the Ulysses workload takes RoPE from its all-to-all; drop --rope-in-kernel")
     rope_cfg = (cpattn.RopeCfg(factor=w.yarn_factor, original_max_position=w.yarn_original)
                 if w.yarn else None)
+    # in-kernel RoPE: the forward rotates as it streams and stores the rotated
+    # q, k, which the backward reads in place of q, k
+    q_rot = torch.empty_like(sh["q"]) if rope_flag else None
+    k_rot = torch.empty_like(sh["k"]) if rope_flag else None
     docs = cu_dev = cu_host = None
     if w.packed:          # cu_seqlens -> per-position document bounds, every step
         cu_host = torch.from_numpy(w.cu_seqlens()).pin_memory()
@@ -461,12 +466,19 @@ def run_ours(args):
             cpattn.doc_bounds(cu_dev, w.T, docs[0], docs[1], stream)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["fwd"]])
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, cp_attn, w.T_valid, w.causal, rope_flag, stream,
-                   docs=docs, rope_cfg=rope_cfg if rope_flag else None)
+        if rope_flag:
+            cpattn.fwd_rope_save(sh["q"], sh["k"], sh["v"], o, lse, q_rot, k_rot, cp_attn, w.T_valid, w.causal,
+                                 stream, docs=docs, rope_cfg=rope_cfg)
+        else:
+            cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, cp_attn, w.T_valid, w.causal, False, stream, docs=docs)
         if evs:
             cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["bwd"]])
-        cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
-                   w.causal, rope_flag, stream, docs=docs, rope_cfg=rope_cfg if rope_flag else None)
+        if rope_flag:
+            cpattn.bwd_rotated(q_rot, k_rot, sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
+                               w.causal, stream, docs=docs, rope_cfg=rope_cfg)
+        else:
+            cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
+                       w.causal, False, stream, docs=docs)
         for i, name in enumerate(("o", "dq", "dk", "dv")):
             if evs:
                 cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
@@ -666,7 +678,8 @@ def run_ours(args):
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {**workload_config(w), "parallelism": f"replica per GPU x{world}",
                            "rope_path": ("fused into shard/unshard" if fused else
-                                         "inside the attention kernels" if rope_flag else "none")},
+                                         "inside the attention kernels (forward stores the rotated q, k)"
+                                         if rope_flag else "none")},
                 "tokens_per_s": world * w.B * w.T_valid / (ms * 1e-3),
                 "frac_of_bf16_peak": value / world / peaks["bf16_tflops"],
                 "frac_of_bf16_peak_sustained": value / world / peaks["bf16_tflops_sustained"],

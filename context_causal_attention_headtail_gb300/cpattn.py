@@ -26,7 +26,7 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
            "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen", "cpattn_ulysses_a2a",
            "cpattn_ulysses_a2a_rope", "cpattn_fwd_rope_cfg", "cpattn_bwd_rope_cfg",
-           "cpattn_check_wait_timeout")
+           "cpattn_check_wait_timeout", "cpattn_fwd_rope_save", "cpattn_bwd_rotated")
 
 
 class CpattnError(RuntimeError):
@@ -75,6 +75,8 @@ def _declare(lib):
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
         "cpattn_check_wait_timeout": [_c.c_ulonglong, _vp],
+        "cpattn_fwd_rope_save": [_vp] * 7 + [_i] * 8 + [_vp, _vp, _c.POINTER(RopeCfg), _i, _vp],
+        "cpattn_bwd_rotated": [_vp] * 10 + [_i] * 8 + [_vp, _vp, _c.POINTER(RopeCfg), _i, _vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
     }
     for name, args in sig.items():
@@ -174,6 +176,19 @@ def cpattn_bwd_rope_cfg(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_vali
     _check(lib().cpattn_bwd_rope_cfg(q, k, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv,
                                      d, cp, causal, None if cfg is None else ctypes.byref(cfg), dt,
                                      stream))
+
+
+def cpattn_fwd_rope_save(q, k, v, o, lse, q_rot, k_rot, B, T, T_valid, H, H_kv, d, cp, causal, doc_lo, doc_hi,
+                         cfg, dt, stream=None):
+    _check(lib().cpattn_fwd_rope_save(q, k, v, o, lse, q_rot, k_rot, B, T, T_valid, H, H_kv, d, cp, causal,
+                                      doc_lo, doc_hi, None if cfg is None else ctypes.byref(cfg), dt, stream))
+
+
+def cpattn_bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal,
+                       doc_lo, doc_hi, cfg, dt, stream=None):
+    _check(lib().cpattn_bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d,
+                                    cp, causal, doc_lo, doc_hi, None if cfg is None else ctypes.byref(cfg), dt,
+                                    stream))
 
 
 def cpattn_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, stream=None):
@@ -381,6 +396,28 @@ def bwd(q, k, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=Tru
         cpattn_bwd(*args, H, *tail)
     else:
         cpattn_bwd_gqa(*args, H, H_kv, *tail)
+
+
+def fwd_rope_save(q, k, v, o, lse, q_rot, k_rot, cp, T_valid=None, causal=True, stream=None, docs=None,
+                  rope_cfg: RopeCfg | None = None):
+    """fwd with in-kernel RoPE that also stores the rotated q_rot, k_rot for bwd_rotated."""
+    B, H, T, d = q.shape
+    H_kv = _kv_heads(q, k, v, k_rot)
+    cpattn_fwd_rope_save(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(q_rot), _ptr(k_rot), B, T,
+                         T if T_valid is None else T_valid, H, H_kv, d, cp, int(causal),
+                         None if docs is None else _ptr(docs[0]), None if docs is None else _ptr(docs[1]),
+                         rope_cfg, _dtype_code(q), _stream(stream))
+
+
+def bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=None, causal=True, stream=None,
+                docs=None, rope_cfg: RopeCfg | None = None):
+    """dq, dk, dv with respect to the unrotated q, k, from the rotated copies that fwd_rope_save stored."""
+    B, H, T, d = q_rot.shape
+    H_kv = _kv_heads(q_rot, k_rot, v, dk, dv)
+    cpattn_bwd_rotated(_ptr(q_rot), _ptr(k_rot), _ptr(v), _ptr(o), _ptr(lse), _ptr(dO), _ptr(dq), _ptr(dk),
+                       _ptr(dv), _ptr(workspace), B, T, T if T_valid is None else T_valid, H, H_kv, d, cp,
+                       int(causal), None if docs is None else _ptr(docs[0]), None if docs is None else _ptr(docs[1]),
+                       rope_cfg, _dtype_code(q_rot), _stream(stream))
 
 
 def merge(o_parts, lse_parts, o, lse, stream=None):

@@ -375,7 +375,8 @@ cpattn_status cpattn_fwd(const void *q, const void *k, const void *v, void *o, f
 static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
                               int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
-                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg = nullptr);
+                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg = nullptr,
+                              void *q_rot = nullptr, void *k_rot = nullptr);
 
 cpattn_status cpattn_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
                              int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
@@ -407,7 +408,8 @@ cpattn_status cpattn_fwd_rope_cfg(const void *q, const void *k, const void *v, v
 static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
                               int rope, const int *doc_lo, const int *doc_hi, cpattn_dtype dt,
-                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg) {
+                              cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg, void *q_rot,
+                              void *k_rot) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse) return fail(CPATTN_ERR_ARG, "null pointer");
   cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, rope, dt);
@@ -425,6 +427,8 @@ static cpattn_status fwd_impl(const void *q, const void *k, const void *v, void 
   g.doc_lo = doc_lo;
   g.doc_hi = doc_hi;
   g.rope_cfg = rope_cfg;
+  g.q_rot = q_rot;
+  g.k_rot = k_rot;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   trace_record(0, s);
   if (dt == CPATTN_F32)
@@ -456,7 +460,7 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
                               void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                               int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
                               cpattn_dtype dt, cpattn_stream_t stream,
-                              const cpattn_rope_cfg *rope_cfg = nullptr);
+                              const cpattn_rope_cfg *rope_cfg = nullptr, bool rope_epi = false);
 
 cpattn_status cpattn_bwd_gqa(const void *q, const void *k, const void *v, const void *o,
                              const float *lse, const void *dO, void *dq, void *dk, void *dv,
@@ -507,7 +511,8 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
                               const float *lse, const void *dO, void *dq, void *dk, void *dv,
                               void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
                               int cp, int causal, int rope, const int *doc_lo, const int *doc_hi,
-                              cpattn_dtype dt, cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg) {
+                              cpattn_dtype dt, cpattn_stream_t stream, const cpattn_rope_cfg *rope_cfg,
+                              bool rope_epi) {
   g_msg[0] = 0;
   if (!q || !k || !v || !o || !lse || !dO || !dq || !dk || !dv || !workspace)
     return fail(CPATTN_ERR_ARG, "null pointer");
@@ -538,6 +543,7 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
   g.doc_lo = doc_lo;
   g.doc_hi = doc_hi;
   g.rope_cfg = rope_cfg;
+  g.rope_epi = rope_epi;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
   trace_record(0, s);
@@ -553,6 +559,66 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
     st = launch_bwd_bf16(q, k, v, o, lse, dO, dq, dk, dv, D, g, s);
   trace_record(3, s);
   return st;
+}
+
+// ------------------------------------------- in-kernel RoPE, rotated once
+static bool uses_tables(int T, int cp) {
+  const long long tpc = ((long long)T / (2 * cp) + 127) / 128;
+  return 2LL * cp * tpc <= kTableTiles;
+}
+
+cpattn_status cpattn_fwd_rope_save(const void *q, const void *k, const void *v, void *o, float *lse, void *q_rot,
+                                   void *k_rot, int B, int T, int T_valid, int H, int H_kv, int d, int cp,
+                                   int causal, const int32_t *doc_lo, const int32_t *doc_hi,
+                                   const cpattn_rope_cfg *cfg, cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if (!q_rot || !k_rot) return fail(CPATTN_ERR_ARG, "q_rot and k_rot must not be NULL");
+  if ((doc_lo == nullptr) != (doc_hi == nullptr)) return fail(CPATTN_ERR_ARG, "give both document bounds or neither");
+  if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
+  cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, 1, dt);
+  if (st != CPATTN_OK) return st;
+  if ((st = check_heads(H, H_kv)) != CPATTN_OK) return st;
+  if (!aligned16(q_rot) || !aligned16(k_rot)) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+  const size_t elt = dt == CPATTN_F32 ? 4 : 2;
+  const size_t tq = (size_t)B * H * T * d * elt, tkv = (size_t)B * H_kv * T * d * elt;
+  const void *bufs[] = {q, k, v, o, lse, q_rot, k_rot};
+  const size_t sizes[] = {tq, tkv, tkv, tq, (size_t)B * H * T * 4, tq, tkv};
+  for (int i = 5; i < 7; ++i)
+    for (int j = 0; j < 7; ++j)
+      if (i != j && bufs[j] && overlaps(bufs[i], sizes[i], bufs[j], sizes[j]))
+        return fail(CPATTN_ERR_ARG, "q_rot and k_rot must not overlap each other, the inputs or the outputs");
+  if (dt == CPATTN_BF16 && uses_tables(T, cp))   // rotated tiles stored by the attention kernel itself
+    return fwd_impl(q, k, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, 1, doc_lo, doc_hi, dt, stream, cfg,
+                    q_rot, k_rot);
+  // fp32, or a schedule past the tile tables: rotate first, then attend with rope = 0
+  Geometry g = geometry(B, H, T, T, d, cp, 1, 1, H_kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_rope_sharded(q, q_rot, g, H, dt, false, cfg, s)) != CPATTN_OK) return st;
+  if ((st = launch_rope_sharded(k, k_rot, g, H_kv, dt, false, cfg, s)) != CPATTN_OK) return st;
+  return fwd_impl(q_rot, k_rot, v, o, lse, B, T, T_valid, H, H_kv, d, cp, causal, 0, doc_lo, doc_hi, dt, stream);
+}
+
+cpattn_status cpattn_bwd_rotated(const void *q_rot, const void *k_rot, const void *v, const void *o,
+                                 const float *lse, const void *dO, void *dq, void *dk, void *dv, void *workspace,
+                                 int B, int T, int T_valid, int H, int H_kv, int d, int cp, int causal,
+                                 const int32_t *doc_lo, const int32_t *doc_hi, const cpattn_rope_cfg *cfg,
+                                 cpattn_dtype dt, cpattn_stream_t stream) {
+  g_msg[0] = 0;
+  if ((doc_lo == nullptr) != (doc_hi == nullptr)) return fail(CPATTN_ERR_ARG, "give both document bounds or neither");
+  if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
+  cpattn_status st = check_attn(B, T, T_valid, H, d, cp, causal, 1, dt);   // RoPE needs d in {64, 128}
+  if (st != CPATTN_OK) return st;
+  if (dt == CPATTN_BF16 && uses_tables(T, cp))   // R^T in the dQ and dK epilogues
+    return bwd_impl(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal, 0,
+                    doc_lo, doc_hi, dt, stream, cfg, true);
+  // fp32, or a schedule past the tile tables: dq', dk' from the rope = 0 kernels, then R^T in place
+  st = bwd_impl(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d, cp, causal, 0,
+                doc_lo, doc_hi, dt, stream);
+  if (st != CPATTN_OK) return st;
+  Geometry g = geometry(B, H, T, T, d, cp, 1, 1, H_kv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = launch_rope_sharded(dq, dq, g, H, dt, true, cfg, s)) != CPATTN_OK) return st;
+  return launch_rope_sharded(dk, dk, g, H_kv, dt, true, cfg, s);
 }
 
 // --------------------------------------------------- allocation-free backward

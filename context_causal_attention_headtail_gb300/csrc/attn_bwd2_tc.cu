@@ -73,45 +73,6 @@ __device__ __forceinline__ void rope_row_words(uint32_t *w, int pos, const RopeT
   }
 }
 
-// Stores scale * m R^T of one pair of 32-column chunks of a TMEM row (m the
-// attention temperature of the RoPE configuration, 1 for the standard one): columns
-// 32a..32a+31 and their rotation partners D/2 further on (frequencies
-// 32a..32a+31), for the key or query at natural position pos, as bf16 at
-// dst + the same columns (every lane of the warp must call this).
-template <int D>
-__device__ __forceinline__ void store_tmem_pair_rope(uint32_t t_col0, int a, float scale, int pos,
-                                                     const RopeTheta &th, __nv_bfloat16 *dst, bool valid) {
-  uint32_t ra[32], rb[32];
-  tc::tmem_ld32(t_col0 + 32 * a, ra);
-  tc::tmem_ld32(t_col0 + 32 * a + D / 2, rb);
-  tc::tmem_ld_wait();
-  uint32_t pa[16], pb[16];
-#pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    float o[2][2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float sn, cs;
-      rope_sincos(pos, th.hi[32 * a + e + u], th.lo[32 * a + e + u], sn, cs);
-      sn *= th.mscale;
-      cs *= th.mscale;
-      const float x = __uint_as_float(ra[e + u]) * scale, y = __uint_as_float(rb[e + u]) * scale;
-      o[0][u] = fmaf(x, cs, y * sn);    // R^T: x cos + y sin
-      o[1][u] = fmaf(y, cs, -x * sn);   //      y cos - x sin
-    }
-    pa[e / 2] = pack_bf16x2(o[0][0], o[0][1]);
-    pb[e / 2] = pack_bf16x2(o[1][0], o[1][1]);
-  }
-  if (valid) {
-    uint4 *da = reinterpret_cast<uint4 *>(dst + 32 * a), *db = reinterpret_cast<uint4 *>(dst + 32 * a + D / 2);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      da[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
-      db[v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
-    }
-  }
-}
-
 // ================================================================== dQ
 // Query-stationary. TMEM: Q (bf16 A operand) 0, dO 64, S 128, dP 256, dQ 384.
 // Warpgroup h owns key columns [64h, 64h+64) of each tile and writes its
@@ -139,7 +100,7 @@ struct Dq3Cfg {
   static constexpr uint32_t colQ = 0, colDO = 64, colS = 128, colDP = 256, colDQ = 384;
 };
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool EPI = false>
 __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     dq2_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ Bwd2Params p) {
@@ -403,7 +364,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done, (n - 1) & 1, wc));
       if (ok) {
         tc::tc_fence_after();
-        if (!ROPE)
+        if (!ROPE && !EPI)
           store_tmem_cols(t_row + C::colDQ, h * (D / 2), D / 64, p.scale, p.dq + grow * D, valid);
         else if (D == 128 || h == 0)   // warpgroup h: frequencies 32h..32h+31 (D = 64: warpgroup 0, all 32)
           store_tmem_pair_rope<D>(t_row + C::colDQ, h, p.scale, q_pos, p.theta, p.dq + grow * D, valid);
@@ -454,7 +415,7 @@ struct Dkdv3Cfg {
   static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
 };
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool EPI = false>
 __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     dkdv2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -790,7 +751,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dk_done, (n - 1) & 1, wc));
         if (ok) {
           tc::tc_fence_after();
-          if (ROPE && h == 1) {   // dK = R^T dK' at the key's position
+          if ((ROPE || EPI) && h == 1) {   // dK = R^T dK' at the key's position
 #pragma unroll 1
             for (int a = 0; a < D / 64; ++a)
               store_tmem_pair_rope<D>(t_row + C::colDK, a, p.scale, k_pos, p.theta, dst, valid);
@@ -814,24 +775,24 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
   }
 }
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool EPI = false>
 cpattn_status launch_dkdv2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                              const CUtensorMap &mdo, const Bwd2Params &bp, unsigned grid, cudaStream_t s) {
   constexpr int threads = ROPE ? 384 : 320;
   constexpr int smem = Dkdv3Cfg<D>::SMEM;
-  auto kern = dkdv2_tc_kernel<D, ROPE>;
+  auto kern = dkdv2_tc_kernel<D, ROPE, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
   kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
   return check_launch("tensor-core dK/dV kernel (pipelined)");
 }
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool EPI = false>
 cpattn_status launch_dq2_t(const CUtensorMap &mk, const CUtensorMap &mv, const Bwd2Params &bp, unsigned grid,
                            cudaStream_t s) {
   constexpr int threads = ROPE ? 384 : 320;
   constexpr int smem = Dq3Cfg<D>::SMEM;
-  auto kern = dq2_tc_kernel<D, ROPE>;
+  auto kern = dq2_tc_kernel<D, ROPE, EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dQ kernel", smem);
   kern<<<grid, threads, smem, s>>>(mk, mv, bp);
@@ -878,17 +839,20 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   cpattn_status st;
   if (g.d == 128)
     st = g.rope ? launch_dkdv2_t<128, true>(mq, mk, mv, mdo, bp, gr, s)
-                : launch_dkdv2_t<128, false>(mq, mk, mv, mdo, bp, gr, s);
+         : g.rope_epi ? launch_dkdv2_t<128, false, true>(mq, mk, mv, mdo, bp, gr, s)
+                      : launch_dkdv2_t<128, false>(mq, mk, mv, mdo, bp, gr, s);
   else
     st = g.rope ? launch_dkdv2_t<64, true>(mq, mk, mv, mdo, bp, gr, s)
-                : launch_dkdv2_t<64, false>(mq, mk, mv, mdo, bp, gr, s);
+         : g.rope_epi ? launch_dkdv2_t<64, false, true>(mq, mk, mv, mdo, bp, gr, s)
+                      : launch_dkdv2_t<64, false>(mq, mk, mv, mdo, bp, gr, s);
   if (st != CPATTN_OK) return st;
   trace_record(2, s);
-  // dQ: CTA pairs with two-SM MMAs at d = 128 (inputs already rotated); the
-  // one-CTA pipelined kernel otherwise.
+  // dQ: CTA pairs with two-SM MMAs at d = 128 when q, k arrive rotated (or
+  // without RoPE); the one-CTA pipelined kernel otherwise.
   if (g.d == 128 && !g.rope) return launch_dq_pair_bf16(q, k, v, lse, dO, dq, D, g, s);
   if (g.d == 128) return launch_dq2_t<128, true>(mk, mv, bp, gr, s);
-  return g.rope ? launch_dq2_t<64, true>(mk, mv, bp, gr, s) : launch_dq2_t<64, false>(mk, mv, bp, gr, s);
+  if (g.rope) return launch_dq2_t<64, true>(mk, mv, bp, gr, s);
+  return g.rope_epi ? launch_dq2_t<64, false, true>(mk, mv, bp, gr, s) : launch_dq2_t<64, false>(mk, mv, bp, gr, s);
 }
 
 }  // namespace cpattn

@@ -141,7 +141,7 @@ struct GroupQSchedule {
 // A kernel that uses a table runs only when 2*cp*tiles_per_chunk <= kMaxTiles,
 // so the tile index in its chunk fits in 10 bits (tiles_per_chunk <= 1024)
 // and the slot 2r + half in 11 bits (2*cp <= 2048).
-constexpr int kMaxTiles = 2048;   // entries per CTA (16 KiB of shared memory)
+constexpr int kMaxTiles = kTableTiles;   // entries per CTA (16 KiB of shared memory)
 
 struct TileEntry {
   int pos0;
@@ -305,6 +305,45 @@ __device__ __forceinline__ QBounds q_bounds(const int *doc_lo, const int *doc_hi
   qb.doc_lo_max = lo_max;
   qb.doc_hi_min = hi_min;
   return qb;
+}
+
+// Stores scale * m R^T of one pair of 32-column chunks of a TMEM row (m the
+// attention temperature of the RoPE configuration, 1 for the standard one): columns
+// 32a..32a+31 and their rotation partners D/2 further on (frequencies
+// 32a..32a+31), for the key or query at natural position pos, as bf16 at
+// dst + the same columns (every lane of the warp must call this).
+template <int D>
+__device__ __forceinline__ void store_tmem_pair_rope(uint32_t t_col0, int a, float scale, int pos,
+                                                     const RopeTheta &th, __nv_bfloat16 *dst, bool valid) {
+  uint32_t ra[32], rb[32];
+  tc::tmem_ld32(t_col0 + 32 * a, ra);
+  tc::tmem_ld32(t_col0 + 32 * a + D / 2, rb);
+  tc::tmem_ld_wait();
+  uint32_t pa[16], pb[16];
+#pragma unroll
+  for (int e = 0; e < 32; e += 2) {
+    float o[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float sn, cs;
+      rope_sincos(pos, th.hi[32 * a + e + u], th.lo[32 * a + e + u], sn, cs);
+      sn *= th.mscale;
+      cs *= th.mscale;
+      const float x = __uint_as_float(ra[e + u]) * scale, y = __uint_as_float(rb[e + u]) * scale;
+      o[0][u] = fmaf(x, cs, y * sn);    // R^T: x cos + y sin
+      o[1][u] = fmaf(y, cs, -x * sn);   //      y cos - x sin
+    }
+    pa[e / 2] = pack_bf16x2(o[0][0], o[0][1]);
+    pb[e / 2] = pack_bf16x2(o[1][0], o[1][1]);
+  }
+  if (valid) {
+    uint4 *da = reinterpret_cast<uint4 *>(dst + 32 * a), *db = reinterpret_cast<uint4 *>(dst + 32 * a + D / 2);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      da[v] = make_uint4(pa[4 * v], pa[4 * v + 1], pa[4 * v + 2], pa[4 * v + 3]);
+      db[v] = make_uint4(pb[4 * v], pb[4 * v + 1], pb[4 * v + 2], pb[4 * v + 3]);
+    }
+  }
 }
 
 }  // namespace cpattn

@@ -44,6 +44,7 @@ struct DqPairParams {
   int group;                 // query heads per K/V head
   const int *doc_lo, *doc_hi;
   float scale, scale_log2;
+  RopeTheta theta;           // R^T of the epilogue (EPI)
 };
 
 struct DqPairCfg {
@@ -73,6 +74,9 @@ __device__ __forceinline__ uint32_t cluster_id_x() {
   return r;
 }
 
+// EPI: q and k arrive rotated (in-kernel RoPE done by the forward); dQ leaves
+// through R^T at the query's position.
+template <bool EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     dq_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
                    const __grid_constant__ CUtensorMap tm_kr, const __grid_constant__ CUtensorMap tm_vr,
@@ -355,7 +359,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     }
     if (ok && n > 0) {
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dq_done, (n - 1) & 1, wc));
-      if (ok) {
+      if (ok && EPI) {   // frequencies 32h..32h+31 of dQ and their partners 64 columns on: R^T
+        tc::tc_fence_after();
+        store_tmem_pair_rope<D>(t_row + C::colDQ, h, p.scale, q_pos, p.theta, p.dq + grow * D, valid);
+      } else if (ok) {
         tc::tc_fence_after();
 #pragma unroll 1
         for (int cb = 0; cb < 2; ++cb) {   // this warpgroup's 64 columns of dQ, scaled, as bf16
@@ -396,7 +403,7 @@ cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, c
                                   const void *dO, void *dq, const float *D, const Geometry &g,
                                   cudaStream_t s) {
   using C = DqPairCfg;
-  if (g.d != C::D || g.rope) return fail(CPATTN_ERR_UNSUPPORTED, "paired dQ kernel: d = 128 without in-kernel RoPE");
+  if (g.d != C::D || g.rope) return fail(CPATTN_ERR_UNSUPPORTED, "paired dQ kernel: d = 128, q and k not rotated in-kernel");
   const long long BH = (long long)g.B * g.H;
   const long long n_slots = BH * 2 * g.cp;
   const long long n_kv_slots = (long long)g.B * g.Hkv * 2 * g.cp;
@@ -424,9 +431,11 @@ cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, c
   dp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)g.d));
   const long long pairs = BH * 2 * g.cp * ((dp.tpc + 1) / 2);
   if (2 * pairs > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
-  if (cudaFuncSetAttribute(dq_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  make_rope_theta(g.d, &dp.theta, g.rope_cfg);
+  auto kern = g.rope_epi ? dq_pair_kernel<true> : dq_pair_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the paired dQ kernel", C::SMEM);
-  dq_pair_kernel<<<(unsigned)(2 * pairs), 320, C::SMEM, s>>>(mq, mkc, mkr, mvr, dp);
+  kern<<<(unsigned)(2 * pairs), 320, C::SMEM, s>>>(mq, mkc, mkr, mvr, dp);
   return check_launch("tensor-core dQ kernel (CTA pairs)");
 }
 

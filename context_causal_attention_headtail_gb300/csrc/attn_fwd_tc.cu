@@ -348,6 +348,12 @@ __global__ void __launch_bounds__(ROPE ? 320 : 192, 1)
 // With in-kernel RoPE (ROPE), warps 10-11 rotate Q0, Q1 once and every K
 // tile in shared memory between its TMA landing and its first MMA (q_ready,
 // k_ready); the issuer waits for those instead of the TMA barriers.
+// SAVE (with ROPE) also stores the rotated tiles for the backward: Q0, Q1 to
+// q_rot, and the CTA's two diagonal K tiles (the key rows at the positions of
+// its own query rows, which every query tile reads) to k_rot -- by the first
+// query head of each K/V-head group only -- so that every rotated row is
+// written once. A K stage with a store in flight is released by the rotation
+// warp once the store has read it (k_empty then counts two arrivals).
 template <int D>
 struct Fwd2Cfg {
   static constexpr int NS = (D == 128) ? 2 : 4;   // stages of the K ring and of the V ring
@@ -364,10 +370,12 @@ struct Fwd2Cfg {
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
 };
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool SAVE = false>
 __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     fwd2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p) {
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdParams p,
+                   const __grid_constant__ CUtensorMap tm_qrot, const __grid_constant__ CUtensorMap tm_krot) {
+  static_assert(!SAVE || ROPE, "saving rotated tiles needs the in-kernel rotation");
   using C = Fwd2Cfg<D>;
   constexpr int NS = C::NS;
   extern __shared__ uint8_t smem_raw[];
@@ -416,6 +424,9 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       const uint32_t b = bar0 + 8 * i;
       uint32_t cnt = (b == bar_p_full(0) || b == bar_p_full(1)) ? 128 : 1;
       if (b >= bar_q_ready) cnt = 64;   // q_ready, k_ready[]: the two rotation warps
+      if (SAVE)
+        for (int st = 0; st < NS; ++st)
+          if (b == bar_k_empty(st)) cnt = 2;   // the issuer's commit and the rotation warp's release
       tc::mbar_init(b, cnt);
     }
     abort_flag[0] = 0;
@@ -538,11 +549,20 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     // ------------------------------------------------ RoPE rotation warps
     tc::RopeRows<D, 64> rr;   // warps 10-11
     rr.init((warp - 10) * 32 + lane, p.theta);
+    const bool storer = SAVE && warp == 10 && lane == 0;
+    const int own_slot = 2 * rq + hq;
+    const bool kv_writer = (bh % p.group) == 0;     // first query head of its K/V group
     if (__all_sync(0xffffffffu, tc::mbar_wait(bar_q_full, 0, wc))) {
       rr.rotate(smem + C::OFF_Q, q_pos0);
       rr.rotate(smem + C::OFF_Q + C::TILE, q_pos0 + kTile);
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(bar_q_ready);
+      if (storer && tc::mbar_wait(bar_q_ready, 0, wc)) {   // both rotation warps are done with Q
+        for (int i = 0; i < 2 && y0 + i * kTile < c; ++i)
+          for (int blk = 0; blk < D / 64; ++blk)
+            tc::tma_store_3d(&tm_qrot, sQ(i) + blk * kTile * 128, blk * 64, y0 + i * kTile, q_z);
+        tc::tma_store_commit();
+      }
       for (int n = 0; n < ntiles; ++n) {
         decode_tile(tab[n], t);
         const int st = n % NS;
@@ -550,8 +570,19 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         rr.rotate(smem + C::OFF_K + st * C::TILE, t.pos0);
         tc::fence_proxy_async_smem();
         tc::mbar_arrive(bar_k_ready(st));
+        if (storer) {
+          const bool diag = kv_writer && t.slot == own_slot && (t.y0 == y0 || t.y0 == y0 + kTile);
+          if (diag && tc::mbar_wait(bar_k_ready(st), (n / NS) & 1, wc)) {
+            for (int blk = 0; blk < D / 64; ++blk)
+              tc::tma_store_3d(&tm_krot, sK(st) + blk * kTile * 128, blk * 64, t.y0, bkv * 2 * cp + t.slot);
+            tc::tma_store_commit();
+            tc::tma_store_wait_read();                      // the stage may be refilled after this
+          }
+          tc::mbar_arrive(bar_k_empty(st));
+        }
       }
     }
+    if (storer) tc::tma_store_wait_all();
   } else {
     // ----------------------------------------------- softmax warpgroups 0, 1
     const int wg = warp >> 2;
@@ -725,14 +756,15 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 
 namespace {
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool SAVE = false>
 cpattn_status launch_fwd2_t(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                            const FwdParams &fp, unsigned grid, cudaStream_t s) {
+                            const FwdParams &fp, unsigned grid, cudaStream_t s,
+                            const CUtensorMap *mqr = nullptr, const CUtensorMap *mkr = nullptr) {
   constexpr int smem = Fwd2Cfg<D>::SMEM;
-  auto kern = fwd2_tc_kernel<D, ROPE>;
+  auto kern = fwd2_tc_kernel<D, ROPE, SAVE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the forward kernel", smem);
-  kern<<<grid, ROPE ? 384 : 320, smem, s>>>(mq, mk, mv, fp);
+  kern<<<grid, ROPE ? 384 : 320, smem, s>>>(mq, mk, mv, fp, SAVE ? *mqr : mq, SAVE ? *mkr : mk);
   return check_launch("tensor-core forward kernel (paired tiles)");
 }
 
@@ -780,6 +812,14 @@ cpattn_status launch_fwd_bf16(const void *q, const void *k, const void *v, void 
   if (2LL * g.cp * fp.tpc <= kMaxTiles) {
     const long long grid2 = BH * 2 * g.cp * ((fp.tpc + 1) / 2);
     if (grid2 > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many query tiles");
+    if (g.q_rot) {   // in-kernel RoPE that also stores the rotated q, k
+      CUtensorMap mqr, mkr;
+      if (!g.rope || !make_tile_map(&mqr, g.q_rot, g.d, g.c, n_slots) ||
+          !make_tile_map(&mkr, g.k_rot, g.d, g.c, n_kv_slots))
+        return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the rotated copies");
+      return g.d == 128 ? launch_fwd2_t<128, true, true>(mq, mk, mv, fp, (unsigned)grid2, s, &mqr, &mkr)
+                        : launch_fwd2_t<64, true, true>(mq, mk, mv, fp, (unsigned)grid2, s, &mqr, &mkr);
+    }
     if (g.d == 128)
       return g.rope ? launch_fwd2_t<128, true>(mq, mk, mv, fp, (unsigned)grid2, s)
                     : launch_fwd2_t<128, false>(mq, mk, mv, fp, (unsigned)grid2, s);

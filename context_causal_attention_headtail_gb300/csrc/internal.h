@@ -39,6 +39,11 @@ void make_rope_theta(int d, RopeTheta *t, const cpattn_rope_cfg *cfg = nullptr);
 // Host validation of a RoPE configuration.
 cpattn_status check_rope_cfg(const cpattn_rope_cfg *cfg);
 
+// The pipelined attention kernels keep each CTA's tile schedule in a table of
+// this many entries; longer schedules (2*cp*ceil(c/128) above it) take the
+// one-tile kernels.
+constexpr int kTableTiles = 2048;
+
 // HeadTail geometry of one [B,H,T,d] problem.
 struct Geometry {
   int B, H, T, T_valid, d, cp, c;  // c = T / (2 cp)
@@ -50,6 +55,12 @@ struct Geometry {
   // In-kernel RoPE frequencies and temperature (host pointer read by the
   // launchers; nullptr: the standard rotation, base 10000).
   const cpattn_rope_cfg *rope_cfg = nullptr;
+  // Forward with in-kernel RoPE: also store the rotated q and k here (sharded
+  // layout, like q and k); nullptr: do not.
+  void *q_rot = nullptr, *k_rot = nullptr;
+  // Backward on q, k that are already rotated: the kernels rotate nothing and
+  // return dq, dk through R^T (rope must be 0 then).
+  bool rope_epi = false;
 };
 
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------
@@ -117,5 +128,11 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, const float *lse,
                                   const void *dO, void *dq, const float *D, const Geometry &g,
                                   cudaStream_t s);
+// dst = m R(p) src (inverse: m R(p)^T src) for every row of a HeadTail-sharded
+// [B*H, T, d] tensor, p the row's natural position (RoPE configuration cfg,
+// nullptr: standard); dst may equal src (each element is read, then written,
+// by the same thread).
+cpattn_status launch_rope_sharded(const void *src, void *dst, const Geometry &g, int heads, cpattn_dtype dt,
+                                  bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s);
 
 }  // namespace cpattn

@@ -273,6 +273,99 @@ static cpattn_status launch_rope_map(const void *src, void *dst, const Map &map,
   return check_launch(inverse ? "inverse permutation + RoPE kernel" : "permutation + RoPE kernel");
 }
 
+// RoPE of a tensor that is already HeadTail-sharded: chunk ch = (head, slot)
+// keeps its rows (nat = perm), its first row sits at natural position
+// chunk_of(slot / 2, slot % 2) * c.
+struct SlotMap {
+  int cp, c;
+  __device__ __forceinline__ int rows() const { return c; }
+  __device__ __forceinline__ void at(long long ch, long long &nat, long long &perm, int &pos0) const {
+    const int slot = (int)(ch % (2 * cp));
+    nat = perm = ch * (long long)c;
+    pos0 = chunk_of(slot >> 1, slot & 1, cp) * c;
+  }
+};
+
+// The rotation of shard_rope_kernel on a sharded tensor, without __restrict__:
+// dst may equal src (every element is read and then written by one thread).
+template <typename T, int D, bool INVERSE>
+__global__ void __launch_bounds__(256) rope_sharded_kernel(const T *src, T *dst, SlotMap map, long long n_chunks,
+                                                           RopeTheta th) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int GROUPS = (D / 2) / VEC;
+  constexpr int RS = 256 / GROUPS;
+  const int grp = threadIdx.x % GROUPS, lrow = threadIdx.x / GROUPS;
+  const int f0 = grp * VEC;
+  const int c = map.rows();
+  for (long long ch = blockIdx.y; ch < n_chunks; ch += gridDim.y) {
+    long long row0, unused;
+    int pos0;
+    map.at(ch, row0, unused, pos0);
+    const int row_begin = blockIdx.x * kRopeRowsPerBlock + lrow;
+    const int row_end = min(c, (int)(blockIdx.x + 1) * kRopeRowsPerBlock);
+    if (row_begin >= row_end) continue;
+    float cs[VEC], sn[VEC], cd[VEC], sd[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      rope_sincos(pos0 + row_begin, th.hi[f0 + v], th.lo[f0 + v], sn[v], cs[v]);
+      rope_sincos(RS, th.hi[f0 + v], th.lo[f0 + v], sd[v], cd[v]);
+    }
+    for (int o = row_begin; o < row_end; o += RS) {
+      const T *in = src + (row0 + o) * D;
+      T *out = dst + (row0 + o) * D;
+      const uint4 ua = *reinterpret_cast<const uint4 *>(in + f0);
+      const uint4 ub = *reinterpret_cast<const uint4 *>(in + f0 + D / 2);
+      float x[VEC], y[VEC];
+      unpack16<T>(ua, x);
+      unpack16<T>(ub, y);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        const float s_ = INVERSE ? -sn[v] : sn[v];
+        const float xr = fmaf(x[v], cs[v], -y[v] * s_);
+        const float yr = fmaf(y[v], cs[v], x[v] * s_);
+        x[v] = xr * th.mscale;
+        y[v] = yr * th.mscale;
+        const float nc = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
+        const float ns = fmaf(sn[v], cd[v], cs[v] * sd[v]);
+        cs[v] = nc;
+        sn[v] = ns;
+      }
+      *reinterpret_cast<uint4 *>(out + f0) = pack16<T>(x);
+      *reinterpret_cast<uint4 *>(out + f0 + D / 2) = pack16<T>(y);
+    }
+  }
+}
+
+template <typename T, int D>
+static void launch_rope_sharded_t(const void *src, void *dst, const SlotMap &map, long long n_chunks, bool inverse,
+                                  const RopeTheta &th, cudaStream_t s) {
+  const unsigned gx = (unsigned)((map.c + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock);
+  const unsigned gy = (unsigned)(n_chunks < 65535 ? n_chunks : 65535);
+  dim3 grid(gx, gy);
+  if (inverse)
+    rope_sharded_kernel<T, D, true><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst), map,
+                                                         n_chunks, th);
+  else
+    rope_sharded_kernel<T, D, false><<<grid, 256, 0, s>>>(static_cast<const T *>(src), static_cast<T *>(dst), map,
+                                                          n_chunks, th);
+}
+
+cpattn_status launch_rope_sharded(const void *src, void *dst, const Geometry &g, int heads, cpattn_dtype dt,
+                                  bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  RopeTheta th;
+  make_rope_theta(g.d, &th, cfg);
+  const SlotMap map{g.cp, g.c};
+  const long long n_chunks = (long long)g.B * heads * 2 * g.cp;
+  if (dt == CPATTN_BF16) {
+    if (g.d == 128) launch_rope_sharded_t<__nv_bfloat16, 128>(src, dst, map, n_chunks, inverse, th, s);
+    else launch_rope_sharded_t<__nv_bfloat16, 64>(src, dst, map, n_chunks, inverse, th, s);
+  } else {
+    if (g.d == 128) launch_rope_sharded_t<float, 128>(src, dst, map, n_chunks, inverse, th, s);
+    else launch_rope_sharded_t<float, 64>(src, dst, map, n_chunks, inverse, th, s);
+  }
+  return check_launch(inverse ? "RoPE^T kernel (sharded rows)" : "RoPE kernel (sharded rows)");
+}
+
 cpattn_status launch_shard_rope(const void *src, void *dst, const Geometry &g, cpattn_dtype dt,
                                 bool inverse, const cpattn_rope_cfg *cfg, cudaStream_t s) {
   const HeadTailMap map{g.cp, g.c};

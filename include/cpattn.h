@@ -240,6 +240,39 @@ cpattn_status cpattn_bwd_varlen(const void *q, const void *k, const void *v, con
                                 int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
                                 cpattn_dtype dt, cpattn_stream_t stream);
 
+/* ------------------------------- in-kernel RoPE, rotated once per call ---
+ * RoPE at global positions applied by the attention calls themselves (Claude
+ * Logs, 2026-05-07, 2026-06-05, 2026-06-29: each token's global position), for
+ * one document or packed documents, with the rotation done once: the forward
+ * rotates q and k as it streams them and also stores the rotated copies,
+ *   q_rot = m R(p) q,  k_rot = m R(p) k   (sharded layout, caller-owned,
+ *   16-byte aligned, the sizes of q and k; m = 1 and base 10000 when cfg is
+ *   NULL, else the YaRN configuration of cpattn_rope_cfg),
+ * and the backward takes those copies in place of q and k, runs the kernels
+ * that rotate nothing, and returns the gradients with respect to the
+ * UNROTATED q and k (dq = m R(p)^T dQ', dk = m R(p)^T dK' in the kernels'
+ * epilogues). The results equal cpattn_fwd_rope_cfg / cpattn_bwd_rope_cfg on
+ * the same q, k; the backward does not rotate every streamed tile again.
+ *   doc_lo, doc_hi : NULL (one sequence) or the per-position document bounds
+ *                    of cpattn_doc_bounds (packed documents; RoPE keeps the
+ *                    global positions).
+ * Other arguments, layouts and errors as cpattn_fwd_gqa / cpattn_bwd_gqa with
+ * rope = 1; q_rot and k_rot must not overlap any other buffer. The backward's
+ * workspace is cpattn_bwd_workspace_bytes(B, T, H, d). For bf16 inputs whose
+ * tile schedule fits the kernels' tables (2*cp*ceil(T/(2cp)/128) <= 2048) the
+ * rotation is fused as described; otherwise (fp32, or longer schedules) the
+ * forward rotates q and k in one pass before attending and the backward
+ * applies R^T in one pass after it, with the same results. */
+cpattn_status cpattn_fwd_rope_save(const void *q, const void *k, const void *v, void *o, float *lse,
+                                   void *q_rot, void *k_rot, int B, int T, int T_valid, int H, int H_kv,
+                                   int d, int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
+                                   const cpattn_rope_cfg *cfg, cpattn_dtype dt, cpattn_stream_t stream);
+cpattn_status cpattn_bwd_rotated(const void *q_rot, const void *k_rot, const void *v, const void *o,
+                                 const float *lse, const void *dO, void *dq, void *dk, void *dv,
+                                 void *workspace, int B, int T, int T_valid, int H, int H_kv, int d,
+                                 int cp, int causal, const int32_t *doc_lo, const int32_t *doc_hi,
+                                 const cpattn_rope_cfg *cfg, cpattn_dtype dt, cpattn_stream_t stream);
+
 /* ----------------------------------------------- Ulysses all-to-all ---
  * The Ulysses (DeepSpeed) variant of sequence parallelism on P virtual
  * ranks (Claude Logs, 2026-06-30: all-to-all layout swaps [B,H,Tl,D] <->

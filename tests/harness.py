@@ -98,14 +98,17 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     """rope_mode (when w.rope): "kernel" passes rope=1 to cpattn_fwd / cpattn_bwd
     (cpattn_fwd_rope_cfg / cpattn_bwd_rope_cfg for YaRN); "shard" rotates q, k in
     cpattn_shard_rope (cpattn_shard_rope_cfg for YaRN), runs the attention with
-    rope=0 and takes dq, dk back through cpattn_unshard_rope. Packed documents
-    take RoPE from the "shard" path only."""
+    rope=0 and takes dq, dk back through cpattn_unshard_rope; "save" runs
+    cpattn_fwd_rope_save (the forward rotates in-kernel and stores q_rot, k_rot)
+    and cpattn_bwd_rotated on those copies. Packed documents take RoPE from the
+    "shard" and "save" paths."""
     dev = torch.device(device)
     stream = torch.cuda.current_stream(dev)
     fused = w.rope and rope_mode == "shard"
-    rope_flag = w.rope and not fused
-    if w.packed and w.rope and not fused:
-        raise ValueError("packed documents take RoPE from the shard / unshard passes")
+    saved = w.rope and rope_mode == "save"
+    rope_flag = w.rope and rope_mode == "kernel"
+    if w.packed and rope_flag:
+        raise ValueError("packed documents take RoPE from the shard / unshard passes or the save path")
     cfg = gpu_rope_cfg(w)
     docs = None
     if w.packed:
@@ -122,16 +125,26 @@ def run_gpu(w: Workload, inp: dict, device="cuda:0", with_bwd=True, repeat=1,
     o = torch.empty_like(sh["q"])
     lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
     out = {}
+    if saved:
+        q_rot, k_rot = torch.empty_like(sh["q"]), torch.empty_like(sh["k"])
     for _ in range(repeat):
-        cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
-                   docs=docs, rope_cfg=cfg if rope_flag else None)
+        if saved:
+            cpattn.fwd_rope_save(sh["q"], sh["k"], sh["v"], o, lse, q_rot, k_rot, w.cp, w.T_valid, w.causal,
+                                 stream, docs=docs, rope_cfg=cfg)
+        else:
+            cpattn.fwd(sh["q"], sh["k"], sh["v"], o, lse, w.cp, w.T_valid, w.causal, rope_flag, stream,
+                       docs=docs, rope_cfg=cfg if rope_flag else None)
     if with_bwd:
         dq, dk, dv = torch.empty_like(sh["q"]), torch.empty_like(sh["k"]), torch.empty_like(sh["v"])
         ws = torch.empty(cpattn.cpattn_bwd_workspace_bytes(w.B, w.T, w.H, w.d), dtype=torch.uint8,
                          device=dev)
         for _ in range(repeat):
-            cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
-                       w.causal, rope_flag, stream, docs=docs, rope_cfg=cfg if rope_flag else None)
+            if saved:
+                cpattn.bwd_rotated(q_rot, k_rot, sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
+                                   w.causal, stream, docs=docs, rope_cfg=cfg)
+            else:
+                cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, w.cp, w.T_valid,
+                           w.causal, rope_flag, stream, docs=docs, rope_cfg=cfg if rope_flag else None)
         for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
             nt = torch.empty_like(t)
             if fused and name in ("dq", "dk"):

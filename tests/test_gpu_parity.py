@@ -315,7 +315,7 @@ def test_shard_index_matches_oracle():
 
 # -------------------------------------------------- small, full compare ----
 
-ROPE_MODES = ["kernel", "shard"]
+ROPE_MODES = ["kernel", "shard", "save"]
 
 SMALL_F32 = [
     WORKLOADS["tiny_fp32"],
@@ -369,10 +369,10 @@ SMALL_BF16 = [
 @pytest.mark.parametrize("mode", ROPE_MODES)
 @pytest.mark.parametrize("w", SMALL_F32 + SMALL_GQA_F32, ids=lambda w: w.name)
 def test_fp32_path_full(w, mode):
-    if mode == "shard" and not w.rope:
+    if mode != "kernel" and not w.rope:
         pytest.skip("no RoPE: one path")
     if mode == "kernel" and w.packed and w.rope:
-        pytest.skip("packed documents take RoPE from the shard / unshard passes")
+        pytest.skip("packed documents take RoPE from the shard passes or the save path")
     inp = make_inputs(w, seed=SEEDS.get(w.name, 99))
     _check_full(w, run_gpu(w, inp, rope_mode=mode), _oracle_full(w, inp))
 
@@ -380,10 +380,10 @@ def test_fp32_path_full(w, mode):
 @pytest.mark.parametrize("mode", ROPE_MODES)
 @pytest.mark.parametrize("w", SMALL_BF16, ids=lambda w: w.name)
 def test_bf16_path_full(w, mode):
-    if mode == "shard" and not w.rope:
+    if mode != "kernel" and not w.rope:
         pytest.skip("no RoPE: one path")
     if mode == "kernel" and w.packed and w.rope:
-        pytest.skip("packed documents take RoPE from the shard / unshard passes")
+        pytest.skip("packed documents take RoPE from the shard passes or the save path")
     inp = make_inputs(w, seed=7 + w.T + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     want = _oracle_full(w, inp)
@@ -400,6 +400,43 @@ def test_bf16_deterministic(mode):
     a, b = run_gpu(w, inp, rope_mode=mode), run_gpu(w, inp, rope_mode=mode)
     for k in a:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("w", [make_workload("save_gqa_yarn", B=1, T=1536, H=4, H_kv=2, d=128, cp=3, rope=True,
+                                             yarn_factor=2.0, yarn_original=512),
+                               make_workload("save_d64", B=2, T=1024, H=2, d=64, cp=2, rope=True)],
+                         ids=lambda w: w.name)
+def test_fwd_rope_save_stores_the_rotated_inputs(w):
+    """cpattn_fwd_rope_save writes q_rot = m R q and k_rot = m R k at every
+    sharded row (no padding here, so every key tile is read by the query tile
+    at its own positions): bounded against the oracle's rotation."""
+    from harness import gpu_rope_cfg
+    inp = make_inputs(w, seed=21 + w.T)
+    dev = torch.device("cuda:0")
+    sh = {}
+    for n_ in ("q", "k", "v"):
+        x = inp[n_].to(dev)
+        sh[n_] = torch.empty_like(x)
+        cpattn.shard(x, sh[n_], w.cp)
+    o = torch.empty_like(sh["q"])
+    lse = torch.empty((w.B, w.H, w.T), dtype=torch.float32, device=dev)
+    q_rot, k_rot = torch.full_like(sh["q"], float("nan")), torch.full_like(sh["k"], float("nan"))
+    cpattn.fwd_rope_save(sh["q"], sh["k"], sh["v"], o, lse, q_rot, k_rot, w.cp, w.T_valid, w.causal,
+                         docs=None, rope_cfg=gpu_rope_cfg(w))
+    cpattn.cpattn_sync_status(None)
+    spec = oracle_rope(w)
+    spec = A.STANDARD_ROPE if spec is True else spec
+    m = spec.mscale()
+    for name, got in (("q", q_rot), ("k", k_rot)):
+        xd = inp[name].double().numpy()
+        want = HT.shard(A.rope(xd, np.arange(w.T), spec), w.cp)
+        g = got.double().cpu().numpy()
+        assert np.isfinite(g).all(), f"{name}_rot has rows that were not written"
+        pair = np.sqrt(xd[..., : w.d // 2] ** 2 + xd[..., w.d // 2:] ** 2)
+        pair = HT.shard(np.concatenate([pair, pair], axis=-1), w.cp)
+        bound = 2.0 ** -8 * np.abs(want) + 1e-5 * m * pair + 1e-7
+        worst = float((np.abs(g - want) / bound).max())
+        assert worst <= 1.0, f"{name}_rot: worst error/bound {worst:.3f}"
 
 
 # ------------------------------------------------------------- merge ----
@@ -456,7 +493,9 @@ def _sampled_check(w, inp, got, heads, kv_heads, n_random=24):
                                        ("padded_12289", "shard"), ("padded_12289", "kernel"),
                                        ("gqa_32k", "shard"), ("gqa_32k", "kernel"),
                                        ("yarn_32k", "shard"), ("yarn_32k", "kernel"),
-                                       ("varlen_32k", "shard")])
+                                       ("varlen_32k", "shard"), ("window_32k", "save"),
+                                       ("gqa_32k", "save"), ("padded_12289", "save"),
+                                       ("varlen_32k", "save"), ("gpt2_small", "save")])
 def test_workload_full_size_sampled(name, mode):
     w = WORKLOADS[name]
     inp = make_inputs(w, SEEDS[name])
@@ -592,7 +631,7 @@ WIDE_TABLE = [
 def test_wide_tile_tables_full(w, mode):
     assert 1024 < 2 * w.cp * -(-w.chunk // 128) <= 2048
     if mode == "kernel" and w.packed:
-        pytest.skip("packed documents take RoPE from the shard / unshard passes")
+        pytest.skip("packed documents take RoPE from the shard passes or the save path")
     inp = make_inputs(w, seed=13 + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     _check_full(w, got, _oracle_full(w, inp))
@@ -603,7 +642,7 @@ def test_wide_tile_tables_full(w, mode):
 def test_one_tile_kernels_full(w, mode):
     assert 2 * w.cp * -(-w.chunk // 128) > 2048
     if mode == "kernel" and w.packed:
-        pytest.skip("packed documents take RoPE from the shard / unshard passes")
+        pytest.skip("packed documents take RoPE from the shard passes or the save path")
     inp = make_inputs(w, seed=11 + w.cp)
     got = run_gpu(w, inp, rope_mode=mode)
     _check_full(w, got, _oracle_full(w, inp))

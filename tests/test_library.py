@@ -75,6 +75,21 @@ def test_fwd_validation(lib, args, status):
     assert cpattn.cpattn_last_error() != ""
 
 
+def test_rope_save_and_rotated_validation(lib):
+    st = lib.cpattn_fwd_rope_save(*P[:5], None, P[6], 1, 1024, 1024, 2, 2, 128, 2, 1, None, None, None,
+                                  cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG
+    st = lib.cpattn_fwd_rope_save(*P[:5], P[0], P[6], 1, 1024, 1024, 2, 2, 128, 2, 1, None, None, None,
+                                  cpattn.BF16, None)            # q_rot aliases q
+    assert st == cpattn.ERR_ARG and "overlap" in cpattn.cpattn_last_error()
+    st = lib.cpattn_fwd_rope_save(*P[:7], 1, 1024, 1024, 2, 2, 96, 2, 1, None, None, None, cpattn.BF16, None)
+    assert st == cpattn.ERR_SHAPE
+    st = lib.cpattn_bwd_rotated(*P, 1, 1024, 1024, 2, 2, 128, 2, 1, P[0], None, None, cpattn.BF16, None)
+    assert st == cpattn.ERR_ARG and "document" in cpattn.cpattn_last_error()
+    st = lib.cpattn_bwd_rotated(*P, 1, 1000, 1000, 2, 2, 128, 3, 1, None, None, None, cpattn.BF16, None)
+    assert st == cpattn.ERR_SHAPE
+
+
 def test_wait_probe_limit_is_validated(lib):
     for bad in (0, 999, 10 ** 9 + 1):
         assert lib.cpattn_check_wait_timeout(bad, None) == cpattn.ERR_ARG
