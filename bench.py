@@ -46,15 +46,15 @@ DEFAULT_WORKLOAD = "window_32k"
 # kernel_digest). A capture whose digest no longer matches the sources in the
 # tree describes an older kernel: the bench then reports the traffic as null.
 NCU_TRAFFIC = {
-    ("window_32k", "fwd"): (2.217879e9 + 0.120774e9, None),
-    ("window_32k", "bwd_dkdv"): (4.115046e9 + 0.239118e9, None),
-    ("window_32k", "bwd_dq"): (4.067247e9 + 0.120400e9, None),
+    ("window_32k", "fwd"): (0.403631e9 + 0.119130e9, "0366dbae1087"),
+    ("window_32k", "bwd_dkdv"): (0.541742e9 + 0.240560e9, "dde0d5c549b2"),
+    ("window_32k", "bwd_dq"): (0.541444e9 + 0.119546e9, "965dd1d41141"),
 }
 CSRC = os.path.join(ROOT, "context_causal_attention_headtail_gb300", "csrc")
 KERNEL_SOURCES = {
     "fwd": ("attn_fwd_tc.cu", "tc_common.cuh", "attn_common.cuh", "device_common.cuh"),
     "bwd_dkdv": ("attn_bwd2_tc.cu", "tc_common.cuh", "attn_common.cuh", "device_common.cuh"),
-    "bwd_dq": ("attn_bwd2_tc.cu", "tc_common.cuh", "attn_common.cuh", "device_common.cuh"),
+    "bwd_dq": ("attn_dq_pair.cu", "tc_common.cuh", "attn_common.cuh", "device_common.cuh"),
 }
 
 

@@ -407,9 +407,11 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int ppc = (tpc + 1) / 2;                  // tile pairs per chunk
-  const int bh = blockIdx.x % p.BH;
+  // Heads vary slowest: the CTAs in flight work on one head (or a few), so
+  // the K/V tiles they all stream stay in L2.
+  const int bh = blockIdx.x / (2 * cp * ppc);
   const int bkv = bh / p.group;                   // K/V head of this query head
-  const int g = blockIdx.x / p.BH;
+  const int g = blockIdx.x % (2 * cp * ppc);
   const int kq = 2 * cp - 1 - g / ppc;            // latest chunks first: they carry the most work
   const int pq = ppc - 1 - g % ppc;
   int rq, hq;
