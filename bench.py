@@ -420,11 +420,14 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     kernels = ["shard", "fwd", "bwd_D", "bwd_dkdv", "bwd_dq", "unshard"]
-    launches_per_step = 4 + 1 + 3 + 4 + (1 if w.packed else 0)
+    # the ring path shards q, k, v, dO in one launch and unshards o, dq, dk, dv in one;
+    # the Ulysses all-to-all runs per tensor
+    n_passes = 4 if P else 1
+    launches_per_step = 2 * n_passes + 1 + 3 + (1 if w.packed else 0)
 
     def new_events():
         evs = {"shard": [], "unshard": []}
-        for _ in range(4):
+        for _ in range(n_passes):
             evs["shard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
             evs["unshard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
         evs["fwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -451,17 +454,20 @@ def run_ours(args):
         cu_dev = cu_host.to(dev)
         docs = (torch.empty(w.T, dtype=torch.int32, device=dev), torch.empty(w.T, dtype=torch.int32, device=dev))
 
+    names_in, names_out = ("q", "k", "v", "do"), ("o", "dq", "dk", "dv")
+
     def step(evs=None, nat=nat, outs_nat=outs_nat, lse=lse):
-        for i, name in enumerate(("q", "k", "v", "do")):
-            if evs:
-                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
-            if P:
+        if P:
+            for i, name in enumerate(names_in):
+                if evs:
+                    cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][i]])
                 cpattn.ulysses_a2a(nat[name], sh[name], P, rope=fused and name in ("q", "k"), cfg=rope_cfg,
                                    stream=stream)
-            elif fused and name in ("q", "k"):
-                cpattn.shard_rope(nat[name], sh[name], w.cp, stream, cfg=rope_cfg)
-            else:
-                cpattn.shard(nat[name], sh[name], w.cp, stream)
+        else:   # one launch for the four tensors, q and k rotated when RoPE is fused into it
+            if evs:
+                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["shard"][0]])
+            cpattn.shard_batch([nat[n_] for n_ in names_in], [sh[n_] for n_ in names_in], w.cp,
+                               rope=[fused and n_ in ("q", "k") for n_ in names_in], stream=stream, cfg=rope_cfg)
         if docs is not None:
             cpattn.doc_bounds(cu_dev, w.T, docs[0], docs[1], stream)
         if evs:
@@ -479,16 +485,18 @@ def run_ours(args):
         else:
             cpattn.bwd(sh["q"], sh["k"], sh["v"], o, lse, sh["do"], dq, dk, dv, ws, cp_attn, w.T_valid,
                        w.causal, False, stream, docs=docs)
-        for i, name in enumerate(("o", "dq", "dk", "dv")):
-            if evs:
-                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
-            if P:
+        if P:
+            for i, name in enumerate(names_out):
+                if evs:
+                    cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][i]])
                 cpattn.ulysses_a2a(outs[name], outs_nat[name], P, inverse=True,
                                    rope=fused and name in ("dq", "dk"), cfg=rope_cfg, stream=stream)
-            elif fused and name in ("dq", "dk"):
-                cpattn.unshard_rope(outs[name], outs_nat[name], w.cp, stream, cfg=rope_cfg)
-            else:
-                cpattn.unshard(outs[name], outs_nat[name], w.cp, stream)
+        else:
+            if evs:
+                cpattn.cpattn_set_trace_events([e.cuda_event for e in evs["unshard"][0]])
+            cpattn.shard_batch([outs[n_] for n_ in names_out], [outs_nat[n_] for n_ in names_out], w.cp,
+                               rope=[fused and n_ in ("dq", "dk") for n_ in names_out], stream=stream,
+                               cfg=rope_cfg, inverse=True)
         if evs:
             cpattn.cpattn_set_trace_events([])
 

@@ -26,7 +26,8 @@ EXPORTS = ("cpattn_shard", "cpattn_unshard", "cpattn_shard_rope", "cpattn_unshar
            "cpattn_fwd_gqa", "cpattn_bwd_gqa", "cpattn_shard_rope_cfg", "cpattn_unshard_rope_cfg",
            "cpattn_doc_bounds", "cpattn_fwd_varlen", "cpattn_bwd_varlen", "cpattn_ulysses_a2a",
            "cpattn_ulysses_a2a_rope", "cpattn_fwd_rope_cfg", "cpattn_bwd_rope_cfg",
-           "cpattn_check_wait_timeout", "cpattn_fwd_rope_save", "cpattn_bwd_rotated")
+           "cpattn_check_wait_timeout", "cpattn_fwd_rope_save", "cpattn_bwd_rotated", "cpattn_shard_batch",
+           "cpattn_unshard_batch")
 
 
 class CpattnError(RuntimeError):
@@ -75,6 +76,10 @@ def _declare(lib):
         "cpattn_merge": [_c.POINTER(_vp), _c.POINTER(_vp), _i, _vp, _vp, _i, _i, _i, _i, _i, _vp],
         "cpattn_sync_status": [_vp],
         "cpattn_check_wait_timeout": [_c.c_ulonglong, _vp],
+        "cpattn_shard_batch": [_c.POINTER(_vp), _c.POINTER(_vp), _c.POINTER(_i), _c.POINTER(_i), _i, _i, _i, _i, _i,
+                               _c.POINTER(RopeCfg), _i, _vp],
+        "cpattn_unshard_batch": [_c.POINTER(_vp), _c.POINTER(_vp), _c.POINTER(_i), _c.POINTER(_i), _i, _i, _i, _i, _i,
+                                 _c.POINTER(RopeCfg), _i, _vp],
         "cpattn_fwd_rope_save": [_vp] * 7 + [_i] * 8 + [_vp, _vp, _c.POINTER(RopeCfg), _i, _vp],
         "cpattn_bwd_rotated": [_vp] * 10 + [_i] * 8 + [_vp, _vp, _c.POINTER(RopeCfg), _i, _vp],
         "cpattn_set_trace_events": [_c.POINTER(_vp), _i],
@@ -189,6 +194,23 @@ def cpattn_bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T,
     _check(lib().cpattn_bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, B, T, T_valid, H, H_kv, d,
                                     cp, causal, doc_lo, doc_hi, None if cfg is None else ctypes.byref(cfg), dt,
                                     stream))
+
+
+def _batch_args(src, dst, heads, rope):
+    n = len(src)
+    return ((_vp * n)(*src), (_vp * n)(*dst), (_i * n)(*heads), (_i * n)(*rope), n)
+
+
+def cpattn_shard_batch(src, dst, heads, rope, B, T, d, cp, cfg, dt, stream=None):
+    s_, d_, h_, r_, n = _batch_args(src, dst, heads, rope)
+    _check(lib().cpattn_shard_batch(s_, d_, h_, r_, n, B, T, d, cp, None if cfg is None else ctypes.byref(cfg),
+                                    dt, stream))
+
+
+def cpattn_unshard_batch(src, dst, heads, rope, B, T, d, cp, cfg, dt, stream=None):
+    s_, d_, h_, r_, n = _batch_args(src, dst, heads, rope)
+    _check(lib().cpattn_unshard_batch(s_, d_, h_, r_, n, B, T, d, cp, None if cfg is None else ctypes.byref(cfg),
+                                      dt, stream))
 
 
 def cpattn_doc_bounds(cu_seqlens, n_docs, T, doc_lo, doc_hi, stream=None):
@@ -418,6 +440,20 @@ def bwd_rotated(q_rot, k_rot, v, o, lse, dO, dq, dk, dv, workspace, cp, T_valid=
                        _ptr(dv), _ptr(workspace), B, T, T if T_valid is None else T_valid, H, H_kv, d, cp,
                        int(causal), None if docs is None else _ptr(docs[0]), None if docs is None else _ptr(docs[1]),
                        rope_cfg, _dtype_code(q_rot), _stream(stream))
+
+
+def shard_batch(srcs, dsts, cp, rope=None, stream=None, cfg: RopeCfg | None = None, inverse=False):
+    """HeadTail shard (inverse: unshard) of several [B, H_i, T, d] tensors in one launch;
+    rope[i] rotates tensor i (R in, R^T out)."""
+    B, _, T, d = srcs[0].shape
+    heads = [t.shape[1] for t in srcs]
+    for a, b_ in zip(srcs, dsts):
+        if tuple(a.shape) != tuple(b_.shape) or a.shape[0] != B or a.shape[2] != T or a.shape[3] != d:
+            raise CpattnError(ERR_SHAPE, "batched tensors must share B, T and d, and dst the shape of src")
+    rope = [0] * len(srcs) if rope is None else [int(bool(r)) for r in rope]
+    fn = cpattn_unshard_batch if inverse else cpattn_shard_batch
+    fn([_ptr(t) for t in srcs], [_ptr(t) for t in dsts], heads, rope, B, T, d, cp, cfg, _dtype_code(srcs[0]),
+       _stream(stream))
 
 
 def merge(o_parts, lse_parts, o, lse, stream=None):

@@ -323,6 +323,59 @@ cpattn_status cpattn_unshard_rope_cfg(const void *src, void *dst, int B, int H, 
   return shard_common(src, dst, B, H, T, d, cp, dt, stream, true, true, cfg);
 }
 
+static cpattn_status shard_batch_common(const void *const *src, void *const *dst, const int *heads, const int *rope,
+                                        int n, int B, int T, int d, int cp, const cpattn_rope_cfg *cfg,
+                                        cpattn_dtype dt, cpattn_stream_t stream, bool inverse) {
+  g_msg[0] = 0;
+  if (!src || !dst || !heads || !rope) return fail(CPATTN_ERR_ARG, "null pointer");
+  if (n < 1 || n > kBatchMax) return fail(CPATTN_ERR_ARG, "n=%d must be in [1, %d]", n, kBatchMax);
+  if (cfg && check_rope_cfg(cfg) != CPATTN_OK) return CPATTN_ERR_ARG;
+  if (dt != CPATTN_F32 && dt != CPATTN_BF16) return fail(CPATTN_ERR_DTYPE, "unknown dtype %d", (int)dt);
+  const int elt = dt == CPATTN_F32 ? 4 : 2;
+  if (d != 64 && d != 128) return fail(CPATTN_ERR_SHAPE, "d=%d: only 64 and 128 are supported", d);
+  if (T > (1 << 24)) return fail(CPATTN_ERR_SHAPE, "T=%d exceeds 2^24", T);
+  ShardBatch b;
+  b.n = n;
+  long long chunks = 0;
+  size_t bytes[kBatchMax];
+  for (int i = 0; i < n; ++i) {
+    cpattn_status st = check_common(B, heads[i], T, d, cp);
+    if (st != CPATTN_OK) return st;
+    if (!src[i] || !dst[i]) return fail(CPATTN_ERR_ARG, "null pointer for tensor %d", i);
+    if (!aligned16(src[i]) || !aligned16(dst[i])) return fail(CPATTN_ERR_ALIGN, "pointers must be 16-byte aligned");
+    if (rope[i] != 0 && rope[i] != 1) return fail(CPATTN_ERR_ARG, "rope[%d] must be 0 or 1", i);
+    bytes[i] = (size_t)B * heads[i] * T * d * elt;
+    b.src[i] = src[i];
+    b.dst[i] = dst[i];
+    b.rope[i] = rope[i];
+    b.first_chunk[i] = chunks;
+    chunks += (long long)B * heads[i] * 2 * cp;
+  }
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j)
+      if (overlaps(dst[i], bytes[i], src[j], bytes[j]) || (i != j && overlaps(dst[i], bytes[i], dst[j], bytes[j])))
+        return fail(CPATTN_ERR_ARG, "a destination overlaps another buffer of the batch");
+  b.n_chunks = chunks;
+  Geometry g = geometry(B, 1, T, T, d, cp, 1, 0);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  trace_record(0, s);
+  cpattn_status st = launch_shard_batch(b, g, dt, inverse, cfg, s);
+  trace_record(1, s);
+  return st;
+}
+
+cpattn_status cpattn_shard_batch(const void *const *src, void *const *dst, const int *heads, const int *rope, int n,
+                                 int B, int T, int d, int cp, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                 cpattn_stream_t stream) {
+  return shard_batch_common(src, dst, heads, rope, n, B, T, d, cp, cfg, dt, stream, false);
+}
+
+cpattn_status cpattn_unshard_batch(const void *const *src, void *const *dst, const int *heads, const int *rope, int n,
+                                   int B, int T, int d, int cp, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                   cpattn_stream_t stream) {
+  return shard_batch_common(src, dst, heads, rope, n, B, T, d, cp, cfg, dt, stream, true);
+}
+
 static cpattn_status ulysses_common(const void *src, void *dst, int B, int H, int T, int d, int P,
                                     int inverse, bool rope, const cpattn_rope_cfg *cfg,
                                     cpattn_dtype dt, cpattn_stream_t stream) {

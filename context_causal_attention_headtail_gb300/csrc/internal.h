@@ -128,6 +128,20 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, const float *lse,
                                   const void *dO, void *dq, const float *D, const Geometry &g,
                                   cudaStream_t s);
+// Up to kBatchMax tensors of one [B, H_i, T, d] layout (H_i per tensor)
+// through the HeadTail shard (or unshard) in one launch; tensor i with rope[i]
+// set is rotated (R in, R^T out) at natural positions.
+constexpr int kBatchMax = 8;
+struct ShardBatch {
+  const void *src[kBatchMax];
+  void *dst[kBatchMax];
+  int rope[kBatchMax];
+  long long first_chunk[kBatchMax];   // first chunk of tensor i in the launch's chunk order
+  int n;
+  long long n_chunks;
+};
+cpattn_status launch_shard_batch(const ShardBatch &b, const Geometry &g, cpattn_dtype dt, bool inverse,
+                                 const cpattn_rope_cfg *cfg, cudaStream_t s);
 // dst = m R(p) src (inverse: m R(p)^T src) for every row of a HeadTail-sharded
 // [B*H, T, d] tensor, p the row's natural position (RoPE configuration cfg,
 // nullptr: standard); dst may equal src (each element is read, then written,

@@ -273,6 +273,105 @@ static cpattn_status launch_rope_map(const void *src, void *dst, const Map &map,
   return check_launch(inverse ? "inverse permutation + RoPE kernel" : "permutation + RoPE kernel");
 }
 
+// ---------------------------------------------- several tensors, one launch ---
+// The HeadTail shard (or unshard) of up to kBatchMax tensors of one sequence
+// layout in one launch: blockIdx.y walks the chunks of every tensor in turn,
+// blockIdx.x the 256-row blocks of a chunk. A tensor with rope set goes
+// through the RoPE pass of shard_rope_kernel (R on the way in, R^T on the way
+// out), the others through a plain 16-byte copy; one launch instead of one per
+// tensor saves the ramp-up and drain of the separate launches.
+template <typename T, int D, bool INVERSE>
+__global__ void __launch_bounds__(256) shard_batch_kernel(ShardBatch b, HeadTailMap map, RopeTheta th) {
+  constexpr int VEC = VecOf<T>::N;
+  constexpr int GROUPS = (D / 2) / VEC;       // frequency groups per row
+  constexpr int RS = 256 / GROUPS;            // rows advanced per step
+  constexpr int ROW_U4 = D * (int)sizeof(T) / 16;
+  const int c = map.rows();
+  for (long long ch = blockIdx.y; ch < b.n_chunks; ch += gridDim.y) {
+    int i = 0;
+#pragma unroll 1
+    while (i + 1 < b.n && ch >= b.first_chunk[i + 1]) ++i;
+    long long nat0, shd0;
+    int pos0;
+    map.at(ch - b.first_chunk[i], nat0, shd0, pos0);
+    const int r_begin = blockIdx.x * kRopeRowsPerBlock;
+    const int r_end = min(c, r_begin + kRopeRowsPerBlock);
+    if (r_begin >= r_end) continue;
+    const T *src = static_cast<const T *>(b.src[i]);
+    T *dst = static_cast<T *>(b.dst[i]);
+    if (!b.rope[i]) {   // rows [r_begin, r_end) are contiguous on both sides
+      const uint4 *s4 = reinterpret_cast<const uint4 *>(src + ((INVERSE ? shd0 : nat0) + r_begin) * D);
+      uint4 *d4 = reinterpret_cast<uint4 *>(dst + ((INVERSE ? nat0 : shd0) + r_begin) * D);
+      const int n4 = (r_end - r_begin) * ROW_U4;
+      int j = threadIdx.x;
+      for (; j + 3 * 256 < n4; j += 4 * 256) {
+        const uint4 a = s4[j], bb = s4[j + 256], cc = s4[j + 512], e = s4[j + 768];
+        d4[j] = a; d4[j + 256] = bb; d4[j + 512] = cc; d4[j + 768] = e;
+      }
+      for (; j < n4; j += 256) d4[j] = s4[j];
+      continue;
+    }
+    const int grp = threadIdx.x % GROUPS, lrow = threadIdx.x / GROUPS;
+    const int f0 = grp * VEC;
+    const int row_begin = r_begin + lrow;
+    if (row_begin >= r_end) continue;
+    float cs[VEC], sn[VEC], cd[VEC], sd[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) {
+      rope_sincos(pos0 + row_begin, th.hi[f0 + v], th.lo[f0 + v], sn[v], cs[v]);
+      rope_sincos(RS, th.hi[f0 + v], th.lo[f0 + v], sd[v], cd[v]);
+    }
+    for (int o = row_begin; o < r_end; o += RS) {
+      const T *in = src + ((INVERSE ? shd0 : nat0) + o) * D;
+      T *out = dst + ((INVERSE ? nat0 : shd0) + o) * D;
+      const uint4 ua = *reinterpret_cast<const uint4 *>(in + f0);
+      const uint4 ub = *reinterpret_cast<const uint4 *>(in + f0 + D / 2);
+      float x[VEC], y[VEC];
+      unpack16<T>(ua, x);
+      unpack16<T>(ub, y);
+#pragma unroll
+      for (int v = 0; v < VEC; ++v) {
+        const float s_ = INVERSE ? -sn[v] : sn[v];
+        const float xr = fmaf(x[v], cs[v], -y[v] * s_);
+        const float yr = fmaf(y[v], cs[v], x[v] * s_);
+        x[v] = xr * th.mscale;
+        y[v] = yr * th.mscale;
+        const float nc = fmaf(cs[v], cd[v], -sn[v] * sd[v]);
+        const float ns = fmaf(sn[v], cd[v], cs[v] * sd[v]);
+        cs[v] = nc;
+        sn[v] = ns;
+      }
+      *reinterpret_cast<uint4 *>(out + f0) = pack16<T>(x);
+      *reinterpret_cast<uint4 *>(out + f0 + D / 2) = pack16<T>(y);
+    }
+  }
+}
+
+template <typename T, int D>
+static void launch_shard_batch_t(const ShardBatch &b, const HeadTailMap &map, bool inverse, const RopeTheta &th,
+                                 cudaStream_t s) {
+  const unsigned gx = (unsigned)((map.c + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock);
+  const unsigned gy = (unsigned)(b.n_chunks < 65535 ? b.n_chunks : 65535);
+  dim3 grid(gx, gy);
+  if (inverse) shard_batch_kernel<T, D, true><<<grid, 256, 0, s>>>(b, map, th);
+  else shard_batch_kernel<T, D, false><<<grid, 256, 0, s>>>(b, map, th);
+}
+
+cpattn_status launch_shard_batch(const ShardBatch &b, const Geometry &g, cpattn_dtype dt, bool inverse,
+                                 const cpattn_rope_cfg *cfg, cudaStream_t s) {
+  RopeTheta th;
+  make_rope_theta(g.d, &th, cfg);
+  const HeadTailMap map{g.cp, g.c};
+  if (dt == CPATTN_BF16) {
+    if (g.d == 128) launch_shard_batch_t<__nv_bfloat16, 128>(b, map, inverse, th, s);
+    else launch_shard_batch_t<__nv_bfloat16, 64>(b, map, inverse, th, s);
+  } else {
+    if (g.d == 128) launch_shard_batch_t<float, 128>(b, map, inverse, th, s);
+    else launch_shard_batch_t<float, 64>(b, map, inverse, th, s);
+  }
+  return check_launch(inverse ? "batched unshard kernel" : "batched shard kernel");
+}
+
 // RoPE of a tensor that is already HeadTail-sharded: chunk ch = (head, slot)
 // keeps its rows (nat = perm), its first row sits at natural position
 // chunk_of(slot / 2, slot % 2) * c.

@@ -133,6 +133,27 @@ cpattn_status cpattn_unshard_rope_cfg(const void *src, void *dst, int B, int H, 
  * T entries). Launches nothing. */
 cpattn_status cpattn_shard_index(int T, int cp, int32_t *idx_host);
 
+/* -------------------------------------------- several tensors at once ---
+ * The HeadTail shard (cpattn_shard_batch) or unshard (cpattn_unshard_batch)
+ * of n tensors (1 <= n <= 8) in one launch, e.g. q, k, v, dO before the
+ * attention and o, dq, dk, dv after it ("Claude Logs", 2026-05-16: the chunk-
+ * level HeadTail permutation as one GPU pass):
+ *   src[i], dst[i] : device [B, heads[i], T, d] (natural order in, sharded
+ *                    out for shard; the reverse for unshard), out of place
+ *   rope[i] = 1    : also rotate at the global position, as cpattn_shard_rope
+ *                    / cpattn_unshard_rope (R on the way in, R^T on the way
+ *                    out; cfg as in cpattn_shard_rope_cfg, NULL = standard)
+ * src, dst, heads and rope are host arrays of n entries. The result equals
+ * the n single calls. Errors as cpattn_shard / cpattn_shard_rope; a
+ * destination that overlaps any other buffer of the batch is CPATTN_ERR_ARG;
+ * d must be 64 or 128. */
+cpattn_status cpattn_shard_batch(const void *const *src, void *const *dst, const int *heads, const int *rope, int n,
+                                 int B, int T, int d, int cp, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                 cpattn_stream_t stream);
+cpattn_status cpattn_unshard_batch(const void *const *src, void *const *dst, const int *heads, const int *rope, int n,
+                                   int B, int T, int d, int cp, const cpattn_rope_cfg *cfg, cpattn_dtype dt,
+                                   cpattn_stream_t stream);
+
 /* ------------------------------------------------------------- forward ---
  * Ring attention forward (Claude Logs, 2026-03-20 ring + SDPAMerger;
  * 2026-04-20 global causal masking; 2026-06-17 step shapes).

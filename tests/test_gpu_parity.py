@@ -59,6 +59,30 @@ def test_shard_unshard_bit_exact(dtype, B, H, T, d, cp):
     assert torch.equal(zs.cpu(), x)
 
 
+@pytest.mark.parametrize("dtype,B,H,H_kv,T,d,cp,yarn", [(torch.bfloat16, 1, 4, 2, 1200, 128, 2, False),
+                                                         (torch.float32, 2, 2, 1, 768, 64, 3, True),
+                                                         (torch.bfloat16, 1, 16, 16, 32768, 128, 2, False)])
+def test_shard_batch_equals_single_calls(dtype, B, H, H_kv, T, d, cp, yarn):
+    """cpattn_shard_batch / cpattn_unshard_batch (q, k rotated, v, dO plain; GQA
+    heads) give bit for bit what the single-tensor calls give."""
+    g = torch.Generator().manual_seed(T + H)
+    shapes = [(B, H, T, d), (B, H_kv, T, d), (B, H_kv, T, d), (B, H, T, d)]
+    xs = [(torch.randn(sh, generator=g) * 0.5).to(dtype).cuda() for sh in shapes]
+    rope = [1, 1, 0, 0]
+    cfg = cpattn.RopeCfg(factor=2.0, original_max_position=T // 2) if yarn else None
+    for inverse in (False, True):
+        got = [torch.empty_like(x) for x in xs]
+        cpattn.shard_batch(xs, got, cp, rope=rope, cfg=cfg, inverse=inverse)
+        for x, y, r in zip(xs, got, rope):
+            want = torch.empty_like(x)
+            if r:
+                (cpattn.unshard_rope if inverse else cpattn.shard_rope)(x, want, cp, cfg=cfg)
+            else:
+                (cpattn.unshard if inverse else cpattn.shard)(x, want, cp)
+            torch.cuda.synchronize()
+            assert torch.equal(y, want)
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("B,H,T,d,cp", [(1, 2, 8, 64, 2), (2, 1, 1200, 128, 2), (1, 2, 32768, 128, 2),
                                         (1, 1, 12296, 64, 4)])

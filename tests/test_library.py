@@ -90,6 +90,23 @@ def test_rope_save_and_rotated_validation(lib):
     assert st == cpattn.ERR_SHAPE
 
 
+def test_shard_batch_validation(lib):
+    def call(src, dst, heads, rope, n=None, d=128, T=1024, cp=2):
+        n = len(src) if n is None else n
+        k = max(len(src), 1)
+        return lib.cpattn_shard_batch((ctypes.c_void_p * k)(*src), (ctypes.c_void_p * k)(*dst),
+                                      (ctypes.c_int * k)(*heads), (ctypes.c_int * k)(*rope), n, 1, T, d, cp,
+                                      None, cpattn.BF16, None)
+    assert call(P[:2], P[2:4], [2, 2], [1, 0], n=0) == cpattn.ERR_ARG
+    assert call(P[:2], P[2:4], [2, 2], [1, 0], n=9) == cpattn.ERR_ARG
+    assert call(P[:2], P[2:4], [2, 2], [2, 0]) == cpattn.ERR_ARG                       # rope flag
+    assert call(P[:2], [P[2], P[1]], [2, 2], [1, 0]) == cpattn.ERR_ARG                 # dst 1 is src 1
+    assert "overlaps" in cpattn.cpattn_last_error()
+    assert call(P[:2], P[2:4], [2, 2], [1, 0], d=96) == cpattn.ERR_SHAPE
+    assert call(P[:2], P[2:4], [2, 2], [1, 0], T=1000, cp=3) == cpattn.ERR_SHAPE
+    assert call(P[:2], [P[2] + 8, P[3]], [2, 2], [1, 0]) == cpattn.ERR_ALIGN
+
+
 def test_wait_probe_limit_is_validated(lib):
     for bad in (0, 999, 10 ** 9 + 1):
         assert lib.cpattn_check_wait_timeout(bad, None) == cpattn.ERR_ARG
