@@ -423,7 +423,9 @@ def run_ours(args):
     # the ring path shards q, k, v, dO in one launch and unshards o, dq, dk, dv in one;
     # the Ulysses all-to-all runs per tensor
     n_passes = 4 if P else 1
-    launches_per_step = 2 * n_passes + 1 + 3 + (1 if w.packed else 0)
+    # at d = 128 the paired dQ kernel computes D = rowsum(dO * O) itself: no D launch
+    d_fused = w.d == 128
+    launches_per_step = 2 * n_passes + 1 + (2 if d_fused else 3) + (1 if w.packed else 0)
 
     def new_events():
         evs = {"shard": [], "unshard": []}
@@ -431,7 +433,8 @@ def run_ours(args):
             evs["shard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
             evs["unshard"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
         evs["fwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-        evs["bwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        # backward: start, after the D pass, dK/dV start / end, dQ start / end
+        evs["bwd"] = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
         for e in [x for p in evs["shard"] + evs["unshard"] for x in p] + evs["fwd"] + evs["bwd"]:
             e.record(stream)   # creates the underlying CUDA event so its handle can be passed down
         return evs
@@ -537,8 +540,8 @@ def run_ours(args):
         ker_ms["fwd"] += evs["fwd"][0].elapsed_time(evs["fwd"][1])
         b = evs["bwd"]
         ker_ms["bwd_D"] += b[0].elapsed_time(b[1])
-        ker_ms["bwd_dkdv"] += b[1].elapsed_time(b[2])
-        ker_ms["bwd_dq"] += b[2].elapsed_time(b[3])
+        ker_ms["bwd_dkdv"] += b[2].elapsed_time(b[3])
+        ker_ms["bwd_dq"] += b[4].elapsed_time(b[5])
     ker_ms = {k: v / args.steps for k, v in ker_ms.items()}
 
     # e2e through the same public API, host buffers in and out. Every step
@@ -618,10 +621,12 @@ def run_ours(args):
         "fwd": ("tensor", 2 * unit_flops),
         "bwd_dkdv": ("tensor", 4 * unit_flops),
         "bwd_dq": ("tensor", 1 * unit_flops),     # S and dP recomputation is not credited
-        "bwd_D": ("hbm", 2 * tensor_bytes + w.B * w.H * w.T * 4),
+        "bwd_D": ("hbm", 2 * tensor_bytes + w.B * w.H * w.T * 4),   # dropped below when fused
         "shard": ("hbm", 2 * input_bytes(w, elt)),     # read + write of q, k, v, dO
         "unshard": ("hbm", 2 * input_bytes(w, elt)),   # of o, dq, dk, dv
     }
+    if d_fused:
+        del ker_work["bwd_D"]
     ker_rep = {}
     for name, (bound, work) in ker_work.items():
         t = ker_ms[name] * 1e-3
@@ -660,7 +665,7 @@ def run_ours(args):
                                        "frac": ach / peaks["hbm_gbs"],
                                        "note": "cpattn_merge of 2 fp32 partials, timed outside the step"}
         del o_parts, l_parts, o_m, l_m
-    dom = max(("fwd", "bwd_dkdv", "bwd_dq", "bwd_D"), key=lambda k: ker_ms[k])
+    dom = max((k_ for k_ in ("fwd", "bwd_dkdv", "bwd_dq", "bwd_D") if k_ in ker_work), key=lambda k: ker_ms[k])
     d = ker_rep[dom]
     traffic, traffic_src = ncu_traffic(w.name, dom) if not rope_flag else (None, "in-kernel RoPE build")
     # The timed region lasts well under a second, so the burst peak applies;

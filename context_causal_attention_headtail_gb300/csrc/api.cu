@@ -161,6 +161,11 @@ EncodeTiledFn encode_tiled_fn() {
 
 using namespace cpattn;
 
+static bool uses_tables(int T, int cp) {
+  const long long tpc = ((long long)T / (2 * cp) + 127) / 128;
+  return 2LL * cp * tpc <= kTableTiles;
+}
+
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static cpattn_status check_common(int B, int H, int T, int d, int cp) {
@@ -599,10 +604,18 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
   g.rope_epi = rope_epi;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *D = static_cast<float *>(workspace);
+  // The paired dQ kernel (bf16, d = 128, q and k not rotated in-kernel, tile
+  // tables) computes D = rowsum(dO * O) for its own rows and runs first;
+  // every other path runs the D pass before its kernels.
+  const bool d_in_dq = dt == CPATTN_BF16 && d == 128 && !rope && uses_tables(T, cp);
   trace_record(0, s);
-  st = launch_bwd_preprocess(o, dO, D, (long long)B * H * T, d, dt, s);
+  if (d_in_dq) {
+    g.o_for_D = o;
+  } else {
+    st = launch_bwd_preprocess(o, dO, D, (long long)B * H * T, d, dt, s);
+    if (st != CPATTN_OK) return st;
+  }
   trace_record(1, s);
-  if (st != CPATTN_OK) return st;
   if (dt == CPATTN_F32)
     st = launch_bwd_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                           static_cast<const float *>(v), static_cast<const float *>(o), lse,
@@ -610,16 +623,10 @@ static cpattn_status bwd_impl(const void *q, const void *k, const void *v, const
                           static_cast<float *>(dk), static_cast<float *>(dv), D, g, s);
   else
     st = launch_bwd_bf16(q, k, v, o, lse, dO, dq, dk, dv, D, g, s);
-  trace_record(3, s);
   return st;
 }
 
 // ------------------------------------------- in-kernel RoPE, rotated once
-static bool uses_tables(int T, int cp) {
-  const long long tpc = ((long long)T / (2 * cp) + 127) / 128;
-  return 2LL * cp * tpc <= kTableTiles;
-}
-
 cpattn_status cpattn_fwd_rope_save(const void *q, const void *k, const void *v, void *o, float *lse, void *q_rot,
                                    void *k_rot, int B, int T, int T_valid, int H, int H_kv, int d, int cp,
                                    int causal, const int32_t *doc_lo, const int32_t *doc_hi,

@@ -837,6 +837,12 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
   if (grid > 0x7fffffffLL) return fail(CPATTN_ERR_SHAPE, "too many tiles");
   const unsigned gr = (unsigned)grid;
   cpattn_status st;
+  if (g.o_for_D) {   // the paired dQ kernel computes D (for its rows and for dK/dV) and runs first
+    trace_record(4, s);
+    if ((st = launch_dq_pair_bf16(q, k, v, lse, dO, dq, D, g, s)) != CPATTN_OK) return st;
+    trace_record(5, s);
+  }
+  trace_record(2, s);
   if (g.d == 128)
     st = g.rope ? launch_dkdv2_t<128, true>(mq, mk, mv, mdo, bp, gr, s)
          : g.rope_epi ? launch_dkdv2_t<128, false, true>(mq, mk, mv, mdo, bp, gr, s)
@@ -846,13 +852,17 @@ cpattn_status launch_bwd2_bf16(const void *q, const void *k, const void *v, cons
          : g.rope_epi ? launch_dkdv2_t<64, false, true>(mq, mk, mv, mdo, bp, gr, s)
                       : launch_dkdv2_t<64, false>(mq, mk, mv, mdo, bp, gr, s);
   if (st != CPATTN_OK) return st;
-  trace_record(2, s);
+  trace_record(3, s);
+  if (g.o_for_D) return CPATTN_OK;
   // dQ: CTA pairs with two-SM MMAs at d = 128 when q, k arrive rotated (or
   // without RoPE); the one-CTA pipelined kernel otherwise.
-  if (g.d == 128 && !g.rope) return launch_dq_pair_bf16(q, k, v, lse, dO, dq, D, g, s);
-  if (g.d == 128) return launch_dq2_t<128, true>(mk, mv, bp, gr, s);
-  if (g.rope) return launch_dq2_t<64, true>(mk, mv, bp, gr, s);
-  return g.rope_epi ? launch_dq2_t<64, false, true>(mk, mv, bp, gr, s) : launch_dq2_t<64, false>(mk, mv, bp, gr, s);
+  trace_record(4, s);
+  if (g.d == 128 && !g.rope) st = launch_dq_pair_bf16(q, k, v, lse, dO, dq, D, g, s);
+  else if (g.d == 128) st = launch_dq2_t<128, true>(mk, mv, bp, gr, s);
+  else if (g.rope) st = launch_dq2_t<64, true>(mk, mv, bp, gr, s);
+  else st = g.rope_epi ? launch_dq2_t<64, false, true>(mk, mv, bp, gr, s) : launch_dq2_t<64, false>(mk, mv, bp, gr, s);
+  trace_record(5, s);
+  return st;
 }
 
 }  // namespace cpattn

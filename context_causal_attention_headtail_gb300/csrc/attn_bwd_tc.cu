@@ -581,10 +581,11 @@ cpattn_status launch_bwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dK/dV kernel", smem);
     bp.out0 = dk;
     bp.out1 = dv;
+    trace_record(2, s);
     kern<<<grid / bp.group, threads, smem, s>>>(mq, mk, mv, mdo, bp);   // one CTA per K/V-head key tile
     cpattn_status st = check_launch("tensor-core dK/dV kernel");
     if (st != CPATTN_OK) return st;
-    trace_record(2, s);
+    trace_record(3, s);
   }
   {
     constexpr int smem = DqCfg<D>::SMEM;
@@ -593,8 +594,11 @@ cpattn_status launch_bwd_t(const CUtensorMap &mq, const CUtensorMap &mk, const C
       return fail(CPATTN_ERR_CUDA, "cannot set %d bytes of shared memory for the dQ kernel", smem);
     bp.out0 = dq;
     bp.out1 = nullptr;
+    trace_record(4, s);
     kern<<<grid, threads, smem, s>>>(mq, mk, mv, mdo, bp);
-    return check_launch("tensor-core dQ kernel");
+    cpattn_status st = check_launch("tensor-core dQ kernel");
+    trace_record(5, s);
+    return st;
   }
 }
 

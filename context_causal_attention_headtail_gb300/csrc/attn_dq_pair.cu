@@ -26,6 +26,12 @@
 // dS (bf16 A operand) 64..127, S 128..255, dP 256..383, dQ 384..511.
 // Warps 0-7: softmax (warpgroup h owns key columns [64h, 64h+64)); warp 8:
 // TMA producer and TMEM allocator; warp 9: MMA issuer (leader only).
+// With the forward's O given, warpgroup 1 computes its rows'
+// D = rowsum(dO * O) (the backward's preprocess, "Claude Logs", 2026-03-24)
+// from the dO row it loads into TMEM anyway, after handing dO over, so the
+// O loads overlap the first products; D goes to warpgroup 0 through shared
+// memory (d_ready) and out to the dK/dV kernel, which then runs after this
+// one: no separate D pass.
 #include <math.h>
 
 #include "attn_common.cuh"
@@ -37,7 +43,9 @@ constexpr float kLog2eP = 1.4426950408889634f;
 
 struct DqPairParams {
   const __nv_bfloat16 *dO;   // sharded [BH, T, 128]
-  const float *lse, *D;      // [BH, T]
+  const __nv_bfloat16 *o;    // the forward's O: D = rowsum(dO * O) is computed here and written to D; nullptr: read D
+  const float *lse;          // [BH, T]
+  float *D;                  // [BH, T]
   __nv_bfloat16 *dq;
   int *err;
   int BH, T, T_valid, c, cp, causal, tpc;
@@ -57,10 +65,11 @@ struct DqPairCfg {
   static constexpr int OFF_K = QT;
   static constexpr int OFF_V = OFF_K + NK * KSTAGE;
   static constexpr int OFF_BAR = OFF_V + NV * HT;
-  // q_full, qdo_ready, s_full, s_free, dp_full, dp_free, ds_ready, dq_done, fin, (spare),
+  // q_full, qdo_ready, s_full, s_free, dp_full, dp_free, ds_ready, dq_done, fin, d_ready,
   // k_full[NK], k_empty[NK], v_full[NV], v_empty[NV]
   static constexpr int NBAR = 10 + 2 * NK + 2 * NV;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_DROW = OFF_BAR + NBAR * 8;   // D of the tile's 128 rows (fp32)
+  static constexpr int OFF_MISC = OFF_DROW + 512;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
   static constexpr uint32_t colDO = 0, colDS = 64, colS = 128, colDP = 256, colDQ = 384;
@@ -95,7 +104,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_q_full = bar0, bar_qdo = bar0 + 8, bar_s_full = bar0 + 16, bar_s_free = bar0 + 24,
                  bar_dp_full = bar0 + 32, bar_dp_free = bar0 + 40, bar_ds_ready = bar0 + 48,
-                 bar_dq_done = bar0 + 56, bar_fin = bar0 + 64;
+                 bar_dq_done = bar0 + 56, bar_fin = bar0 + 64, bar_d_ready = bar0 + 72;
+  float *s_drow = reinterpret_cast<float *>(smem + C::OFF_DROW);
   auto bar_k_full = [&](int st) { return bar0 + 80 + 8 * st; };
   auto bar_k_empty = [&](int st) { return bar0 + 80 + 8 * NK + 8 * st; };
   auto bar_v_full = [&](int st) { return bar0 + 80 + 16 * NK + 8 * st; };
@@ -128,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
       const bool by_warps = b == bar_qdo || b == bar_s_free || b == bar_dp_free || b == bar_ds_ready;
-      tc::mbar_init(b, by_warps ? C::kWarpArrivals : 1);
+      tc::mbar_init(b, by_warps ? C::kWarpArrivals : b == bar_d_ready ? 128 : 1);
     }
     abort_flag[0] = 0;
     abort_flag[1] = 0;
@@ -259,29 +269,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y_own + row);
     const float lse2 = valid ? p.lse[grow] * kLog2eP : INFINITY;
-    const float Drow = valid ? p.D[grow] : 0.f;
+    float Drow = (!p.o && valid) ? p.D[grow] : 0.f;   // with O given: computed below
     const uint32_t l_qdo = tc::mapa_shared(bar_qdo, 0), l_s_free = tc::mapa_shared(bar_s_free, 0),
                    l_dp_free = tc::mapa_shared(bar_dp_free, 0), l_ds_ready = tc::mapa_shared(bar_ds_ready, 0);
     auto warp_arrive = [&](uint32_t leader_bar) {   // after this warp's TMEM accesses are complete
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(leader_bar);
     };
-    if (h == 1) {   // this thread's row of dO into TMEM (A operand of dP)
+    if (h == 1) {   // this thread's row of dO into TMEM (A operand of dP), then D
       const uint4 *src = reinterpret_cast<const uint4 *>(p.dO + grow * D);
-#pragma unroll 1
-      for (int cb = 0; cb < D / 64; ++cb) {
-        uint32_t r[32];
+      uint32_t r[D / 64][32];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = valid ? src[cb * 8 + v] : make_uint4(0u, 0u, 0u, 0u);
-          r[4 * v] = x.x; r[4 * v + 1] = x.y; r[4 * v + 2] = x.z; r[4 * v + 3] = x.w;
-        }
-        tc::tmem_st32(t_row + C::colDO + cb * 32, r);
+      for (int v = 0; v < D / 8; ++v) {
+        const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t *rv = &r[v / 8][4 * (v % 8)];
+        rv[0] = x.x; rv[1] = x.y; rv[2] = x.z; rv[3] = x.w;
       }
+#pragma unroll
+      for (int cb = 0; cb < D / 64; ++cb) tc::tmem_st32(t_row + C::colDO + cb * 32, r[cb]);
       tc::tmem_st_wait();
+      tc::tc_fence_before();
+      warp_arrive(l_qdo);
+      if (p.o) {   // D = rowsum(dO * O), fixed summation order (bitwise reproducible)
+        const uint4 *o_src = reinterpret_cast<const uint4 *>(p.o + grow * D);
+        uint64_t acc[4] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f), tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) {
+          const uint4 b = valid ? o_src[v] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t *aw = &r[v / 8][4 * (v % 8)];
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            acc[w] = tc::ffma2(tc::f2(bf16lo_to_f32(aw[w]), bf16hi_to_f32(aw[w])),
+                               tc::f2(bf16lo_to_f32(bw[w]), bf16hi_to_f32(bw[w])), acc[w]);
+        }
+        float a0, a1, a2, a3, a4, a5, a6, a7;
+        tc::unf2(acc[0], a0, a1);
+        tc::unf2(acc[1], a2, a3);
+        tc::unf2(acc[2], a4, a5);
+        tc::unf2(acc[3], a6, a7);
+        Drow = ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+        s_drow[row] = Drow;
+        if (valid) p.D[grow] = Drow;
+        tc::mbar_arrive(bar_d_ready);
+      }
+    } else {
+      tc::tc_fence_before();
+      warp_arrive(l_qdo);
     }
-    tc::tc_fence_before();
-    warp_arrive(l_qdo);
     const float sl2 = p.scale_log2;
     int dlo, dhi;   // this row's document [dlo, dhi)
     doc_bounds_at(p.doc_lo, p.doc_hi, min(q_pos, p.T - 1), p.T, dlo, dhi);
@@ -326,6 +361,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       }
       ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_dp_full, n & 1, wc));
       if (!ok) break;
+      if (n == 0 && p.o && h == 0) {   // D of this row, from warpgroup 1
+        ok = __all_sync(0xffffffffu, tc::mbar_wait(bar_d_ready, 0, wc));
+        if (!ok) break;
+        Drow = s_drow[row];
+      }
       tc::tc_fence_after();
       uint32_t pk[2][16];
       {
@@ -400,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
 }  // namespace
 
 cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, const float *lse,
-                                  const void *dO, void *dq, const float *D, const Geometry &g,
+                                  const void *dO, void *dq, float *D, const Geometry &g,
                                   cudaStream_t s) {
   using C = DqPairCfg;
   if (g.d != C::D || g.rope) return fail(CPATTN_ERR_UNSUPPORTED, "paired dQ kernel: d = 128, q and k not rotated in-kernel");
@@ -413,6 +453,7 @@ cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, c
     return fail(CPATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (is the driver too old?)");
   DqPairParams dp;
   dp.dO = static_cast<const __nv_bfloat16 *>(dO);
+  dp.o = static_cast<const __nv_bfloat16 *>(g.o_for_D);
   dp.lse = lse;
   dp.D = D;
   dp.dq = static_cast<__nv_bfloat16 *>(dq);

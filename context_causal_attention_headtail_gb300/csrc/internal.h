@@ -61,6 +61,10 @@ struct Geometry {
   // Backward on q, k that are already rotated: the kernels rotate nothing and
   // return dq, dk through R^T (rope must be 0 then).
   bool rope_epi = false;
+  // Backward: O of the forward when the dQ kernel computes D = rowsum(dO * O)
+  // itself (and writes it for the dK/dV kernel, which then runs after it);
+  // nullptr when a separate D pass has run.
+  const void *o_for_D = nullptr;
 };
 
 // ---- launchers (one per kernel family), all asynchronous on `s` ----------
@@ -126,7 +130,7 @@ bool make_tile_map(CUtensorMap *m, const void *base, int D, int c, long long n_s
 // dQ of the pipelined backward by CTA pairs (two-SM MMAs), d = 128, inputs
 // already rotated (attn_dq_pair.cu); D = rowsum(dO * O) precomputed.
 cpattn_status launch_dq_pair_bf16(const void *q, const void *k, const void *v, const float *lse,
-                                  const void *dO, void *dq, const float *D, const Geometry &g,
+                                  const void *dO, void *dq, float *D, const Geometry &g,
                                   cudaStream_t s);
 // Up to kBatchMax tensors of one [B, H_i, T, d] layout (H_i per tensor)
 // through the HeadTail shard (or unshard) in one launch; tensor i with rope[i]

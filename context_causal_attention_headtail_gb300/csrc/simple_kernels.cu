@@ -1015,15 +1015,14 @@ cpattn_status launch_bwd_f32(const float *q, const float *k, const float *v, con
   const unsigned kv_blocks = (unsigned)(((long long)g.B * g.Hkv * g.T + 3) / 4);
   RopeTheta th;
   make_rope_theta(g.d, &th, g.rope_cfg);
-  if (g.d == 128) {
-    bwd_dkdv_f32_kernel<128><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
-    trace_record(2, s);
-    bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
-  } else {
-    bwd_dkdv_f32_kernel<64><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
-    trace_record(2, s);
-    bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
-  }
+  trace_record(2, s);
+  if (g.d == 128) bwd_dkdv_f32_kernel<128><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
+  else bwd_dkdv_f32_kernel<64><<<kv_blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dk, dv, g, th);
+  trace_record(3, s);
+  trace_record(4, s);
+  if (g.d == 128) bwd_dq_f32_kernel<128><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
+  else bwd_dq_f32_kernel<64><<<blocks, 128, 0, s>>>(q, k, v, lse, dO, D, dq, g, th);
+  trace_record(5, s);
   return check_launch("fp32 backward kernels");
 }
 

@@ -388,9 +388,11 @@ cpattn_status cpattn_check_wait_timeout(unsigned long long limit_ns, cpattn_stre
  * destroyed here) that later calls from this host thread record on their
  * stream at kernel boundaries:
  *   cpattn_fwd : events[0] before the attention kernel, events[1] after it;
- *   cpattn_bwd : events[0] before the D = rowsum(dO*O) kernel, events[1]
- *                after it, events[2] after the dK/dV kernel, events[3] after
- *                the dQ kernel;
+ *   cpattn_bwd : events[0] before its first kernel, events[1] after the
+ *                D = rowsum(dO*O) pass (right after events[0] where the dQ
+ *                kernel computes D itself), events[2] / events[3] before /
+ *                after the dK/dV kernel, events[4] / events[5] before / after
+ *                the dQ kernel (the dQ kernel runs first when it computes D);
  *   cpattn_shard / cpattn_unshard : events[0] before, events[1] after.
  * A call records only the events it has (n large enough). n = 0 or
  * events = NULL turns tracing off. Errors: CPATTN_ERR_ARG if n < 0 or n > 8. */
