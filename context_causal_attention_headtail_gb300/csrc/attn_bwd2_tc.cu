@@ -415,6 +415,9 @@ struct Dkdv3Cfg {
   static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
 };
 
+// K/V heads per launch-order group of the dK/dV kernel.
+constexpr int kDkdvHeadGroup = 2;
+
 template <int D, bool ROPE, bool EPI = false>
 __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     dkdv2_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -448,10 +451,11 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
-  // K/V head, varying slowest so that the CTAs in flight share its query
-  // heads' Q/dO tiles in L2; its group's query heads are bkv*group + [0, group)
-  const int bkv = blockIdx.x / (2 * cp * tpc);
-  const int g = blockIdx.x % (2 * cp * tpc);
+  // K/V head bkv, a few at a time so that the CTAs in flight share their
+  // query heads' Q/dO tiles in L2, heaviest CTAs first; its group's query
+  // heads are bkv*group + [0, group)
+  int bkv, g;
+  head_group_order<kDkdvHeadGroup>((int)blockIdx.x, 2 * cp * tpc, (int)gridDim.x / (2 * cp * tpc), bkv, g);
   const int kk_chunk = g / tpc;     // earliest keys first: they are seen by the most queries
   const int kt = g % tpc;
   int rk, hk;
@@ -475,6 +479,13 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     abort_flag[0] = 0;
     abort_flag[1] = 0;
     tc::mbar_fence_init();
+    tc::fence_proxy_async_smem();
+    // the stationary K and V tiles load while the tile table is built
+    tc::mbar_arrive_expect_tx(bar_kv_full, 2 * C::TILE);
+    for (int blk = 0; blk < D / 64; ++blk) {
+      tc::tma_load_3d(sK + blk * kTile * 128, &tm_k, bar_kv_full, blk * 64, kt * kTile, k_z);
+      tc::tma_load_3d(sV + blk * kTile * 128, &tm_v, bar_kv_full, blk * 64, kt * kTile, k_z);
+    }
   }
   if (warp == 8) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
@@ -494,18 +505,12 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
   const tc::WaitCtx wc{abort_flag, p.err};
   const tc::WaitCtx drain{abort_flag + 1, p.err};
 
-  const int k_ragged = k_rows < kTile;
   TileInfo t;
 
   if (warp == 8) {
     if (lane == 0) {
       tc::tma_prefetch_desc(&tm_q);
       tc::tma_prefetch_desc(&tm_do);
-      tc::mbar_arrive_expect_tx(bar_kv_full, 2 * C::TILE);
-      for (int blk = 0; blk < D / 64; ++blk) {
-        tc::tma_load_3d(sK + blk * kTile * 128, &tm_k, bar_kv_full, blk * 64, kt * kTile, k_z);
-        tc::tma_load_3d(sV + blk * kTile * 128, &tm_v, bar_kv_full, blk * 64, kt * kTile, k_z);
-      }
     }
     int n = 0, ent = 0, gi = 0;
     while (n < ntot) {

@@ -143,6 +143,21 @@ struct GroupQSchedule {
 // and the slot 2r + half in 11 bits (2*cp <= 2048).
 constexpr int kMaxTiles = kTableTiles;   // entries per CTA (16 KiB of shared memory)
 
+// Launch order of the pipelined kernels: `heads` heads of `per_head` CTAs
+// each (per head, heaviest first), taken in groups of G heads whose CTAs
+// interleave (CTA 0 of every head of the group, then CTA 1, ...). Only a
+// group's operands are live in L2 at a time, and within a group the heaviest
+// CTAs of all its heads start first, so a launch ends on light CTAs instead of
+// on the heavy start of its last head. G = 1: heads one after the other.
+template <int G>
+__device__ __forceinline__ void head_group_order(int idx, int per_head, int heads, int &head, int &unit) {
+  const int h0 = idx / (G * per_head) * G;
+  const int gs = min(G, heads - h0);
+  const int r = idx - h0 * per_head;
+  head = h0 + r % gs;
+  unit = r / gs;
+}
+
 struct TileEntry {
   int pos0;
   uint32_t packed;   // bits 0-9 tile index in chunk, 10-20 slot, 21-27 nvalid-1, 31 need_mask
@@ -197,9 +212,37 @@ struct KvBounds {
 
 // K/V tiles seen by a query tile of rank r (the KvSchedule order: ring steps,
 // head chunk then tail chunk). All 32 lanes call it; returns the tile count.
+// Writes one batch of (up to 32) chunk groups into the table: lane L's group
+// has cnt tiles t0, t0 + 1, ... at tab[off ...]. A few long groups (the usual
+// case: 2cp <= 32 groups of up to c/128 tiles) are written by all lanes, one
+// group after the other; many short ones by their own lane each.
+template <class Make>
+__device__ __forceinline__ void write_groups(TileEntry *tab, int groups, int cnt, int off, int t0, int cpos,
+                                             int slot, int lane, Make make) {
+  if (__reduce_max_sync(0xffffffffu, cnt) > groups) {
+    for (int src = 0; src < groups; ++src) {
+      const int n = __shfl_sync(0xffffffffu, cnt, src);
+      const int o = __shfl_sync(0xffffffffu, off, src);
+      const int s0 = __shfl_sync(0xffffffffu, t0, src);
+      const int sp = __shfl_sync(0xffffffffu, cpos, src);
+      const int ss = __shfl_sync(0xffffffffu, slot, src);
+      for (int i = lane; i < n; i += 32) tab[o + i] = make(sp, s0 + i, ss);
+    }
+  } else {
+    for (int i = 0; i < cnt; ++i) tab[off + i] = make(cpos, t0 + i, slot);
+  }
+}
+
 __device__ inline int build_kv_table(TileEntry *tab, int cp, int c, int r, int causal, int T_valid,
                                      const KvBounds &kb, int lane) {
   const int tpc = (c + kTile - 1) / kTile;
+  auto make = [&](int cpos, int kt, int slot) {
+    const int pos0 = cpos + kt * kTile;
+    const int nv = min(kTile, c - kt * kTile);
+    const int nm = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > kb.qmin) ||
+                   (pos0 < kb.doc_lo_max) || (pos0 + nv > kb.doc_hi_min);
+    return encode_tile(pos0, kt, slot, nv, nm);
+  };
   int base = 0;
   for (int g0 = 0; g0 < 2 * cp; g0 += 32) {
     const int g = g0 + lane;
@@ -214,14 +257,7 @@ __device__ inline int build_kv_table(TileEntry *tab, int cp, int c, int r, int c
       cnt = t1 - t0 + 1;
     }
     const int off = warp_offset(cnt, lane, base);
-    for (int i = 0; i < cnt; ++i) {
-      const int kt = t0 + i;
-      const int pos0 = cpos + kt * kTile;
-      const int nv = min(kTile, c - kt * kTile);
-      const int nm = (nv < kTile) || (pos0 + nv > T_valid) || (causal && pos0 + nv - 1 > kb.qmin) ||
-                     (pos0 < kb.doc_lo_max) || (pos0 + nv > kb.doc_hi_min);
-      tab[off + i] = encode_tile(pos0, kt, slot, nv, nm);
-    }
+    write_groups(tab, min(32, 2 * cp - g0), cnt, off, t0, cpos, slot, lane, make);
   }
   return base;
 }
@@ -240,6 +276,13 @@ struct QBounds {
 __device__ inline int build_q_table(TileEntry *tab, int cp, int c, int j, int causal, int T_valid,
                                     const QBounds &qb, int k_ragged, int lane) {
   const int tpc = (c + kTile - 1) / kTile;
+  auto make = [&](int cpos, int qt, int slot) {
+    const int pos0 = cpos + qt * kTile;
+    const int nv = min(kTile, c - qt * kTile);
+    const int nm = (nv < kTile) || k_ragged || (qb.kmax >= T_valid) || (causal && qb.kmax > pos0) ||
+                   (pos0 < qb.doc_lo_max) || (pos0 + nv > qb.doc_hi_min);
+    return encode_tile(pos0, qt, slot, nv, nm);
+  };
   int base = 0;
   for (int g0 = 0; g0 < 2 * cp; g0 += 32) {
     const int g = g0 + lane;
@@ -254,14 +297,7 @@ __device__ inline int build_q_table(TileEntry *tab, int cp, int c, int j, int ca
       cnt = t1 - t0 + 1;
     }
     const int off = warp_offset(cnt, lane, base);
-    for (int i = 0; i < cnt; ++i) {
-      const int qt = t0 + i;
-      const int pos0 = cpos + qt * kTile;
-      const int nv = min(kTile, c - qt * kTile);
-      const int nm = (nv < kTile) || k_ragged || (qb.kmax >= T_valid) || (causal && qb.kmax > pos0) ||
-                     (pos0 < qb.doc_lo_max) || (pos0 + nv > qb.doc_hi_min);
-      tab[off + i] = encode_tile(pos0, qt, slot, nv, nm);
-    }
+    write_groups(tab, min(32, 2 * cp - g0), cnt, off, t0, cpos, slot, lane, make);
   }
   return base;
 }

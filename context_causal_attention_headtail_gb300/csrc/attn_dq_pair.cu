@@ -77,6 +77,9 @@ struct DqPairCfg {
   static constexpr uint32_t kWarpArrivals = 16;
 };
 
+// Heads per launch-order group of the paired dQ kernel.
+constexpr int kDqHeadGroup = 1;
+
 __device__ __forceinline__ uint32_t cluster_id_x() {
   uint32_t r;
   asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
@@ -119,9 +122,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int ppc = (tpc + 1) / 2;                  // tile pairs per chunk
   const int pair = (int)cluster_id_x();
-  const int bh = pair / (2 * cp * ppc);           // heads vary slowest (K/V tiles shared in L2)
+  int bh, g;   // a few heads at a time (K/V tiles shared in L2), heaviest pairs first
+  head_group_order<kDqHeadGroup>(pair, 2 * cp * ppc, p.BH, bh, g);
   const int bkv = bh / p.group;                   // K/V head of this query head
-  const int g = pair % (2 * cp * ppc);
   const int kq = 2 * cp - 1 - g / ppc;            // latest chunks first: they carry the most work
   const int pq = ppc - 1 - g % ppc;
   int rq, hq;
@@ -146,6 +149,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
   }
   tc::cluster_sync_all();          // both CTAs' barriers exist before either touches the other's
   if (warp == 8) {
+    if (lane == 0) {   // the stationary Q tiles load while the tile table is built
+      if (leader) tc::mbar_arrive_expect_tx(bar_q_full, 2 * C::QT);
+      const uint32_t lq = tc::mapa_shared(bar_q_full, 0);
+      for (int blk = 0; blk < D / 64; ++blk)
+        tc::tma_load_3d_pair(sQ + blk * kTile * 128, &tm_q, lq, blk * 64, y_own, q_z);
+    }
+    __syncwarp();
     tc::tmem_alloc_pair(tc::smem_u32(tmem_slot), 512);
     tc::tmem_relinquish_pair();
     const KvBounds kb = kv_bounds(p.doc_lo, p.doc_hi, p.T, p.T_valid, p.causal, q_pos_pair,
@@ -154,7 +164,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     if (lane == 0) *ntiles_slot = nt;
   }
   tc::tc_fence_before();
-  tc::cluster_sync_all();
+  tc::cluster_arrive();
+  // Warpgroup 1 of the softmax warps: this thread's rows of dO (and of O, for
+  // D) are loaded while the pair waits at the barrier (a release arrival
+  // after the loads would wait for them).
+  const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y_own + (threadIdx.x & 127));
+  const bool row_valid = (int)(threadIdx.x & 127) < q_rows;
+  uint4 pre_do[D / 8], pre_o[D / 8];
+  if (warp >= 4 && warp < 8) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.dO + grow * D);
+#pragma unroll
+    for (int v = 0; v < D / 8; ++v) pre_do[v] = row_valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+    if (p.o) {
+      const uint4 *o_src = reinterpret_cast<const uint4 *>(p.o + grow * D);
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) pre_o[v] = row_valid ? o_src[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  tc::cluster_wait();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = *ntiles_slot;
@@ -169,10 +196,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       tc::tma_prefetch_desc(&tm_kr);
       tc::tma_prefetch_desc(&tm_kc);
       tc::tma_prefetch_desc(&tm_vr);
-      if (leader) tc::mbar_arrive_expect_tx(bar_q_full, 2 * C::QT);
-      const uint32_t lq = tc::mapa_shared(bar_q_full, 0);
-      for (int blk = 0; blk < D / 64; ++blk)
-        tc::tma_load_3d_pair(sQ + blk * kTile * 128, &tm_q, lq, blk * 64, y_own, q_z);
       int nk = 0, nv = 0;   // K / V tiles issued
       while (nk < ntiles && (decode_tile(tab[nk], t), true)) {
         const int z = bkv * 2 * cp + t.slot;
@@ -265,9 +288,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
     const int h = warp >> 2;
     const int row = threadIdx.x & 127;
     const int q_pos = q_pos0 + row;
-    const bool valid = row < q_rows;
+    const bool valid = row_valid;
     const uint32_t t_row = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y_own + row);
     const float lse2 = valid ? p.lse[grow] * kLog2eP : INFINITY;
     float Drow = (!p.o && valid) ? p.D[grow] : 0.f;   // with O given: computed below
     const uint32_t l_qdo = tc::mapa_shared(bar_qdo, 0), l_s_free = tc::mapa_shared(bar_s_free, 0),
@@ -277,11 +299,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       if (lane == 0) tc::mbar_arrive_cluster(leader_bar);
     };
     if (h == 1) {   // this thread's row of dO into TMEM (A operand of dP), then D
-      const uint4 *src = reinterpret_cast<const uint4 *>(p.dO + grow * D);
       uint32_t r[D / 64][32];
 #pragma unroll
       for (int v = 0; v < D / 8; ++v) {
-        const uint4 x = valid ? src[v] : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 x = pre_do[v];
         uint32_t *rv = &r[v / 8][4 * (v % 8)];
         rv[0] = x.x; rv[1] = x.y; rv[2] = x.z; rv[3] = x.w;
       }
@@ -291,11 +312,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(320, 1)
       tc::tc_fence_before();
       warp_arrive(l_qdo);
       if (p.o) {   // D = rowsum(dO * O), fixed summation order (bitwise reproducible)
-        const uint4 *o_src = reinterpret_cast<const uint4 *>(p.o + grow * D);
         uint64_t acc[4] = {tc::f2(0.f, 0.f), tc::f2(0.f, 0.f), tc::f2(0.f, 0.f), tc::f2(0.f, 0.f)};
 #pragma unroll
         for (int v = 0; v < D / 8; ++v) {
-          const uint4 b = valid ? o_src[v] : make_uint4(0u, 0u, 0u, 0u);
+          const uint4 b = pre_o[v];
           const uint32_t *aw = &r[v / 8][4 * (v % 8)];
           const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll

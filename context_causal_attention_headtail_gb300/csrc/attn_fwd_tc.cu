@@ -366,9 +366,12 @@ struct Fwd2Cfg {
   // q_ready, k_ready[NS]
   static constexpr int NBAR = 9 + 5 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
+  static constexpr int SMEM = OFF_MISC + 32 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
 };
+
+// Heads per launch-order group of the paired-tile forward.
+constexpr int kFwdHeadGroup = 4;
 
 template <int D, bool ROPE, bool SAVE = false>
 __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
@@ -401,17 +404,18 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   int *ntiles_slot = reinterpret_cast<int *>(smem + C::OFF_MISC + 12);
-  TileEntry *tab = reinterpret_cast<TileEntry *>(smem + C::OFF_MISC + 16);
+  // first output row of the CTA (kept in shared memory: the epilogue reloads it)
+  volatile long long *row_base = reinterpret_cast<volatile long long *>(smem + C::OFF_MISC + 16);
+  TileEntry *tab = reinterpret_cast<TileEntry *>(smem + C::OFF_MISC + 32);
   constexpr uint32_t colO0 = 256;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cp = p.cp, c = p.c, tpc = p.tpc;
   const int ppc = (tpc + 1) / 2;                  // tile pairs per chunk
-  // Heads vary slowest: the CTAs in flight work on one head (or a few), so
-  // the K/V tiles they all stream stay in L2.
-  const int bh = blockIdx.x / (2 * cp * ppc);
+  // A few heads at a time (their K/V tiles stay in L2), heaviest CTAs first.
+  int bh, g;
+  head_group_order<kFwdHeadGroup>((int)blockIdx.x, 2 * cp * ppc, (int)gridDim.x / (2 * cp * ppc), bh, g);
   const int bkv = bh / p.group;                   // K/V head of this query head
-  const int g = blockIdx.x % (2 * cp * ppc);
   const int kq = 2 * cp - 1 - g / ppc;            // latest chunks first: they carry the most work
   const int pq = ppc - 1 - g % ppc;
   int rq, hq;
@@ -433,7 +437,14 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     }
     abort_flag[0] = 0;
     abort_flag[1] = 0;
+    *row_base = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y0);
     tc::mbar_fence_init();
+    tc::fence_proxy_async_smem();
+    // the stationary Q tiles load while the tile table is built
+    tc::mbar_arrive_expect_tx(bar_q_full, 2 * C::TILE);
+    for (int i = 0; i < 2; ++i)
+      for (int blk = 0; blk < D / 64; ++blk)
+        tc::tma_load_3d(sQ(i) + blk * kTile * 128, &tm_q, bar_q_full, blk * 64, y0 + i * kTile, q_z);
   }
   if (warp == 8) {
     tc::tmem_alloc(tc::smem_u32(tmem_slot), kTmemCols);
@@ -458,10 +469,6 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     if (lane == 0) {
       tc::tma_prefetch_desc(&tm_k);
       tc::tma_prefetch_desc(&tm_v);
-      tc::mbar_arrive_expect_tx(bar_q_full, 2 * C::TILE);
-      for (int i = 0; i < 2; ++i)
-        for (int blk = 0; blk < D / 64; ++blk)
-          tc::tma_load_3d(sQ(i) + blk * kTile * 128, &tm_q, bar_q_full, blk * 64, y0 + i * kTile, q_z);
       int n = 0;
       while (n < ntiles && (decode_tile(tab[n], t), true)) {
         const int st = n % NS;
@@ -705,7 +712,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         tc::tc_fence_after();
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
         const bool valid = prow < q_rows;
-        const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y0 + prow);
+        const long long grow = *row_base + prow;
         uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
 #pragma unroll 1
         for (int cb = 0; cb < D / 32; ++cb) {
@@ -725,7 +732,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         if (valid) p.lse[grow] = l > 0.f ? (m_run + log2f(l)) * 0.693147180559945309f : -INFINITY;
       }
     } else if (ok && prow < q_rows) {   // no key tile at all (rows outside every document)
-      const long long grow = (long long)bh * p.T + (long long)(2 * c * rq + hq * c + y0 + prow);
+      const long long grow = *row_base + prow;
       uint4 *dst = reinterpret_cast<uint4 *>(p.o + grow * D);
 #pragma unroll 1
       for (int v4 = 0; v4 < D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
