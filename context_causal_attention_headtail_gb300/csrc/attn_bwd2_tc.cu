@@ -385,14 +385,17 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 }
 
 // ============================================================== dK / dV
-// Key-stationary. TMEM: S^T 0, dP^T 128, dV 256, dK 256 + D. Warpgroup h owns
-// query columns [64h, 64h+64) and writes its half of P^T (bf16 pairs, 32
-// columns) at 64h and of dS^T at 128 + 64h, over the start of its own
-// halves, so neither warpgroup waits for the other; the dV and dK MMAs read
-// their A operands from the two 32-column pieces. Per query tile n:
-//   S^T(n), dP^T(n) | dV(n) as soon as P^T(n) is in TMEM | S^T(n+1) once dV(n)
-//   has consumed P^T | dK(n) once dS^T(n) is in TMEM | dP^T(n+1) once dK(n)
-// has consumed dS^T.
+// Key-stationary. TMEM: two 128-column regions R0 = [0, 128), R1 = [128, 256)
+// that trade roles from tile to tile, dV at 256, dK at 256 + D. Tile n
+// writes S^T(n) into R(n & 1) and dP^T(n) into the other region. Warpgroup h
+// owns query columns [64h, 64h+64) and packs both of its bf16 operands into
+// its own 64 columns of the S^T region: P^T(n) at 64h, dS^T(n) at 64h + 32
+// (neither warpgroup waits for the other). Per query tile n:
+//   dV(n) as soon as P^T(n) is in TMEM | S^T(n+1), into the region dP^T(n)
+//   occupied, once the softmax has loaded dP^T(n) | dK(n) once dS^T(n) is in
+//   TMEM | dP^T(n+1), into the region that holds P^T(n) and dS^T(n), once
+//   dK(n) (and so dV(n)) has completed.
+// S^T(n+1) therefore waits for a TMEM load, not for dV(n) to complete.
 // With in-kernel RoPE (ROPE), warps 10-11 rotate the K tile once (k_ready)
 // and every Q tile in shared memory (q_ready), and dK leaves through R^T at
 // the key's position.
@@ -406,13 +409,16 @@ struct Dkdv3Cfg {
   static constexpr int OFF_DO = OFF_Q + NS * TILE;
   static constexpr int OFF_LD = OFF_DO + NS * TILE;  // per stage: lse*log2e [128], D [128]
   static constexpr int OFF_BAR = OFF_LD + NS * 1024;
-  // kv_full, fin, s_full, dp_full, k_ready, (spare), p_ready, ds_ready, dv_done, dk_done, qd_full[NS],
+  // kv_full, fin, s_full, dp_full, k_ready, (spare), p_ready, ds_ready, dp_free, dk_done, qd_full[NS],
   // qd_empty[NS], q_ready[NS]
   static constexpr int NBAR = 10 + 3 * NS;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM = OFF_MISC + 16 + kMaxTiles * 8 + 1024;   // misc, tile table, alignment slack
   static_assert(SMEM <= 232448, "over the 227 KiB of shared memory a CTA may opt into");
-  static constexpr uint32_t colS = 0, colDP = 128, colDV = 256, colDK = 256 + D;
+  static constexpr uint32_t colDV = 256, colDK = 256 + D;
+  // the S^T and dP^T regions of query tile n
+  static __device__ __forceinline__ uint32_t colS(int n) { return (n & 1) ? 128u : 0u; }
+  static __device__ __forceinline__ uint32_t colDP(int n) { return (n & 1) ? 0u : 128u; }
 };
 
 // K/V heads per launch-order group of the dK/dV kernel.
@@ -436,7 +442,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
   const uint32_t bar0 = sbase + C::OFF_BAR;
   const uint32_t bar_kv_full = bar0, bar_fin = bar0 + 8, bar_s_full = bar0 + 16, bar_dp_full = bar0 + 24,
                  bar_p_ready = bar0 + 48,
-                 bar_ds_ready = bar0 + 56, bar_dv_done = bar0 + 64, bar_dk_done = bar0 + 72;
+                 bar_ds_ready = bar0 + 56, bar_dp_free = bar0 + 64, bar_dk_done = bar0 + 72;
   auto bar_qd_full = [&](int st) { return bar0 + 80 + 8 * st; };
   auto bar_qd_empty = [&](int st) { return bar0 + 80 + 8 * NS + 8 * st; };
   const uint32_t bar_k_ready = bar0 + 32;
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
     for (int i = 0; i < C::NBAR; ++i) {
       const uint32_t b = bar0 + 8 * i;
       uint32_t cnt = 1;
-      if (b == bar_p_ready || b == bar_ds_ready) cnt = 256;
+      if (b == bar_p_ready || b == bar_ds_ready || b == bar_dp_free) cnt = 256;
       if (b == bar_k_ready) cnt = 64;       // the two rotation warps
       for (int st = 0; st < NS; ++st) {
         if (b == bar_qd_full(st)) cnt = 33;   // expect_tx arrive + 32 producer lanes
@@ -555,18 +561,18 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       constexpr uint32_t idS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t idA = tc::idesc_bf16(128, D, false, true);
       const uint64_t ak0 = tc::kdesc0(sK), av0 = tc::kdesc0(sV);
-      auto issue_s = [&](int st) {
+      auto issue_s = [&](int st, int n) {   // S^T(n) into its tile's region
         const uint64_t bq = tc::kdesc0(sQ(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss_w(tmem + C::colS, ak0 + tc::koff(kTile, kk), bq + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+          tc::mma_ss_w(tmem + C::colS(n), ak0 + tc::koff(kTile, kk), bq + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
         tc::mma_commit_w(bar_s_full);
       };
-      auto issue_dp = [&](int st) {
+      auto issue_dp = [&](int st, int n) {   // dP^T(n)
         const uint64_t bo = tc::kdesc0(sDO(st));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          tc::mma_ss_w(tmem + C::colDP, av0 + tc::koff(kTile, kk), bo + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
+          tc::mma_ss_w(tmem + C::colDP(n), av0 + tc::koff(kTile, kk), bo + tc::koff(kTile, kk), idS, kk > 0 ? 1u : 0u);
         tc::mma_commit_w(bar_dp_full);
       };
       auto wait_all = [&](uint32_t bar, uint32_t par, const tc::WaitCtx &w) {
@@ -577,8 +583,8 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         ok = wait_all(bar_q_use(0), 0, wc);
         if (ok) {
           tc::tc_fence_after();
-          issue_s(0);
-          issue_dp(0);
+          issue_s(0, 0);
+          issue_dp(0, 0);
         }
         for (int n = 0; ok; ++n) {
           const bool more = n + 1 < ntot;
@@ -586,38 +592,38 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
           const uint32_t acc0 = n > 0 ? 1u : 0u;
           if (!(ok = wait_all(bar_p_ready, n & 1, wc))) break;
           tc::tc_fence_after();
-          {   // dV += P^T(n) dO(n)
+          {   // dV += P^T(n) dO(n): P^T of warpgroup h at colS(n) + 64h
             const uint64_t bo = tc::mndesc0(sDO(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts_w(tmem + C::colDV, tmem + C::colS + kk * 8 + (kk >= 4 ? 32 : 0), bo + tc::mnoff(kk), idA,
+              tc::mma_ts_w(tmem + C::colDV, tmem + C::colS(n) + kk * 8 + (kk >= 4 ? 32 : 0), bo + tc::mnoff(kk), idA,
                          kk > 0 ? 1u : acc0);
-            tc::mma_commit_w(bar_dv_done);
           }
           // S^T(n+1) goes ahead of dK(n): it starts the next tile's
           // exponentials, the longest phase of a tile, while dK(n) and
-          // dP^T(n+1) run.
+          // dP^T(n+1) run. It overwrites dP^T(n), which the softmax has loaded.
           if (more) {
             if (!(ok = wait_all(bar_q_use(st1), ((n + 1) / NS) & 1, wc))) break;
-            if (!(ok = wait_all(bar_dv_done, n & 1, wc))) break;   // S^T(n+1) overwrites P^T(n)
+            if (!(ok = wait_all(bar_dp_free, n & 1, wc))) break;
             tc::tc_fence_after();
-            issue_s(st1);
+            issue_s(st1, n + 1);
           }
           if (!(ok = wait_all(bar_ds_ready, n & 1, wc))) break;
           tc::tc_fence_after();
-          {   // dK += dS^T(n) Q(n)
+          {   // dK += dS^T(n) Q(n): dS^T of warpgroup h at colS(n) + 64h + 32
             const uint64_t bq = tc::mndesc0(sQ(st), kTile);
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk)
-              tc::mma_ts_w(tmem + C::colDK, tmem + C::colDP + kk * 8 + (kk >= 4 ? 32 : 0), bq + tc::mnoff(kk), idA,
-                         kk > 0 ? 1u : acc0);
+              tc::mma_ts_w(tmem + C::colDK, tmem + C::colS(n) + 32 + kk * 8 + (kk >= 4 ? 32 : 0), bq + tc::mnoff(kk),
+                         idA, kk > 0 ? 1u : acc0);
             tc::mma_commit_w(bar_dk_done);
             tc::mma_commit_w(bar_qd_empty(st));
           }
           if (!more) break;
-          if (!(ok = wait_all(bar_dk_done, n & 1, wc))) break;     // dP^T(n+1) overwrites dS^T(n)
+          // dP^T(n+1) overwrites P^T(n) and dS^T(n): after dV(n) and dK(n)
+          if (!(ok = wait_all(bar_dk_done, n & 1, wc))) break;
           tc::tc_fence_after();
-          issue_dp(st1);
+          issue_dp(st1, n + 1);
         }
       }
       tc::mma_commit_w(bar_fin);
@@ -680,8 +686,8 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       float pr[64];
       {
         uint32_t r[2][32];
-        tc::tmem_ld32(t_row + C::colS + 64 * h, r[0]);
-        tc::tmem_ld32(t_row + C::colS + 64 * h + 32, r[1]);
+        tc::tmem_ld32(t_row + C::colS(n) + 64 * h, r[0]);
+        tc::tmem_ld32(t_row + C::colS(n) + 64 * h + 32, r[1]);
         tc::tmem_ld_wait();
         const uint64_t sl2x2 = tc::f2(sl2, sl2);
 #pragma unroll
@@ -710,7 +716,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
-        tc::tmem_st16(t_row + C::colS + 64 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colS(n) + 64 * h + cb * 16, pk);   // P^T
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -720,9 +726,11 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       tc::tc_fence_after();
       {
         uint32_t rd[2][32];
-        tc::tmem_ld32(t_row + C::colDP + 64 * h, rd[0]);
-        tc::tmem_ld32(t_row + C::colDP + 64 * h + 32, rd[1]);
+        tc::tmem_ld32(t_row + C::colDP(n) + 64 * h, rd[0]);
+        tc::tmem_ld32(t_row + C::colDP(n) + 64 * h + 32, rd[1]);
         tc::tmem_ld_wait();
+        tc::tc_fence_before();
+        tc::mbar_arrive(bar_dp_free);   // S^T(n+1) may now overwrite dP^T(n)
 #pragma unroll
         for (int q4 = 0; q4 < 16; ++q4) {
           const float4 d4 = tc::lds_f4(sd + 16u * q4);
@@ -742,7 +750,7 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(pr[cb * 32 + 2 * e], pr[cb * 32 + 2 * e + 1]);
-        tc::tmem_st16(t_row + C::colDP + 64 * h + cb * 16, pk);
+        tc::tmem_st16(t_row + C::colS(n) + 64 * h + 32 + cb * 16, pk);   // dS^T
       }
       tc::tmem_st_wait();
       tc::tc_fence_before();
