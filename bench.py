@@ -46,9 +46,9 @@ DEFAULT_WORKLOAD = "window_32k"
 # kernel_digest). A capture whose digest no longer matches the sources in the
 # tree describes an older kernel: the bench then reports the traffic as null.
 NCU_TRAFFIC = {
-    ("window_32k", "fwd"): (0.403631e9 + 0.119130e9, "0366dbae1087"),
-    ("window_32k", "bwd_dkdv"): (0.541742e9 + 0.240560e9, "dde0d5c549b2"),
-    ("window_32k", "bwd_dq"): (0.541444e9 + 0.119546e9, "965dd1d41141"),
+    ("window_32k", "fwd"): (0.499073e9 + 0.119105e9, "84e69669ab08"),
+    ("window_32k", "bwd_dkdv"): (0.544510e9 + 0.238712e9, "58dc38260a84"),
+    ("window_32k", "bwd_dq"): (0.674378e9 + 0.123720e9, "fab329558ecd"),
 }
 CSRC = os.path.join(ROOT, "context_causal_attention_headtail_gb300", "csrc")
 KERNEL_SOURCES = {
