@@ -291,7 +291,7 @@ def _workload_inputs(w):
     return _INPUT_CACHE[w.name]
 
 
-def oracle_sample(w, seconds_target=12.0, max_heads=8):
+def oracle_sample(w, seconds_target=12.0, max_heads=64):
     """Times the float64 oracle on a bounded sample of the workload.
 
     Sample: full forward + backward of whole heads (b=0, h=0,1,...) over the
