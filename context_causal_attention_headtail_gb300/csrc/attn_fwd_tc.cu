@@ -624,10 +624,18 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
       const bool masked = __any_sync(0xffffffffu, lim < kTile || lo > 0);
       const unsigned width = (unsigned)max(lim - lo, 0);
       // The whole row of S comes out of TMEM in one batch of four loads and
-      // one wait; the max and the exponentials then run from registers.
+      // one wait; the exponentials then run from registers. On a tile without
+      // masks the loads also return the row max of their 32 columns
+      // (tcgen05.ld.red); a masked tile takes the max over its kept columns.
       uint32_t r[4][32];
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (masked) {
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tc::tmem_ld32(t_s + cb * 32, r[cb]);
+        for (int cb = 0; cb < 4; ++cb) tc::tmem_ld32(t_s + cb * 32, r[cb]);
+      } else {
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) tc::tmem_ld32_max(t_s + cb * 32, r[cb], mx[cb]);
+      }
       tc::tmem_ld_wait();
       if (masked) {
 #pragma unroll
@@ -635,18 +643,17 @@ __global__ void __launch_bounds__(ROPE ? 384 : 320, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             if ((unsigned)(cb * 32 + e - lo) >= width) r[cb][e] = 0xff800000u;   // -inf
+        // row max over the kept columns (three-input max)
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb)
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            mx[0] = tc::fmax3(mx[0], __uint_as_float(r[cb][e]), __uint_as_float(r[cb][e + 1]));
+            mx[1] = tc::fmax3(mx[1], __uint_as_float(r[cb][e + 2]), __uint_as_float(r[cb][e + 3]));
+            mx[2] = tc::fmax3(mx[2], __uint_as_float(r[cb][e + 4]), __uint_as_float(r[cb][e + 5]));
+            mx[3] = tc::fmax3(mx[3], __uint_as_float(r[cb][e + 6]), __uint_as_float(r[cb][e + 7]));
+          }
       }
-      // row max over the kept columns (three-input max)
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int cb = 0; cb < 4; ++cb)
-#pragma unroll
-        for (int e = 0; e < 32; e += 8) {
-          mx[0] = tc::fmax3(mx[0], __uint_as_float(r[cb][e]), __uint_as_float(r[cb][e + 1]));
-          mx[1] = tc::fmax3(mx[1], __uint_as_float(r[cb][e + 2]), __uint_as_float(r[cb][e + 3]));
-          mx[2] = tc::fmax3(mx[2], __uint_as_float(r[cb][e + 4]), __uint_as_float(r[cb][e + 5]));
-          mx[3] = tc::fmax3(mx[3], __uint_as_float(r[cb][e + 6]), __uint_as_float(r[cb][e + 7]));
-        }
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       const float m_new = fmaxf(m_run, mt * sl2);
       // The running max moves only when it grows by more than 2^8 (the stale
