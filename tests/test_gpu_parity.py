@@ -367,6 +367,9 @@ SMALL_BF16 = [
     make_workload("ragged_c300", B=1, T=1200, T_valid=1195, H=2, d=128, cp=2, rope=True),
     make_workload("noncausal_pad_d128", B=1, T=640, T_valid=600, H=1, d=128, cp=2, causal=False,
                   rope=False),
+    # 15 (b, h) problems: the launch order's last head group is partial in every kernel
+    # (groups of 4 heads in the forward, of 2 K/V heads in dK/dV)
+    make_workload("heads15_pad", B=3, T=768, T_valid=765, H=5, d=128, cp=2, rope=True),
     # grouped K/V heads: GQA with RoPE and padding, MQA, non-causal GQA, ragged chunks
     make_workload("gqa4x2_rope_pad", B=1, T=1024, T_valid=1021, H=4, H_kv=2, d=128, cp=2, rope=True),
     make_workload("mqa_d64_cp3", B=2, T=768, H=3, H_kv=1, d=64, cp=3, rope=False),
